@@ -1,0 +1,470 @@
+#!/usr/bin/env python3
+"""Throughput of one sparse-MoE FFN layer forward (route -> dispatch -> grouped SwiGLU -> combine)
+on GB300, printed as one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+A step is one moe_layer_forward call over one batch of the workload (inputs resident in HBM).
+Between timed steps a 256 MB buffer is written to flush L2. Each step is timed with CUDA events on
+the launching stream; the K steps are bracketed by a barrier and a device synchronize.
+`e2e` is the same metric through moe_layer_forward_host (pinned host x in, host out, copies in
+the timed region). `roofline` is for the step's dominant kernel, timed live with events recorded
+between the layer's phases (moe_layer_forward_profiled). `cpu_baseline` times the fp64 CPU
+oracle on a bounded sample of the same workload. With N > 1 (torchrun) every rank runs an
+independent replica of the layer (the layer has no cross-token exchange): value = N*T / max time.
+`--impl reference` times the oracle alone (rank 0; the other ranks exit) on the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s (bf16, 1 GB300) and achieved fraction of roofline"
+DEFAULT_CONFIG = "fine_grained"
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+LAUNCHES_PER_STEP = 9  # router, histogram, scan, scatter, tile list, gather, gate/up, down, combine
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.path = tempfile.mktemp(prefix="moe_clocks_", suffix=".csv")
+        self.proc = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.fh,
+                stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ------------------------------------------------------------------------------ workload math
+def touched_experts(counts, C):
+    kept = [min(c, C) if C else c for c in counts]
+    return sum(1 for c in kept if c > 0), sum(kept)
+
+
+def layer_roofline(cfg, n_touched, n_kept, t_layer_s, peaks):
+    P_tc = peaks["bf16_tflops"] * 1e12
+    P_hbm = peaks["hbm_gbs"] * 1e9
+    d, f, E, T, k, S = cfg.d, cfg.f, cfg.E, cfg.T, cfg.k, cfg.S
+    F = 6.0 * T * k * d * f
+    F_alg = 6.0 * n_kept * d * f + 6.0 * T * S * d * f + 2.0 * T * d * E
+    B = (n_touched + S) * 3.0 * d * f * 2 + d * E * 2 + 2.0 * T * d * 2
+    t_roof = max(F / P_tc, B / P_hbm)
+    t_alg = max(F_alg / P_tc, B / P_hbm)
+    return {"bound": "tensor" if F / P_tc >= B / P_hbm else "hbm",
+            "F_flop": F, "F_alg_flop": F_alg, "B_bytes": B, "t_roof_us": t_roof * 1e6,
+            "t_layer_us": t_layer_s * 1e6, "frac": t_roof / t_layer_s,
+            "frac_alg": t_alg / t_layer_s}
+
+
+def kernel_work(cfg, phase, n_touched, n_kept):
+    """Algorithmic (flops, bytes) of one launch of a phase, from the config and the routing."""
+    d, f, E, T, k, S = cfg.d, cfg.f, cfg.E, cfg.T, cfg.k, cfg.S
+    rows = n_kept + S * T
+    ne = n_touched + S
+    if phase == "gate_up_gemm":
+        return 4.0 * rows * d * f, ne * 2.0 * d * f * 2 + rows * d * 2.0 + rows * f * 2.0
+    if phase == "down_gemm":
+        return 2.0 * rows * f * d, ne * 1.0 * f * d * 2 + rows * f * 2.0 + rows * d * 2.0
+    if phase == "router":
+        return 2.0 * T * d * E, T * d * 2.0 + d * E * 2.0 + T * k * 8.0
+    if phase == "combine":
+        return 0.0, (n_kept + S * T) * d * 2.0 + T * d * 2.0 + T * k * 4.0
+    if phase == "tiles_gather":
+        return 0.0, 2.0 * n_kept * d * 2
+    if phase == "dispatch":
+        return 0.0, T * k * 4.0 * 4
+    return 0.0, 0.0
+
+
+def roofline_for(phase, flops, nbytes, secs, peaks, sm_mhz):
+    if flops > 0 and phase != "router":
+        ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+        if flops / max(nbytes, 1.0) >= ridge:
+            ach = flops / secs / 1e12
+            return {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"],
+                    "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"]}
+    if phase == "router":
+        # FFMA pipes: 152 SMs x 128 fp32 lanes x 2 flop x clock
+        clk = (sm_mhz or 2070.0) * 1e6
+        peak = 152 * 128 * 2 * clk / 1e12
+        ach = flops / secs / 1e12
+        return {"bound": "alu", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+                "frac": ach / peak}
+    ach = nbytes / secs / 1e9
+    return {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": ach / peaks["hbm_gbs"]}
+
+
+# ------------------------------------------------------------------------------ oracle timing
+def oracle_sample_run(cfg, x_bits, Wg_bits, bias, u, get_expert, get_shared, n_tok, start=0):
+    """Time the fp64 oracle on tokens [start, start + n_tok) taken as one batch."""
+    import numpy as np
+    import oracle as O
+    sl = slice(start, start + n_tok)
+    x64 = O.bf16_bits_to_f64(x_bits[sl])
+    Wg64 = O.bf16_bits_to_f64(Wg_bits)
+    uu = u[sl] if u is not None else None
+    t0 = time.perf_counter()
+    O.layer(x64, Wg64, cfg.k, get_expert, cfg.E, cfg.mode, bias, uu, cfg.tau,
+            cfg.capacity_factor, n_shared=cfg.S, get_shared=get_shared)
+    return time.perf_counter() - t0
+
+
+class WidenedExperts:
+    """bf16 expert weights (host numpy) widened to float64 on first use and kept."""
+
+    def __init__(self, Wg, Wu, Wd):
+        self.src = (Wg, Wu, Wd)
+        self.cache = {}
+
+    def __call__(self, e):
+        import oracle as O
+        if e not in self.cache:
+            self.cache[e] = tuple(O.bf16_bits_to_f64(w[e]) for w in self.src)
+        return self.cache[e]
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def routing_inputs_np(inp):
+    import workloads as W
+    x_bits = W.bf16_bits(inp["x"])
+    Wg_bits = W.bf16_bits(inp["W_g"])
+    bias = inp["bias"].double().cpu().numpy()
+    u = inp["u"].cpu().numpy() if inp.get("u") is not None else None
+    return x_bits, Wg_bits, bias, u
+
+
+def host_weights_np(inp):
+    import workloads as W
+    ex = WidenedExperts(W.bf16_bits(inp["W_gate"]), W.bf16_bits(inp["W_up"]),
+                        W.bf16_bits(inp["W_down"]))
+    sh = None
+    if inp.get("Ws_gate") is not None:
+        sh = WidenedExperts(W.bf16_bits(inp["Ws_gate"]), W.bf16_bits(inp["Ws_up"]),
+                            W.bf16_bits(inp["Ws_down"]))
+    return ex, sh
+
+
+def cpu_baseline(cfg, inp, target_s=15.0):
+    """The oracle as it stands, timed on a bounded sample (tokens 0..n-1 as one batch)."""
+    x_bits, Wg_bits, bias, u = routing_inputs_np(inp)
+    ex, sh = host_weights_np(inp)
+    # warm: widen every expert the sample can touch (model load, not timed), calibrate size
+    t_small = oracle_sample_run(cfg, x_bits, Wg_bits, bias, u, ex, sh, min(8, cfg.T))
+    t_small = oracle_sample_run(cfg, x_bits, Wg_bits, bias, u, ex, sh, min(8, cfg.T))
+    per_tok = max(t_small / min(8, cfg.T), 1e-6)
+    n = int(max(8, min(cfg.T, target_s / per_tok)))
+    if n < cfg.T:
+        for e in range(cfg.E):   # pre-widen all experts the larger sample may hit
+            ex(e)
+    t = oracle_sample_run(cfg, x_bits, Wg_bits, bias, u, ex, sh, n)
+    return {"value": n / t, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"tokens 0..{n - 1} of the workload as one batch ({n} of {cfg.T}); "
+                      f"float64 numpy oracle, expert weights pre-widened; {t:.2f} s",
+            "seconds": t}
+
+
+# ------------------------------------------------------------------------------ reference arm
+def run_reference(args, cfg):
+    import numpy as np
+    import workloads as W
+    inp = W.make_inputs(cfg, weights_device="cpu")
+    x_bits, Wg_bits, bias, u = routing_inputs_np(inp)
+    ex, sh = host_weights_np(inp)
+    budget = 150.0
+    n0 = min(8, cfg.T)
+    oracle_sample_run(cfg, x_bits, Wg_bits, bias, u, ex, sh, n0)          # widen + warm
+    for e in range(cfg.E):
+        ex(e)
+    t0 = oracle_sample_run(cfg, x_bits, Wg_bits, bias, u, ex, sh, n0)
+    per_tok = max(t0 / n0, 1e-6)
+    n = int(max(1, min(cfg.T, budget / (args.steps + args.warmup) / per_tok)))
+    times = []
+    for i in range(args.warmup + args.steps):
+        start = (i * n) % max(1, cfg.T - n + 1)
+        t = oracle_sample_run(cfg, x_bits, Wg_bits, bias, u, ex, sh, n, start)
+        if i >= args.warmup:
+            times.append(t)
+    mean = sum(times) / len(times)
+    value = n / mean
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": mean * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "config": config_dict(cfg),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "kind": "oracle",
+                             "cores": cpu_cores(),
+                             "sample": f"{n} consecutive tokens per step as one batch "
+                                       f"(window moves each step); float64 numpy oracle"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def config_dict(cfg):
+    return {"workload": cfg.name + ": " + cfg.description, "T": cfg.T, "d": cfg.d, "E": cfg.E,
+            "n_shared": cfg.S, "top_k": cfg.k, "d_ff": cfg.f, "mode": cfg.mode, "tau": cfg.tau,
+            "capacity_factor": cfg.capacity_factor, "seed": cfg.seed,
+            "l2": "flushed between timed steps (256 MB write)", "parallelism": "replicas"}
+
+
+# ------------------------------------------------------------------------------ our arm
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", default=DEFAULT_CONFIG)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    import workloads as W
+    cfg = W.CONFIGS[args.config]
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args, cfg)
+        return
+
+    import torch
+    import sparse_moe_layer_route_gb300 as M
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    peaks, peak_src = load_peaks()
+
+    dev = f"cuda:{local}"
+    inp_host = W.make_inputs(cfg, weights_device=dev)
+    inp = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp_host.items()}
+    mc = M.MoeConfig.from_layer(cfg)
+    ws = M.alloc_workspace(mc, dev)
+    # one-time weight preparation (outside the timed layer): fp16 re-encoding of W_down
+    pk0, pk1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    pk0.record()
+    Wd16 = M.packed_f16(inp["W_down"])
+    Wsd16 = M.packed_f16(inp["Ws_down"]) if inp.get("Ws_down") is not None else None
+    pk1.record()
+    torch.cuda.synchronize()
+    pack_ms = pk0.elapsed_time(pk1)
+    weights = M.make_weights(inp["W_g"], inp["bias"], inp["W_gate"], inp["W_up"], inp["W_down"],
+                             inp.get("Ws_gate"), inp.get("Ws_up"), inp.get("Ws_down"), Wd16,
+                             Wsd16)
+    T, k, E, d = cfg.T, cfg.k, cfg.E, cfg.d
+    out = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    slot_pos = torch.empty(T * k, dtype=torch.int32, device=dev)
+    ro = M.make_route_out(counts=counts, slot_pos=slot_pos)
+    u = inp.get("u")
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    def step():
+        M.layer_forward(mc, weights, inp["x"], u, out, ro, ws)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    faults = M.device_status(ws)
+    if faults:
+        raise SystemExit(f"device fault bits {faults:#x} during warm-up")
+
+    # ---- timed region: K steps, L2 flushed between them
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    wall = time.perf_counter() - wall0
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = sum(step_ms) / len(step_ms)
+
+    # ---- phase breakdown through the profiled entry point (same kernels, events in between)
+    n_prof = min(args.steps, 200)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(n_prof)]
+    for i in range(n_prof):
+        flush.fill_(i & 0xFF)
+        M.layer_forward_profiled(mc, weights, inp["x"], u, out, ro, ws, evs[i])
+    torch.cuda.synchronize()
+    phase_ms = {ph: sum(e[j].elapsed_time(e[j + 1]) for e in evs) / n_prof
+                for j, ph in enumerate(M.PROFILE_PHASES)}
+
+    # ---- e2e: host buffers through moe_layer_forward_host
+    x_h = inp_host["x"].pin_memory()
+    u_h = inp_host["u"].pin_memory() if inp_host.get("u") is not None else None
+    out_h = torch.empty((T, d), dtype=torch.bfloat16).pin_memory()
+    n_e2e = min(args.steps, 200)
+    e_s = [torch.cuda.Event(enable_timing=True) for _ in range(n_e2e)]
+    e_e = [torch.cuda.Event(enable_timing=True) for _ in range(n_e2e)]
+    for i in range(3):
+        M.layer_forward_host(mc, weights, x_h, u_h, out_h, ws)
+    torch.cuda.synchronize()
+    for i in range(n_e2e):
+        flush.fill_(i & 0xFF)
+        e_s[i].record(stream)
+        M.layer_forward_host(mc, weights, x_h, u_h, out_h, ws)
+        e_e[i].record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in zip(e_s, e_e)) / n_e2e
+    faults = M.device_status(ws)
+    if faults:
+        raise SystemExit(f"device fault bits {faults:#x} during the timed region")
+    h2d = T * d * 2 + (T * E * 4 if u_h is not None else 0)
+    d2h = T * d * 2
+
+    # ---- max over ranks
+    if dist is not None:
+        tt = torch.tensor([ms, e2e_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms, e2e_ms = tt.tolist()
+
+    counts_h = counts.cpu().tolist()
+    C = M_capacity(cfg)
+    n_touched, n_kept = touched_experts(counts_h, C)
+    lr = layer_roofline(cfg, n_touched, n_kept, ms / 1e3, peaks)
+    sm_mhz = clk["sm_mhz"] if clk else None
+    dom = max(phase_ms, key=phase_ms.get)
+    fl, by = kernel_work(cfg, dom, n_touched, n_kept)
+    roof = roofline_for(dom, fl, by, phase_ms[dom] / 1e3, peaks, sm_mhz)
+    roof["kernel"] = dom
+    roof["traffic"] = None
+    roof["peak_source"] = f"{peak_src} ({'bf16 burst' if roof['unit'] == 'TFLOP/s' else 'copy'})"
+    kernels = {}
+    for ph in M.PROFILE_PHASES:
+        f_, b_ = kernel_work(cfg, ph, n_touched, n_kept)
+        r = roofline_for(ph, f_, b_, phase_ms[ph] / 1e3, peaks, sm_mhz) if phase_ms[ph] > 0 \
+            else {}
+        kernels[ph] = {"us": phase_ms[ph] * 1e3, **{kk: r[kk] for kk in ("bound", "frac")
+                                                    if kk in r}}
+
+    if rank != 0:
+        return
+    line = {"metric": METRIC, "value": world * T / (ms / 1e3), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded inputs, random-init weights)",
+            "config": config_dict(cfg),
+            "roofline": roof,
+            "layer_roofline": lr,
+            "kernels": kernels,
+            "e2e": {"value": world * T / (e2e_ms / 1e3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+            "clocks": clk,
+            "routing": {"experts_hit": n_touched, "kept_slots": n_kept, "capacity": C,
+                        "dropped_slots": T * k - n_kept,
+                        "max_load": max(counts_h), "mean_load": T * k / E},
+            "weight_pack_ms": pack_ms,
+            "wall_s_timed": wall}
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg, inp_host_weights(inp_host, inp))
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def M_capacity(cfg):
+    """Capacity of the config, as the library computes it (None: no limit)."""
+    if cfg.capacity_factor <= 0:
+        return None
+    from fractions import Fraction
+    import numpy as np
+    return math.ceil(Fraction(float(np.float32(cfg.capacity_factor))) * cfg.T * cfg.k / cfg.E)
+
+
+def inp_host_weights(inp_host, inp_dev):
+    """Routing inputs from the host copy; expert weights copied from the device."""
+    out = dict(inp_host)
+    for key in ("W_gate", "W_up", "W_down", "Ws_gate", "Ws_up", "Ws_down"):
+        if inp_dev.get(key) is not None:
+            out[key] = inp_dev[key].cpu()
+    return out
+
+
+if __name__ == "__main__":
+    main()

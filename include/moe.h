@@ -1,0 +1,217 @@
+/*
+ * moe.h -- C ABI of a sparse Mixture-of-Experts FFN layer forward pass on one GB300 (sm_103a).
+ *
+ * The layer (forward only, per token t of x[T, d]):
+ *   1. router logits   logits[t, e] = sum_j x[t, j] * W_g[j, e]          (fp32 accumulation)
+ *   2. selection score s[t, e] = logits                     (MOE_ROUTE_PLAIN)
+ *                                logits + expert_bias[e]    (MOE_ROUTE_BIAS_SELECT)
+ *                                (logits - log(-log u)) / tau   (MOE_ROUTE_GUMBEL)
+ *   3. top-k           the k largest s, ordered by s descending, ties to the lower index
+ *   4. gates           softmax over the k selected logits (PLAIN, BIAS_SELECT) or over the k
+ *                      selected scores s (GUMBEL)
+ *   5. dispatch        per-expert segments, tokens in ascending order; with a capacity C an
+ *                      expert keeps its first C slots (token order) and drops the rest (gate 0)
+ *   6.-8. experts      y = (silu(x W_gate[e]) * (x W_up[e])) W_down[e]   (SwiGLU)
+ *   9. shared experts  z_s = SwiGLU_s(x) for every token, gate 1
+ *  10. combine         out[t] = sum over kept j of gate[t,j] * y(t,j) + sum_s z_s[t]
+ *
+ * Sources (titles of the pages that define the method):
+ *   router, top-k, softmax over top-k, weighted sum of experts:
+ *       "大模型MoE稀疏激活原理与工程实践", §3.1 路由器 (Router code) and §3.2 专家.
+ *   bias-adjusted (aux-loss-free) selection:
+ *       "AI架构演进从稀疏MoE到条件记忆的工程实践", gating-network code (expert bias added to the
+ *       scores that top-k ranks) and its layered-architecture figure (routing, dispatch,
+ *       compute, aggregation layers).
+ *   Gumbel top-k with temperature:
+ *       "GPT-4 Has 1.8 Trillion Parameters. It Uses 2% of Them Per Token", §3.1 门控网络.
+ *   expert capacity and overflow:
+ *       "参数规模与稀疏激活的真相拆解", §3.2 专家容量 (Level 1 hard limit).
+ *   SwiGLU experts: "GPT-4 ... 2% ...", §3.3; shared experts: "V4" rework page, §2.2.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are caller-owned DEVICE memory unless the name ends in _host.
+ *     The library allocates nothing on the device and keeps no per-call global state; every
+ *     scratch buffer lives in the caller's workspace `ws` (see moe_workspace_size).
+ *   - Row-major layouts. bf16 tensors are passed as uint16_t bit patterns.
+ *     x [T, d]; W_g [d, E]; W_gate, W_up [E, d, d_ff]; W_down [E, d_ff, d];
+ *     shared expert weights [S, d, d_ff] / [S, d_ff, d]; expert_bias fp32 [E];
+ *     gumbel_u fp32 [T, E] with values in (0, 1).
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default stream) and
+ *     returns before it completes. Argument errors are detected on the host and returned
+ *     synchronously (nothing is enqueued then). Errors detected by the kernels (an expert index
+ *     outside [0, E), a pipeline wait that timed out) are recorded in a status word inside `ws`
+ *     and read with moe_device_status.
+ *   - Supported sizes: T >= 1; 1 <= E <= 256; 1 <= top_k <= min(E, 8); 0 <= n_shared <= 4;
+ *     d and d_ff multiples of 64; T * (top_k + n_shared) < 2^31. Anything else returns
+ *     MOE_ERR_UNSUPPORTED.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,   /* NULL pointer where one is required, non-positive size, bad mode */
+  MOE_ERR_UNSUPPORTED = 2,   /* sizes outside the supported range above */
+  MOE_ERR_WORKSPACE = 3,     /* ws is NULL, misaligned (needs 256 B) or smaller than required */
+  MOE_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed (launch, tensor-map encode) */
+  MOE_ERR_DEVICE_FAULT = 5   /* a kernel recorded a fault in the status word */
+} moe_status;
+
+typedef enum {
+  MOE_ROUTE_PLAIN = 0,       /* select and gate on the logits */
+  MOE_ROUTE_BIAS_SELECT = 1, /* select on logits + expert_bias, gate on the logits */
+  MOE_ROUTE_GUMBEL = 2       /* select and gate on (logits - log(-log u)) / tau */
+} moe_route_mode;
+
+/* Bits of the device status word (moe_device_status). */
+#define MOE_DEVFAULT_BAD_EXPERT_INDEX 0x1 /* a top-k index outside [0, E) reached dispatch   */
+#define MOE_DEVFAULT_PIPELINE_TIMEOUT 0x2 /* a GEMM pipeline wait exceeded its bound          */
+#define MOE_DEVFAULT_BAD_TILE 0x4         /* the grouped GEMM met an inconsistent tile list   */
+
+typedef struct {
+  int32_t T;                 /* tokens */
+  int32_t d;                 /* hidden size */
+  int32_t E;                 /* routed experts */
+  int32_t top_k;             /* experts per token */
+  int32_t d_ff;              /* expert intermediate size */
+  int32_t n_shared;          /* always-on shared experts (0..4) */
+  int32_t mode;              /* moe_route_mode */
+  float tau;                 /* Gumbel temperature (> 0); ignored otherwise */
+  float capacity_factor;     /* <= 0: no capacity limit; else C = ceil(cf * T * top_k / E) */
+  int32_t capacity_override; /* > 0: use this capacity C instead of the factor */
+} moe_config;
+
+typedef struct {
+  const uint16_t* W_g;        /* [d, E] bf16 */
+  const float* expert_bias;   /* [E] fp32; required for BIAS_SELECT, ignored otherwise */
+  const uint16_t* W_gate;     /* [E, d, d_ff] bf16 */
+  const uint16_t* W_up;       /* [E, d, d_ff] bf16 */
+  const uint16_t* W_down;     /* [E, d_ff, d] bf16 */
+  const uint16_t* Wsh_gate;   /* [S, d, d_ff] bf16, NULL when n_shared == 0 */
+  const uint16_t* Wsh_up;     /* [S, d, d_ff] bf16 */
+  const uint16_t* Wsh_down;   /* [S, d_ff, d] bf16 */
+  /* Optional fp16 re-encodings of W_down / Wsh_down written once by moe_pack_f16. When given,
+   * the down GEMM runs fp16 x fp16 and carries the SwiGLU activations H in fp16 (11-bit
+   * significand) instead of bf16 (8-bit), which keeps the layer output within bf16 rounding of
+   * the exact result; NULL selects the bf16 down path (no packed copy needed). */
+  const uint16_t* W_down_f16;   /* [E, d_ff, d] fp16 or NULL */
+  const uint16_t* Wsh_down_f16; /* [S, d_ff, d] fp16 or NULL (required when W_down_f16 is set
+                                 * and n_shared > 0) */
+} moe_weights;
+
+/* Optional copies of the routing results written by moe_layer_forward (any member may be
+ * NULL; each non-NULL member receives the same content the stand-alone entry point writes). */
+typedef struct {
+  int32_t* topk_idx;   /* [T, k] */
+  float* topk_w;       /* [T, k] */
+  int32_t* counts;     /* [E] */
+  int32_t* offsets;    /* [E + 1] */
+  int32_t* perm_slot;  /* [T * k] */
+  int32_t* slot_pos;   /* [T * k] */
+} moe_route_out;
+
+/* Bytes of workspace every entry point below needs for this config (an upper bound that is
+ * the same for all of them). Host only; no CUDA call. */
+moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes);
+
+/* Clears the device status word at the start of ws (a 4-byte cudaMemsetAsync on stream).
+ * Call once after allocating a workspace; moe_device_status clears it again after reading. */
+moe_status moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Steps 1-4. Router: logits in fp32 (never stored), selection score, top-k, gates.
+ *   x [T, d] bf16, W_g [d, E] bf16, expert_bias [E] fp32 (BIAS_SELECT; else may be NULL),
+ *   gumbel_u [T, E] fp32 (GUMBEL; else may be NULL).
+ *   Writes topk_idx [T, k] int32 (descending score, ties to the lower index) and
+ *   topk_w [T, k] fp32 (gates, summing to 1 per token). */
+moe_status moe_route(const moe_config* cfg, const uint16_t* x, const uint16_t* W_g,
+                     const float* expert_bias, const float* gumbel_u, int32_t* topk_idx,
+                     float* topk_w, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Step 5. Dispatch ("参数规模与稀疏激活的真相拆解", §3.2 for the capacity rule).
+ *   topk_idx [T, k] int32 in [0, E) (an index outside it sets MOE_DEVFAULT_BAD_EXPERT_INDEX and
+ *   that slot is dropped). Slot index = t * k + j.
+ *   Writes counts [E] (slots per expert before the capacity limit), offsets [E + 1]
+ *   (exclusive scan of min(counts, C); offsets[E] = kept slots N), perm_slot [T * k]
+ *   (position -> slot, tokens ascending inside each expert's segment, -1 at positions >= N)
+ *   and slot_pos [T * k] (slot -> position, -1 for a dropped slot). Bit-exact and
+ *   deterministic. */
+moe_status moe_permute(const moe_config* cfg, const int32_t* topk_idx, int32_t* counts,
+                       int32_t* offsets, int32_t* perm_slot, int32_t* slot_pos, void* ws,
+                       size_t ws_bytes, moe_stream_t stream);
+
+/* Steps 6-9. Gathers x rows into expert order, runs the gate/up grouped GEMM with the fused
+ * SiLU*up epilogue and the down grouped GEMM with the fused gate-scale + unpermute epilogue on
+ * the tensor cores, and the shared experts over all T tokens.
+ *   perm_slot, offsets as written by moe_permute; topk_w [T, k] (NULL: every gate is 1).
+ *   Shared weights may be NULL when cfg->n_shared == 0. W_down_f16 / Wsh_down_f16: optional
+ *   fp16 re-encodings from moe_pack_f16 (see moe_weights); NULL selects the bf16 down path.
+ *   Writes y_slot [T * k + S * T, d] fp32: row t*k + j = gate[t,j] * y(t,j) for every kept
+ *   slot (rows of dropped slots are not written); row T*k + s*T + t = z_s[t]. */
+moe_status moe_grouped_ffn(const moe_config* cfg, const uint16_t* x, const int32_t* perm_slot,
+                           const int32_t* offsets, const float* topk_w, const uint16_t* W_gate,
+                           const uint16_t* W_up, const uint16_t* W_down,
+                           const uint16_t* Wsh_gate, const uint16_t* Wsh_up,
+                           const uint16_t* Wsh_down, const uint16_t* W_down_f16,
+                           const uint16_t* Wsh_down_f16, float* y_slot, void* ws,
+                           size_t ws_bytes, moe_stream_t stream);
+
+/* Step 10. out[t] = sum_{j=0..k-1, slot_pos[t*k+j] >= 0} y_slot[t*k+j]
+ *                   + sum_{s=0..S-1} y_slot[T*k + s*T + t],
+ * summed in fp32 in exactly that order and rounded once to bf16. y_slot fp32, out [T, d] bf16. */
+moe_status moe_combine(const moe_config* cfg, const float* y_slot, const int32_t* slot_pos,
+                       uint16_t* out, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* One-time weight preparation (not part of the layer's per-call work): dst[i] = src[i]
+ * re-encoded from bf16 to fp16, round to nearest even, saturating at +-65504. Exact for every
+ * bf16 value whose magnitude lies in [2^-14, 65504]; smaller magnitudes become fp16 subnormals
+ * (absolute error <= 2^-25). n elements; src and dst device pointers, 16-byte aligned. */
+moe_status moe_pack_f16(const uint16_t* src_bf16, uint16_t* dst_f16, size_t n,
+                        moe_stream_t stream);
+
+/* Steps 1-10 on device buffers: route -> permute -> grouped FFN -> combine, all enqueued on
+ * stream with no host synchronisation. gumbel_u is required for GUMBEL. route_out may be NULL. */
+moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const uint16_t* x,
+                             const float* gumbel_u, uint16_t* out, moe_route_out* route_out,
+                             void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* The same layer with the per-call tensors in HOST memory (pinned memory recommended):
+ * copies x_host [T, d] (and gumbel_u_host [T, E] for GUMBEL) to staging buffers inside ws,
+ * runs moe_layer_forward, and copies out back to out_host [T, d], all enqueued on stream.
+ * Weights stay on the device. The caller must synchronise the stream before reading out_host. */
+moe_status moe_layer_forward_host(const moe_config* cfg, const moe_weights* w,
+                                  const uint16_t* x_host, const float* gumbel_u_host,
+                                  uint16_t* out_host, void* ws, size_t ws_bytes,
+                                  moe_stream_t stream);
+
+/* moe_layer_forward that also records CUDA events (cudaEvent_t handles created by the caller)
+ * on stream at the boundaries of its phases, for per-kernel timing:
+ *   events[0] before the router, [1] after the router, [2] after dispatch (histogram, scan,
+ *   scatter), [3] after the tile list + row gather, [4] after the gate/up GEMM, [5] after the
+ *   down GEMM, [6] after the combine.  n_events must be 7. Same results as moe_layer_forward. */
+moe_status moe_layer_forward_profiled(const moe_config* cfg, const moe_weights* w,
+                                      const uint16_t* x, const float* gumbel_u, uint16_t* out,
+                                      moe_route_out* route_out, void* ws, size_t ws_bytes,
+                                      moe_stream_t stream, void* const* events, int n_events);
+
+/* Synchronises stream, reads the device status word of ws into *fault_bits (MOE_DEVFAULT_*),
+ * clears it, and returns MOE_ERR_DEVICE_FAULT if any bit was set, MOE_ERR_CUDA if the stream
+ * reported an error, else MOE_OK. */
+moe_status moe_device_status(void* ws, moe_stream_t stream, int32_t* fault_bits);
+
+/* Static English description of a status code. */
+const char* moe_status_string(moe_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

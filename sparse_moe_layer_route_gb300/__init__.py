@@ -1,0 +1,231 @@
+"""Python binding of libmoe_gb300.so (the C ABI in include/moe.h).
+
+Argument marshalling only: every function forwards torch tensors' device pointers and the
+current CUDA stream to the entry point of the same name; all computation runs in the library's
+CUDA kernels. There is no fallback: if the library is missing the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmoe_gb300.so")
+
+MOE_OK = 0
+STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
+                3: "MOE_ERR_WORKSPACE", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE_FAULT"}
+ROUTE_PLAIN, ROUTE_BIAS_SELECT, ROUTE_GUMBEL = 0, 1, 2
+DEVFAULT_BAD_EXPERT_INDEX, DEVFAULT_PIPELINE_TIMEOUT, DEVFAULT_BAD_TILE = 0x1, 0x2, 0x4
+
+EXPORTS = ("moe_workspace_size", "moe_workspace_init", "moe_route", "moe_permute",
+           "moe_grouped_ffn", "moe_combine", "moe_layer_forward", "moe_layer_forward_profiled",
+           "moe_layer_forward_host", "moe_pack_f16", "moe_device_status", "moe_status_string")
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}")
+
+
+class MoeConfig(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("d", ctypes.c_int32), ("E", ctypes.c_int32),
+                ("top_k", ctypes.c_int32), ("d_ff", ctypes.c_int32),
+                ("n_shared", ctypes.c_int32), ("mode", ctypes.c_int32), ("tau", ctypes.c_float),
+                ("capacity_factor", ctypes.c_float), ("capacity_override", ctypes.c_int32)]
+
+    @classmethod
+    def make(cls, T, d, E, top_k, d_ff, n_shared=0, mode=ROUTE_PLAIN, tau=1.0,
+             capacity_factor=0.0, capacity_override=0):
+        return cls(T, d, E, top_k, d_ff, n_shared, mode, tau, capacity_factor, capacity_override)
+
+    @classmethod
+    def from_layer(cls, c):
+        """From any object with T, d, E, k, f, S, mode, tau, capacity_factor attributes."""
+        return cls.make(c.T, c.d, c.E, c.k, c.f, c.S, c.mode, c.tau, c.capacity_factor)
+
+
+class MoeWeights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("W_g", "expert_bias", "W_gate", "W_up", "W_down", "Wsh_gate", "Wsh_up",
+                 "Wsh_down", "W_down_f16", "Wsh_down_f16")]
+
+
+class MoeRouteOut(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("topk_idx", "topk_w", "counts", "offsets", "perm_slot", "slot_pos")]
+
+
+_lib = None
+
+
+def lib():
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m sparse_moe_layer_route_gb300._build`")
+        L = ctypes.CDLL(LIB_PATH)
+        P, S, I = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+        cfgp = ctypes.POINTER(MoeConfig)
+        L.moe_workspace_size.argtypes = [cfgp, ctypes.POINTER(ctypes.c_size_t)]
+        L.moe_workspace_init.argtypes = [P, S, P]
+        L.moe_route.argtypes = [cfgp, P, P, P, P, P, P, P, S, P]
+        L.moe_permute.argtypes = [cfgp, P, P, P, P, P, P, S, P]
+        L.moe_grouped_ffn.argtypes = [cfgp, P, P, P, P, P, P, P, P, P, P, P, P, P, P, S, P]
+        L.moe_combine.argtypes = [cfgp, P, P, P, P, S, P]
+        L.moe_layer_forward.argtypes = [cfgp, ctypes.POINTER(MoeWeights), P, P, P,
+                                        ctypes.POINTER(MoeRouteOut), P, S, P]
+        L.moe_layer_forward_profiled.argtypes = [cfgp, ctypes.POINTER(MoeWeights), P, P, P,
+                                                 ctypes.POINTER(MoeRouteOut), P, S, P,
+                                                 ctypes.POINTER(ctypes.c_void_p), I]
+        L.moe_layer_forward_host.argtypes = [cfgp, ctypes.POINTER(MoeWeights), P, P, P, P, S, P]
+        L.moe_pack_f16.argtypes = [P, P, S, P]
+        L.moe_device_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_int32)]
+        L.moe_status_string.argtypes = [I]
+        L.moe_status_string.restype = ctypes.c_char_p
+        for name in EXPORTS:
+            if name != "moe_status_string":
+                getattr(L, name).restype = I
+        _lib = L
+    return _lib
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return stream if isinstance(stream, int) else stream.cuda_stream
+
+
+def _check(status, where):
+    if status != MOE_OK:
+        raise MoeError(status, where)
+
+
+def status_string(status: int) -> str:
+    return lib().moe_status_string(status).decode()
+
+
+def workspace_size(cfg: MoeConfig) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().moe_workspace_size(ctypes.byref(cfg), ctypes.byref(n)), "moe_workspace_size")
+    return n.value
+
+
+def alloc_workspace(cfg: MoeConfig, device="cuda"):
+    """A workspace tensor of the right size (torch allocates; 256-byte aligned) with its status
+    word cleared."""
+    import torch
+    ws = torch.empty(workspace_size(cfg), dtype=torch.uint8, device=device)
+    workspace_init(ws)
+    return ws
+
+
+def workspace_init(ws, stream=None):
+    _check(lib().moe_workspace_init(_ptr(ws), ws.numel(), _stream(stream)), "moe_workspace_init")
+
+
+def route(cfg, x, W_g, expert_bias, gumbel_u, topk_idx, topk_w, ws, stream=None):
+    _check(lib().moe_route(ctypes.byref(cfg), _ptr(x), _ptr(W_g), _ptr(expert_bias),
+                           _ptr(gumbel_u), _ptr(topk_idx), _ptr(topk_w), _ptr(ws), ws.numel(),
+                           _stream(stream)), "moe_route")
+
+
+def permute(cfg, topk_idx, counts, offsets, perm_slot, slot_pos, ws, stream=None):
+    _check(lib().moe_permute(ctypes.byref(cfg), _ptr(topk_idx), _ptr(counts), _ptr(offsets),
+                             _ptr(perm_slot), _ptr(slot_pos), _ptr(ws), ws.numel(),
+                             _stream(stream)), "moe_permute")
+
+
+def grouped_ffn(cfg, x, perm_slot, offsets, topk_w, W_gate, W_up, W_down, Wsh_gate, Wsh_up,
+                Wsh_down, y_slot, ws, stream=None, W_down_f16=None, Wsh_down_f16=None):
+    """y_slot: float32 [T*k + S*T, d]."""
+    _check(lib().moe_grouped_ffn(ctypes.byref(cfg), _ptr(x), _ptr(perm_slot), _ptr(offsets),
+                                 _ptr(topk_w), _ptr(W_gate), _ptr(W_up), _ptr(W_down),
+                                 _ptr(Wsh_gate), _ptr(Wsh_up), _ptr(Wsh_down),
+                                 _ptr(W_down_f16), _ptr(Wsh_down_f16), _ptr(y_slot),
+                                 _ptr(ws), ws.numel(), _stream(stream)), "moe_grouped_ffn")
+
+
+def pack_f16(src_bf16, dst_f16, stream=None):
+    """dst (int16/float16 tensor) = fp16 re-encoding of the bf16 tensor src (same shape)."""
+    assert src_bf16.numel() == dst_f16.numel()
+    _check(lib().moe_pack_f16(_ptr(src_bf16), _ptr(dst_f16), src_bf16.numel(), _stream(stream)),
+           "moe_pack_f16")
+
+
+def packed_f16(src_bf16, stream=None):
+    """A new float16 tensor holding the fp16 re-encoding of src (torch allocates)."""
+    import torch
+    dst = torch.empty(src_bf16.shape, dtype=torch.float16, device=src_bf16.device)
+    pack_f16(src_bf16, dst, stream)
+    return dst
+
+
+def combine(cfg, y_slot, slot_pos, out, ws, stream=None):
+    _check(lib().moe_combine(ctypes.byref(cfg), _ptr(y_slot), _ptr(slot_pos), _ptr(out),
+                             _ptr(ws), ws.numel(), _stream(stream)), "moe_combine")
+
+
+def make_weights(W_g, expert_bias, W_gate, W_up, W_down, Wsh_gate=None, Wsh_up=None,
+                 Wsh_down=None, W_down_f16=None, Wsh_down_f16=None) -> MoeWeights:
+    return MoeWeights(*[_ptr(t) for t in (W_g, expert_bias, W_gate, W_up, W_down, Wsh_gate,
+                                           Wsh_up, Wsh_down, W_down_f16, Wsh_down_f16)])
+
+
+def make_route_out(topk_idx=None, topk_w=None, counts=None, offsets=None, perm_slot=None,
+                   slot_pos=None) -> MoeRouteOut:
+    return MoeRouteOut(*[_ptr(t) for t in (topk_idx, topk_w, counts, offsets, perm_slot,
+                                           slot_pos)])
+
+
+def layer_forward(cfg, weights: MoeWeights, x, gumbel_u, out, route_out: MoeRouteOut | None,
+                  ws, stream=None):
+    _check(lib().moe_layer_forward(ctypes.byref(cfg), ctypes.byref(weights), _ptr(x),
+                                   _ptr(gumbel_u), _ptr(out),
+                                   ctypes.byref(route_out) if route_out is not None else None,
+                                   _ptr(ws), ws.numel(), _stream(stream)), "moe_layer_forward")
+
+
+PROFILE_PHASES = ("router", "dispatch", "tiles_gather", "gate_up_gemm", "down_gemm", "combine")
+
+
+def layer_forward_profiled(cfg, weights: MoeWeights, x, gumbel_u, out, route_out, ws, events,
+                           stream=None):
+    """layer_forward recording the 7 torch.cuda.Event objects in `events` at the phase
+    boundaries (PROFILE_PHASES lie between consecutive events)."""
+    for e in events:
+        if not e.cuda_event:      # torch creates the CUDA event on its first record
+            e.record()
+    arr = (ctypes.c_void_p * 7)(*[e.cuda_event for e in events])
+    _check(lib().moe_layer_forward_profiled(
+        ctypes.byref(cfg), ctypes.byref(weights), _ptr(x), _ptr(gumbel_u), _ptr(out),
+        ctypes.byref(route_out) if route_out is not None else None, _ptr(ws), ws.numel(),
+        _stream(stream), arr, 7), "moe_layer_forward_profiled")
+
+
+def layer_forward_host(cfg, weights: MoeWeights, x_host, gumbel_u_host, out_host, ws,
+                       stream=None):
+    _check(lib().moe_layer_forward_host(ctypes.byref(cfg), ctypes.byref(weights), _ptr(x_host),
+                                        _ptr(gumbel_u_host), _ptr(out_host), _ptr(ws),
+                                        ws.numel(), _stream(stream)), "moe_layer_forward_host")
+
+
+def device_status(ws, stream=None) -> int:
+    """Synchronises, returns the device fault bits (and clears them)."""
+    bits = ctypes.c_int32(0)
+    st = lib().moe_device_status(_ptr(ws), _stream(stream), ctypes.byref(bits))
+    if st not in (MOE_OK, 5):
+        raise MoeError(st, "moe_device_status")
+    return bits.value

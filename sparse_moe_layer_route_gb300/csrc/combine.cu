@@ -1,0 +1,111 @@
+// Combine: out[t] = sum over kept j of y_slot[t*k + j] (already gate-scaled by the down GEMM)
+// + sum over shared s of y_slot[T*k + s*T + t], in that fixed order in fp32, one bf16 rounding.
+//
+// Weighted sum of the selected experts' outputs: "大模型MoE稀疏激活原理与工程实践", §3.1
+// (output = sum(weights[i] * expert_i_output)); aggregation layer of
+// "AI架构演进从稀疏MoE到条件记忆的工程实践" (layered-architecture figure), without its residual.
+// Shared experts always added: "V4" rework page, §2.2.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ void add8(float (&acc)[8], const float* p) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  const float4 b = *reinterpret_cast<const float4*>(p + 4);
+  acc[0] += a.x;
+  acc[1] += a.y;
+  acc[2] += a.z;
+  acc[3] += a.w;
+  acc[4] += b.x;
+  acc[5] += b.y;
+  acc[6] += b.z;
+  acc[7] += b.w;
+}
+
+__global__ void __launch_bounds__(kThreads) combine_kernel(const float* __restrict__ y,
+                                                           const int32_t* __restrict__ slot_pos,
+                                                           uint16_t* __restrict__ out, int T,
+                                                           int d, int k, int S) {
+  const int vec_per_row = d / 8;
+  const long long total = (long long)T * vec_per_row;
+  const long long TK = (long long)T * k;
+  for (long long u = (long long)blockIdx.x * kThreads + threadIdx.x; u < total;
+       u += (long long)gridDim.x * kThreads) {
+    const int t = (int)(u / vec_per_row);
+    const int c = (int)(u % vec_per_row);
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int j = 0; j < k; ++j) {
+      const long long slot = (long long)t * k + j;
+      if (slot_pos[slot] >= 0)
+        add8(acc, y + slot * d + 8 * c);
+    }
+    for (int s = 0; s < S; ++s) {
+      const long long row = TK + (long long)s * T + t;
+      add8(acc, y + row * d + 8 * c);
+    }
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+      o[i] = *reinterpret_cast<const uint32_t*>(&b);
+    }
+    *reinterpret_cast<uint4*>(out + (size_t)t * d + 8 * c) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// dst[i] = fp16(bf16 src[i]), round to nearest even, saturating; 8 elements per thread.
+__global__ void __launch_bounds__(kThreads) pack_f16_kernel(const uint16_t* __restrict__ src,
+                                                            uint16_t* __restrict__ dst, size_t n) {
+  const size_t n8 = n / 8;
+  for (size_t i = (size_t)blockIdx.x * kThreads + threadIdx.x; i < n8;
+       i += (size_t)gridDim.x * kThreads) {
+    const uint4 v = reinterpret_cast<const uint4*>(src)[i];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float lo = __uint_as_float(w[j] << 16), hi = __uint_as_float(w[j] & 0xFFFF0000u);
+      asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(o[j]) : "f"(hi), "f"(lo));
+    }
+    reinterpret_cast<uint4*>(dst)[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  // tail (n not a multiple of 8)
+  const size_t t = n8 * 8 + (size_t)blockIdx.x * kThreads + threadIdx.x;
+  if (blockIdx.x == 0 && t < n) {
+    const float v = __uint_as_float(((uint32_t)src[t]) << 16);
+    uint32_t o;
+    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(o) : "f"(0.0f), "f"(v));
+    dst[t] = (uint16_t)(o & 0xFFFFu);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_pack_f16(const uint16_t* src, uint16_t* dst, size_t n, cudaStream_t st) {
+  long long grid = (long long)((n / 8 + kThreads - 1) / kThreads);
+  const long long cap = (long long)num_sms() * 32;
+  if (grid > cap) grid = cap;
+  if (grid < 1) grid = 1;
+  pack_f16_kernel<<<(unsigned)grid, kThreads, 0, st>>>(src, dst, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const Shape& s, const float* y, const int32_t* slot_pos,
+                           uint16_t* out, cudaStream_t st) {
+  const long long total = (long long)s.T * (s.d / 8);
+  long long grid = (total + kThreads - 1) / kThreads;
+  const long long cap = (long long)num_sms() * 16;
+  if (grid > cap) grid = cap;
+  if (grid < 1) grid = 1;
+  combine_kernel<<<(unsigned)grid, kThreads, 0, st>>>(y, slot_pos, out, s.T, s.d, s.k, s.S);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,464 @@
+// Grouped GEMM over variable-length expert segments on the 5th-generation tensor cores.
+//
+//   gate/up pass (MODE 0):  H[p, n] = silu(sum_k A[p,k] W_gate[e][k,n]) * (sum_k A[p,k] W_up[e][k,n])
+//   down pass    (MODE 1):  Y[row(p), n] = gate(p) * sum_k H[p,k] W_down[e][k,n]     (Y in fp32)
+// H is stored in fp16 (HF16, with an fp16 copy of W_down so both down operands share the type)
+// or in bf16.
+//
+// Expert SwiGLU: "GPT-4 Has 1.8 Trillion Parameters. It Uses 2% of Them Per Token", §3.3, and
+// "大模型MoE稀疏激活原理与工程实践", §3.2 (uniform d -> d_ff -> d experts). Running every
+// expert's rows as one batched tensor-core matmul is the "expert fusion" of the same page's §4.2;
+// the gate-scaled unpermuting epilogue replaces the separate gather/scatter/weighted-sum steps that
+// "AI架构演进从稀疏MoE到条件记忆的工程实践" fuses into one kernel.
+//
+// Design (one CTA per SM, persistent):
+//   warp 0  TMA producer: A tile [128 rows x 64 k] (K-major, 128-byte swizzle) and NCH weight
+//           chunks [64 k x 64 n] (N-major, 128-byte swizzle) per stage, straight from the
+//           row-major [E, K, N] weight tensors (no repack).
+//   warp 1  MMA issuer: tcgen05.mma kind::f16, M=128, N=64*NCH, K=16 per instruction, fp32
+//           accumulators in TMEM, two accumulator buffers so the epilogue of tile i overlaps the
+//           main loop of tile i+1.
+//   warp 2  TMEM allocator.
+//   warps 4-7 epilogue: tcgen05.ld 32 columns at a time, fused SiLU*up (MODE 0) or gate scale and
+//           scatter to slot order (MODE 1), 16-byte stores.
+// Work units: (row tile from the device-written tile list) x (column tile), row tile fastest so
+// CTAs running at the same time share weight tiles through L2. The host never reads the tile
+// count. Every mbarrier wait is bounded (MOE_DEVFAULT_PIPELINE_TIMEOUT on expiry).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <cstdint>
+#include <mutex>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;
+constexpr int kChunkN = 64;
+constexpr int kABytes = kBM * kBK * 2;             // 16 KB
+constexpr int kChunkBytes = kBK * kChunkN * 2;     // 8 KB
+constexpr int kThreads = 256;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s per wait
+
+template <int NCH>
+struct Cfg {
+  static constexpr int BN = NCH * kChunkN;                  // MMA N
+  static constexpr int kStageBytes = kABytes + NCH * kChunkBytes;
+  static constexpr int kStages = (200 * 1024 / kStageBytes) > 8 ? 8 : (200 * 1024 / kStageBytes);
+  static constexpr int kTmemCols = 2 * BN;                  // two accumulators
+  static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+};
+
+struct GemmArgs {
+  const TileEntry* tiles;
+  const Meta* meta;
+  int n_ntiles;       // column tiles
+  int k_blocks;       // K / 64
+  int E;              // routed experts; tile.expert >= E is shared expert (expert - E)
+  void* out;          // H (MODE 0: 16-bit) or Y (MODE 1: fp32)
+  long long out_ld;   // elements per output row
+  const int32_t* perm_slot;  // MODE 1
+  const float* topk_w;       // MODE 1 (NULL: gate 1)
+  int* status;
+};
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&b);
+}
+
+// fp16x2, round to nearest even, saturating to +-65504 (no infinities from large activations)
+__device__ __forceinline__ uint32_t pack_f16x2_sat(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+template <int MODE, int NCH, bool HF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA_routed,
+                        const __grid_constant__ CUtensorMap tmA_shared,
+                        const __grid_constant__ CUtensorMap tmB0_routed,
+                        const __grid_constant__ CUtensorMap tmB1_routed,
+                        const __grid_constant__ CUtensorMap tmB0_shared,
+                        const __grid_constant__ CUtensorMap tmB1_shared, const GemmArgs a) {
+  using C = Cfg<NCH>;
+  constexpr int BN = C::BN;
+  constexpr int STAGES = C::kStages;
+  // gate/up multiplies bf16 x bf16; down multiplies H x W_down in fp16 (HF16) or bf16
+  constexpr uint32_t IDESC =
+      ptx::idesc_f16kind_f32(kBM, BN, 0, 1, (MODE == 1 && HF16) ? 0u : 1u);
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* const gbase = smem_raw + (base - raw);
+  const uint32_t bar0 = base + STAGES * C::kStageBytes;
+  // barrier addresses
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+  const uint32_t mma_done_bar = bar0 + 8u * (2 * STAGES + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + STAGES * C::kStageBytes +
+                                                    8 * (2 * STAGES + 5));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(full_bar(s), 1);
+      ptx::mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(tfull_bar(b), 1);
+      ptx::mbar_init(tempty_bar(b), 4);
+    }
+    ptx::mbar_init(mma_done_bar, 1);
+    *abort_flag = 0;
+    ptx::fence_mbarrier_init();
+    ptx::prefetch_tmap(&tmA_routed);
+    ptx::prefetch_tmap(&tmB0_routed);
+    if (MODE == 0) ptx::prefetch_tmap(&tmB1_routed);
+  }
+  if (warp == 2) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), C::kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int n_mt = a.meta->n_tiles;
+  const long long total = (long long)n_mt * a.n_ntiles;
+
+  if (warp == 0) {
+    if (lane == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t issued_mask = 0, last_parity = 0;  // per stage: issued at least once / its parity
+    bool ok = true;
+    for (long long w = blockIdx.x; w < total && ok; w += gridDim.x) {
+      const TileEntry te = a.tiles[w % n_mt];
+      const int nt = (int)(w / n_mt);
+      const bool shared = te.expert >= a.E;
+      const int ex = shared ? te.expert - a.E : te.expert;
+      const CUtensorMap* tA = shared ? &tmA_shared : &tmA_routed;
+      const CUtensorMap* tB0 = shared ? &tmB0_shared : &tmB0_routed;
+      const CUtensorMap* tB1 = shared ? &tmB1_shared : &tmB1_routed;
+      const int arow = (MODE == 0) ? te.arow0 : te.row0;
+      for (int kb = 0; kb < a.k_blocks; ++kb) {
+        if (!ptx::mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, a.status,
+                                    MOE_DEVFAULT_PIPELINE_TIMEOUT, kWaitLimitNs)) {
+          ok = false;
+          break;
+        }
+        const uint32_t sA = base + stage * C::kStageBytes;
+        const uint32_t sB = sA + kABytes;
+        const uint32_t fb = full_bar(stage);
+        ptx::mbar_arrive_expect_tx(fb, C::kStageBytes);
+        ptx::tma_load_2d(sA, tA, fb, kb * kBK, arow);
+        if (MODE == 0) {
+          // chunks [0, NCH/2): gate columns; [NCH/2, NCH): up columns of the same n range
+#pragma unroll
+          for (int c = 0; c < NCH / 2; ++c) {
+            const int n = nt * (BN / 2) + c * kChunkN;
+            ptx::tma_load_3d(sB + c * kChunkBytes, tB0, fb, n, kb * kBK, ex);
+            ptx::tma_load_3d(sB + (c + NCH / 2) * kChunkBytes, tB1, fb, n, kb * kBK, ex);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < NCH; ++c)
+            ptx::tma_load_3d(sB + c * kChunkBytes, tB0, fb, nt * BN + c * kChunkN, kb * kBK, ex);
+        }
+        issued_mask |= 1u << stage;
+        last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    // never leave while a copy into this CTA's shared memory may still be in flight
+    for (int s = 0; s < STAGES; ++s)
+      if (issued_mask & (1u << s)) {
+        volatile int no_abort = 0;
+        ptx::mbar_wait_bounded(full_bar(s), (last_parity >> s) & 1u, &no_abort, a.status,
+                               MOE_DEVFAULT_PIPELINE_TIMEOUT, kWaitLimitNs / 4);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+    // ------------------------------------------------------------------ MMA issuer
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (long long w = blockIdx.x; w < total && ok; w += gridDim.x) {
+      if (!ptx::mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag, a.status,
+                                  MOE_DEVFAULT_PIPELINE_TIMEOUT, kWaitLimitNs))
+        break;
+      ptx::tc_fence_after();
+      const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+      for (int kb = 0; kb < a.k_blocks; ++kb) {
+        if (!ptx::mbar_wait_bounded(full_bar(stage), phase, abort_flag, a.status,
+                                    MOE_DEVFAULT_PIPELINE_TIMEOUT, kWaitLimitNs)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t sA = base + stage * C::kStageBytes;
+        const uint32_t sB = sA + kABytes;
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk) {
+          // A: K-major, 128 B rows, 8-row groups 1024 B apart; K step of 16 = +32 B in the row.
+          const uint64_t adesc = ptx::smem_desc_sw128(sA + kk * 32, 16, 1024);
+          // B: N-major, 64-column chunks 8 KB apart (LBO), 8-row k groups 1024 B apart (SBO);
+          // K step of 16 rows = +2048 B.
+          const uint64_t bdesc = ptx::smem_desc_sw128(sB + kk * 2048, kChunkBytes, 1024);
+          ptx::umma_f16(d_tmem, adesc, bdesc, IDESC, (kb | kk) != 0 ? 1u : 0u);
+        }
+        ptx::umma_commit(empty_bar(stage));
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      ptx::umma_commit(tfull_bar(acc));
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    // all MMAs issued by this thread have finished before TMEM is released
+    ptx::umma_commit(mma_done_bar);
+    volatile int no_abort = 0;
+    ptx::mbar_wait_bounded(mma_done_bar, 0, &no_abort, a.status, MOE_DEVFAULT_PIPELINE_TIMEOUT,
+                           kWaitLimitNs / 4);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------------ epilogue
+    const int q = warp - 4;  // TMEM lanes [32q, 32q + 32)
+    const int row_in_tile = 32 * q + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (long long w = blockIdx.x; w < total; w += gridDim.x) {
+      const TileEntry te = a.tiles[w % n_mt];
+      const int nt = (int)(w / n_mt);
+      if (!ptx::mbar_wait_bounded(tfull_bar(acc), acc_phase, abort_flag, a.status,
+                                  MOE_DEVFAULT_PIPELINE_TIMEOUT, kWaitLimitNs))
+        break;
+      ptx::tc_fence_after();
+      const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN);
+      const bool valid = row_in_tile < te.rows;
+      const long long p = (long long)te.row0 + row_in_tile;
+      if (MODE == 0) {
+        uint16_t* dst = static_cast<uint16_t*>(a.out) + p * a.out_ld + (long long)nt * (BN / 2);
+#pragma unroll 1
+        for (int c = 0; c < BN / 2 / 32; ++c) {
+          uint32_t g[32], u[32];
+          ptx::tmem_ld_32x32b_x32(taddr + c * 32, g);
+          ptx::tmem_ld_32x32b_x32(taddr + BN / 2 + c * 32, u);
+          ptx::tmem_wait_ld();
+          uint32_t hv[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
+            const float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
+            const float h0 = g0 / (1.0f + __expf(-g0)) * u0;
+            const float h1 = g1 / (1.0f + __expf(-g1)) * u1;
+            hv[i] = HF16 ? pack_f16x2_sat(h0, h1) : pack_bf16x2(h0, h1);
+          }
+          if (valid) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              d4[i] = make_uint4(hv[4 * i], hv[4 * i + 1], hv[4 * i + 2], hv[4 * i + 3]);
+          }
+        }
+      } else {
+        long long orow = p;
+        float gate = 1.0f;
+        if (valid && te.expert < a.E) {
+          const int slot = a.perm_slot[p];
+          orow = slot;
+          if (a.topk_w != nullptr) gate = a.topk_w[slot];
+        }
+        float* dst = static_cast<float*>(a.out) + orow * a.out_ld + (long long)nt * BN;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t v[32];
+          ptx::tmem_ld_32x32b_x32(taddr + c * 32, v);
+          ptx::tmem_wait_ld();
+          if (valid) {
+            float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              d4[i] = make_float4(gate * __uint_as_float(v[4 * i]),
+                                  gate * __uint_as_float(v[4 * i + 1]),
+                                  gate * __uint_as_float(v[4 * i + 2]),
+                                  gate * __uint_as_float(v[4 * i + 3]));
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(tempty_bar(acc));
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = []() {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return (PFN_cuTensorMapEncodeTiled_v12000) nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+// 2-D map over a row-major [rows, K] 16-bit matrix; box = 64 (K) x 128 (rows), 128-byte swizzle.
+bool make_map_a(CUtensorMap* m, const void* ptr, long long rows, long long K,
+                CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
+  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  const cuuint32_t box[2] = {kBK, kBM};
+  const cuuint32_t estr[2] = {1, 1};
+  return encode_fn()(m, dt, 2, const_cast<void*>(ptr), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D map over row-major [n_exp, K, N] 16-bit weights; box = 64 (N) x 64 (K) x 1, 128-byte swizzle.
+bool make_map_b(CUtensorMap* m, const void* ptr, long long n_exp, long long K, long long N,
+                CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
+  const cuuint64_t dims[3] = {(cuuint64_t)N, (cuuint64_t)K, (cuuint64_t)n_exp};
+  const cuuint64_t strides[2] = {(cuuint64_t)N * 2, (cuuint64_t)K * N * 2};
+  const cuuint32_t box[3] = {kChunkN, kBK, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return encode_fn()(m, dt, 3, const_cast<void*>(ptr), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int MODE, int NCH, bool HF16>
+cudaError_t launch_one(const CUtensorMap (&maps)[6], const GemmArgs& args, cudaStream_t st) {
+  using C = Cfg<NCH>;
+  auto kern = grouped_gemm_kernel<MODE, NCH, HF16>;
+  cudaError_t err =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (err != cudaSuccess) return err;
+  kern<<<num_sms(), kThreads, C::kSmemBytes, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4],
+                                                   maps[5], args);
+  return cudaGetLastError();
+}
+
+template <bool HF16>
+cudaError_t launch_pair(const Shape& s, const FfnPtrs& p, cudaStream_t st, cudaEvent_t ev_mid) {
+  const long long rows = s.rows;
+  const bool has_shared = s.S > 0;
+  constexpr CUtensorMapDataType kHType =
+      HF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const uint16_t* Wd = HF16 ? p.W_down_f16 : p.W_down;
+  const uint16_t* Wsd = HF16 ? p.Wsh_down_f16 : p.Wsh_down;
+  // ---- gate/up: A = gathered rows (routed) or x (shared); B = W_gate / W_up
+  CUtensorMap m0[6];
+  bool ok = make_map_a(&m0[0], p.xp, s.TK, s.d) && make_map_a(&m0[1], p.x, s.T, s.d) &&
+            make_map_b(&m0[2], p.W_gate, s.E, s.d, s.f) &&
+            make_map_b(&m0[3], p.W_up, s.E, s.d, s.f);
+  if (has_shared)
+    ok = ok && make_map_b(&m0[4], p.Wsh_gate, s.S, s.d, s.f) &&
+         make_map_b(&m0[5], p.Wsh_up, s.S, s.d, s.f);
+  else {
+    m0[4] = m0[2];
+    m0[5] = m0[3];
+  }
+  if (!ok) return cudaErrorInvalidValue;
+  GemmArgs g{};
+  g.tiles = p.tiles;
+  g.meta = p.meta;
+  g.E = s.E;
+  g.status = p.status;
+  g.k_blocks = s.d / kBK;
+  g.out = p.h;
+  g.out_ld = s.f;
+  cudaError_t err;
+  if (s.f % 128 == 0) {
+    g.n_ntiles = s.f / 128;
+    err = launch_one<0, 4, HF16>(m0, g, st);
+  } else {
+    g.n_ntiles = s.f / 64;
+    err = launch_one<0, 2, HF16>(m0, g, st);
+  }
+  if (err != cudaSuccess) return err;
+  if (ev_mid != nullptr && (err = cudaEventRecord(ev_mid, st)) != cudaSuccess) return err;
+
+  // ---- down: A = H rows; B = W_down; epilogue scales by the gate and writes slot order (fp32)
+  CUtensorMap m1[6];
+  ok = make_map_a(&m1[0], p.h, rows, s.f, kHType) && make_map_b(&m1[2], Wd, s.E, s.f, s.d, kHType);
+  if (has_shared)
+    ok = ok && make_map_b(&m1[4], Wsd, s.S, s.f, s.d, kHType);
+  else
+    m1[4] = m1[2];
+  if (!ok) return cudaErrorInvalidValue;
+  m1[1] = m1[0];
+  m1[3] = m1[2];
+  m1[5] = m1[4];
+  GemmArgs g1 = g;
+  g1.k_blocks = s.f / kBK;
+  g1.out = p.y;
+  g1.out_ld = s.d;
+  g1.perm_slot = p.perm_slot;
+  g1.topk_w = p.topk_w;
+  if (s.d % 256 == 0) {
+    g1.n_ntiles = s.d / 256;
+    return launch_one<1, 4, HF16>(m1, g1, st);
+  } else if (s.d % 128 == 0) {
+    g1.n_ntiles = s.d / 128;
+    return launch_one<1, 2, HF16>(m1, g1, st);
+  }
+  g1.n_ntiles = s.d / 64;
+  return launch_one<1, 1, HF16>(m1, g1, st);
+}
+
+}  // namespace
+
+cudaError_t launch_grouped_ffn(const Shape& s, const FfnPtrs& p, cudaStream_t st,
+                               cudaEvent_t ev_mid) {
+  if (encode_fn() == nullptr) return cudaErrorNotSupported;
+  if (p.W_down_f16 != nullptr) return launch_pair<true>(s, p, st, ev_mid);
+  return launch_pair<false>(s, p, st, ev_mid);
+}
+
+}  // namespace moe

@@ -1,0 +1,91 @@
+// Internal launch interface between the C-ABI layer (moe_api.cu) and the kernels.
+#pragma once
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+constexpr int kTileM = 128;        // rows per grouped-GEMM tile (one UMMA M=128 accumulator)
+constexpr int kPermuteBlock = 256; // slots per dispatch block
+
+struct Shape {
+  int T, d, E, k, f, S, mode;
+  float tau;
+  int C;          // capacity, or INT32_MAX for no limit
+  long long TK;   // T * k
+  long long rows; // rows of the expert-ordered buffers: T * k + S * T
+  int n_pblk;     // dispatch blocks = ceil(T*k / kPermuteBlock)
+  int max_tiles;  // upper bound on grouped-GEMM row tiles
+};
+
+// One grouped-GEMM row tile: rows [row0, row0 + rows) of the expert-ordered buffers belong to
+// `expert` (E + s for shared expert s); the A operand of the gate/up GEMM starts at row `arow0`
+// of its source (the gathered rows for routed experts, x itself for shared ones).
+struct TileEntry {
+  int expert;
+  int row0;
+  int rows;
+  int arow0;
+};
+
+// Meta block inside the workspace (device ints).
+struct Meta {
+  int n_tiles;   // row tiles written by the dispatch scan
+  int n_kept;    // N = kept routed slots
+  int pad[62];
+};
+
+// Offsets of every buffer carved from the caller's workspace (bytes, 256-aligned).
+struct WsLayout {
+  size_t status, meta, topk_idx, topk_w, counts, offsets, perm_slot, slot_pos;
+  size_t blk_hist, blk_base, tiles, xp, h, y, x_stage, u_stage, out_stage;
+  size_t total;
+};
+
+Shape make_shape(const moe_config& c);
+WsLayout ws_layout(const Shape& s);
+
+// ---- launchers (all asynchronous on `st`; return cudaGetLastError()) ----
+cudaError_t launch_router(const Shape& s, const uint16_t* x, const uint16_t* W_g,
+                          const float* bias, const float* u, int32_t* topk_idx, float* topk_w,
+                          cudaStream_t st);
+
+cudaError_t launch_permute(const Shape& s, const int32_t* topk_idx, int32_t* counts,
+                           int32_t* offsets, int32_t* perm_slot, int32_t* slot_pos,
+                           int32_t* blk_hist, int32_t* blk_base, int* status, cudaStream_t st);
+
+// Builds the row-tile list from offsets (routed) plus the shared experts' identity segments,
+// and gathers x rows into expert order (xp[p] = x[perm_slot[p] / k] for p < offsets[E]).
+cudaError_t launch_tiles_and_gather(const Shape& s, const uint16_t* x, const int32_t* perm_slot,
+                                    const int32_t* offsets, uint16_t* xp, TileEntry* tiles,
+                                    Meta* meta, cudaStream_t st);
+
+struct FfnPtrs {
+  const uint16_t* x;
+  const uint16_t* xp;
+  const int32_t* perm_slot;
+  const float* topk_w;
+  const uint16_t *W_gate, *W_up, *W_down;
+  const uint16_t *Wsh_gate, *Wsh_up, *Wsh_down;
+  const uint16_t *W_down_f16, *Wsh_down_f16;  // fp16 down path when W_down_f16 != nullptr
+  uint16_t* h;                                // H: fp16 on the fp16 down path, else bf16
+  float* y;
+  const TileEntry* tiles;
+  const Meta* meta;
+  int* status;
+};
+// ev_mid (optional): recorded on st between the gate/up and the down GEMM.
+cudaError_t launch_grouped_ffn(const Shape& s, const FfnPtrs& p, cudaStream_t st,
+                               cudaEvent_t ev_mid = nullptr);
+
+cudaError_t launch_combine(const Shape& s, const float* y, const int32_t* slot_pos,
+                           uint16_t* out, cudaStream_t st);
+
+cudaError_t launch_pack_f16(const uint16_t* src, uint16_t* dst, size_t n, cudaStream_t st);
+
+int num_sms();
+
+}  // namespace moe

@@ -1,0 +1,374 @@
+// C ABI of the sparse-MoE layer (declarations and argument contracts: include/moe.h).
+// Host-side validation, workspace carving and launch sequencing. No device allocation.
+#include <cuda_runtime.h>
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "internal.h"
+
+namespace moe {
+
+namespace {
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+// ceil(cf * T * k / E) exactly: cf = m * 2^ex with an integer m (24-bit mantissa of the fp32).
+long long exact_capacity(float cf, long long TK, int E) {
+  int ex = 0;
+  const float fr = std::frexp(cf, &ex);          // cf = fr * 2^ex, fr in [0.5, 1)
+  const long long m = (long long)std::ldexp(fr, 24);  // exact: fr has a 24-bit mantissa
+  const int sh = ex - 24;                         // cf = m * 2^sh
+  // value = m * TK * 2^sh / E
+  unsigned __int128 num = (unsigned __int128)m * (unsigned long long)TK;
+  unsigned __int128 den = (unsigned __int128)E;
+  if (sh >= 0) {
+    if (sh > 60) return LLONG_MAX;
+    num <<= sh;
+  } else {
+    if (-sh > 100) return 1;
+    den <<= -sh;
+  }
+  const unsigned __int128 q = (num + den - 1) / den;
+  if (q > (unsigned __int128)LLONG_MAX) return LLONG_MAX;
+  return (long long)q;
+}
+}  // namespace
+
+Shape make_shape(const moe_config& c) {
+  Shape s;
+  s.T = c.T;
+  s.d = c.d;
+  s.E = c.E;
+  s.k = c.top_k;
+  s.f = c.d_ff;
+  s.S = c.n_shared;
+  s.mode = c.mode;
+  s.tau = c.tau;
+  s.TK = (long long)c.T * c.top_k;
+  s.rows = s.TK + (long long)c.n_shared * c.T;
+  long long C = INT_MAX;
+  if (c.capacity_override > 0)
+    C = c.capacity_override;
+  else if (c.capacity_factor > 0.f)
+    C = exact_capacity(c.capacity_factor, s.TK, c.E);
+  if (C > INT_MAX) C = INT_MAX;
+  if (C < 1) C = 1;
+  s.C = (int)C;
+  s.n_pblk = (int)((s.TK + kPermuteBlock - 1) / kPermuteBlock);
+  s.max_tiles = (int)((s.TK + kTileM - 1) / kTileM + s.E +
+                      (long long)s.S * ((s.T + kTileM - 1) / kTileM));
+  return s;
+}
+
+WsLayout ws_layout(const Shape& s) {
+  WsLayout L;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align_up(o + bytes);
+    return at;
+  };
+  L.status = take(sizeof(int));
+  L.meta = take(sizeof(Meta));
+  L.topk_idx = take(sizeof(int32_t) * s.TK);
+  L.topk_w = take(sizeof(float) * s.TK);
+  L.counts = take(sizeof(int32_t) * s.E);
+  L.offsets = take(sizeof(int32_t) * (s.E + 1));
+  L.perm_slot = take(sizeof(int32_t) * s.TK);
+  L.slot_pos = take(sizeof(int32_t) * s.TK);
+  L.blk_hist = take(sizeof(int32_t) * (size_t)s.n_pblk * s.E);
+  L.blk_base = take(sizeof(int32_t) * (size_t)s.n_pblk * s.E);
+  L.tiles = take(sizeof(TileEntry) * (size_t)s.max_tiles);
+  L.xp = take(2ull * s.TK * s.d);
+  L.h = take(2ull * s.rows * s.f);
+  L.y = take(4ull * s.rows * s.d);
+  L.x_stage = take(2ull * s.T * s.d);
+  L.u_stage = take(s.mode == MOE_ROUTE_GUMBEL ? 4ull * s.T * s.E : 0);
+  L.out_stage = take(2ull * s.T * s.d);
+  L.total = o;
+  return L;
+}
+
+int num_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (cache[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev] = n > 0 ? n : 1;
+  }
+  return cache[dev];
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+namespace {
+
+moe_status check_cfg(const moe_config* c) {
+  if (c == nullptr) return MOE_ERR_INVALID_ARG;
+  if (c->T < 1 || c->d < 1 || c->E < 1 || c->top_k < 1 || c->d_ff < 1 || c->n_shared < 0)
+    return MOE_ERR_INVALID_ARG;
+  if (c->mode < MOE_ROUTE_PLAIN || c->mode > MOE_ROUTE_GUMBEL) return MOE_ERR_INVALID_ARG;
+  if (c->mode == MOE_ROUTE_GUMBEL && !(c->tau > 0.f && std::isfinite(c->tau)))
+    return MOE_ERR_INVALID_ARG;
+  if (!std::isfinite(c->capacity_factor)) return MOE_ERR_INVALID_ARG;
+  if (c->E > 256 || c->top_k > 8 || c->top_k > c->E || c->n_shared > 4) return MOE_ERR_UNSUPPORTED;
+  if (c->d % 64 != 0 || c->d_ff % 64 != 0) return MOE_ERR_UNSUPPORTED;
+  const long long rows = (long long)c->T * (c->top_k + c->n_shared);
+  if (rows >= (1ll << 31)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+moe_status check_ws(const moe_config* c, void* ws, size_t ws_bytes) {
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) % 256) != 0) return MOE_ERR_WORKSPACE;
+  if (ws_bytes < ws_layout(make_shape(*c)).total) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+moe_status route_impl(const Shape& s, const uint16_t* x, const uint16_t* W_g, const float* bias,
+                      const float* u, int32_t* idx, float* w, cudaStream_t st) {
+  return cuda_status(launch_router(s, x, W_g, bias, u, idx, w, st));
+}
+
+moe_status permute_impl(const Shape& s, const WsLayout& L, void* ws, const int32_t* idx,
+                        int32_t* counts, int32_t* offsets, int32_t* perm_slot, int32_t* slot_pos,
+                        cudaStream_t st) {
+  return cuda_status(launch_permute(s, idx, counts, offsets, perm_slot, slot_pos,
+                                    at<int32_t>(ws, L.blk_hist), at<int32_t>(ws, L.blk_base),
+                                    at<int>(ws, L.status), st));
+}
+
+moe_status ffn_impl(const Shape& s, const WsLayout& L, void* ws, const uint16_t* x,
+                    const int32_t* perm_slot, const int32_t* offsets, const float* topk_w,
+                    const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wd,
+                    const uint16_t* Wsg, const uint16_t* Wsu, const uint16_t* Wsd,
+                    const uint16_t* Wd16, const uint16_t* Wsd16, float* y,
+                    cudaStream_t st, cudaEvent_t ev_gathered = nullptr,
+                    cudaEvent_t ev_gate_up = nullptr) {
+  cudaError_t e = launch_tiles_and_gather(s, x, perm_slot, offsets, at<uint16_t>(ws, L.xp),
+                                          at<TileEntry>(ws, L.tiles), at<Meta>(ws, L.meta), st);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (ev_gathered != nullptr && cudaEventRecord(ev_gathered, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  FfnPtrs p;
+  p.x = x;
+  p.xp = at<uint16_t>(ws, L.xp);
+  p.perm_slot = perm_slot;
+  p.topk_w = topk_w;
+  p.W_gate = Wg;
+  p.W_up = Wu;
+  p.W_down = Wd;
+  p.Wsh_gate = Wsg;
+  p.Wsh_up = Wsu;
+  p.Wsh_down = Wsd;
+  p.W_down_f16 = Wd16;
+  p.Wsh_down_f16 = Wsd16;
+  p.h = at<uint16_t>(ws, L.h);
+  p.y = y;
+  p.tiles = at<TileEntry>(ws, L.tiles);
+  p.meta = at<Meta>(ws, L.meta);
+  p.status = at<int>(ws, L.status);
+  return cuda_status(launch_grouped_ffn(s, p, st, ev_gate_up));
+}
+
+moe_status layer_impl(const moe_config* cfg, const moe_weights* w, const uint16_t* x,
+                      const float* gumbel_u, uint16_t* out, moe_route_out* ro, void* ws,
+                      size_t ws_bytes, cudaStream_t st, cudaEvent_t const* ev) {
+  moe_status r = check_cfg(cfg);
+  if (r != MOE_OK) return r;
+  if (!w || !x || !out || !w->W_g || !w->W_gate || !w->W_up || !w->W_down)
+    return MOE_ERR_INVALID_ARG;
+  if (cfg->mode == MOE_ROUTE_BIAS_SELECT && !w->expert_bias) return MOE_ERR_INVALID_ARG;
+  if (cfg->mode == MOE_ROUTE_GUMBEL && !gumbel_u) return MOE_ERR_INVALID_ARG;
+  if (cfg->n_shared > 0 && (!w->Wsh_gate || !w->Wsh_up || !w->Wsh_down))
+    return MOE_ERR_INVALID_ARG;
+  if (w->W_down_f16 && cfg->n_shared > 0 && !w->Wsh_down_f16) return MOE_ERR_INVALID_ARG;
+  if ((r = check_ws(cfg, ws, ws_bytes)) != MOE_OK) return r;
+  const Shape s = make_shape(*cfg);
+  const WsLayout L = ws_layout(s);
+  auto mark = [&](int i) { return ev == nullptr || cudaEventRecord(ev[i], st) == cudaSuccess; };
+  int32_t* idx = (ro && ro->topk_idx) ? ro->topk_idx : at<int32_t>(ws, L.topk_idx);
+  float* gw = (ro && ro->topk_w) ? ro->topk_w : at<float>(ws, L.topk_w);
+  int32_t* counts = (ro && ro->counts) ? ro->counts : at<int32_t>(ws, L.counts);
+  int32_t* offsets = (ro && ro->offsets) ? ro->offsets : at<int32_t>(ws, L.offsets);
+  int32_t* perm_slot = (ro && ro->perm_slot) ? ro->perm_slot : at<int32_t>(ws, L.perm_slot);
+  int32_t* slot_pos = (ro && ro->slot_pos) ? ro->slot_pos : at<int32_t>(ws, L.slot_pos);
+  if (!mark(0)) return MOE_ERR_CUDA;
+  if ((r = route_impl(s, x, w->W_g, w->expert_bias, gumbel_u, idx, gw, st)) != MOE_OK) return r;
+  if (!mark(1)) return MOE_ERR_CUDA;
+  if ((r = permute_impl(s, L, ws, idx, counts, offsets, perm_slot, slot_pos, st)) != MOE_OK)
+    return r;
+  if (!mark(2)) return MOE_ERR_CUDA;
+  float* y = at<float>(ws, L.y);
+  if ((r = ffn_impl(s, L, ws, x, perm_slot, offsets, gw, w->W_gate, w->W_up, w->W_down,
+                    w->Wsh_gate, w->Wsh_up, w->Wsh_down, w->W_down_f16, w->Wsh_down_f16, y, st,
+                    ev ? ev[3] : nullptr,
+                    ev ? ev[4] : nullptr)) != MOE_OK)
+    return r;
+  if (!mark(5)) return MOE_ERR_CUDA;
+  if ((r = cuda_status(launch_combine(s, y, slot_pos, out, st))) != MOE_OK) return r;
+  return mark(6) ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes) {
+  moe_status r = check_cfg(cfg);
+  if (r != MOE_OK) return r;
+  if (bytes == nullptr) return MOE_ERR_INVALID_ARG;
+  *bytes = ws_layout(make_shape(*cfg)).total;
+  return MOE_OK;
+}
+
+moe_status moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (ws == nullptr || ws_bytes < 256 || (reinterpret_cast<uintptr_t>(ws) % 256) != 0)
+    return MOE_ERR_WORKSPACE;
+  return cuda_status(cudaMemsetAsync(ws, 0, sizeof(int), (cudaStream_t)stream));
+}
+
+moe_status moe_route(const moe_config* cfg, const uint16_t* x, const uint16_t* W_g,
+                     const float* expert_bias, const float* gumbel_u, int32_t* topk_idx,
+                     float* topk_w, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  moe_status r = check_cfg(cfg);
+  if (r != MOE_OK) return r;
+  if (!x || !W_g || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
+  if (cfg->mode == MOE_ROUTE_BIAS_SELECT && !expert_bias) return MOE_ERR_INVALID_ARG;
+  if (cfg->mode == MOE_ROUTE_GUMBEL && !gumbel_u) return MOE_ERR_INVALID_ARG;
+  if ((r = check_ws(cfg, ws, ws_bytes)) != MOE_OK) return r;
+  const Shape s = make_shape(*cfg);
+  return route_impl(s, x, W_g, expert_bias, gumbel_u, topk_idx, topk_w, (cudaStream_t)stream);
+}
+
+moe_status moe_permute(const moe_config* cfg, const int32_t* topk_idx, int32_t* counts,
+                       int32_t* offsets, int32_t* perm_slot, int32_t* slot_pos, void* ws,
+                       size_t ws_bytes, moe_stream_t stream) {
+  moe_status r = check_cfg(cfg);
+  if (r != MOE_OK) return r;
+  if (!topk_idx || !counts || !offsets || !perm_slot || !slot_pos) return MOE_ERR_INVALID_ARG;
+  if ((r = check_ws(cfg, ws, ws_bytes)) != MOE_OK) return r;
+  const Shape s = make_shape(*cfg);
+  const WsLayout L = ws_layout(s);
+  return permute_impl(s, L, ws, topk_idx, counts, offsets, perm_slot, slot_pos,
+                      (cudaStream_t)stream);
+}
+
+moe_status moe_grouped_ffn(const moe_config* cfg, const uint16_t* x, const int32_t* perm_slot,
+                           const int32_t* offsets, const float* topk_w, const uint16_t* W_gate,
+                           const uint16_t* W_up, const uint16_t* W_down,
+                           const uint16_t* Wsh_gate, const uint16_t* Wsh_up,
+                           const uint16_t* Wsh_down, const uint16_t* W_down_f16,
+                           const uint16_t* Wsh_down_f16, float* y_slot, void* ws,
+                           size_t ws_bytes, moe_stream_t stream) {
+  moe_status r = check_cfg(cfg);
+  if (r != MOE_OK) return r;
+  if (!x || !perm_slot || !offsets || !W_gate || !W_up || !W_down || !y_slot)
+    return MOE_ERR_INVALID_ARG;
+  if (cfg->n_shared > 0 && (!Wsh_gate || !Wsh_up || !Wsh_down)) return MOE_ERR_INVALID_ARG;
+  if (W_down_f16 && cfg->n_shared > 0 && !Wsh_down_f16) return MOE_ERR_INVALID_ARG;
+  if ((r = check_ws(cfg, ws, ws_bytes)) != MOE_OK) return r;
+  const Shape s = make_shape(*cfg);
+  const WsLayout L = ws_layout(s);
+  return ffn_impl(s, L, ws, x, perm_slot, offsets, topk_w, W_gate, W_up, W_down, Wsh_gate,
+                  Wsh_up, Wsh_down, W_down_f16, Wsh_down_f16, y_slot, (cudaStream_t)stream);
+}
+
+moe_status moe_combine(const moe_config* cfg, const float* y_slot, const int32_t* slot_pos,
+                       uint16_t* out, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  moe_status r = check_cfg(cfg);
+  if (r != MOE_OK) return r;
+  if (!y_slot || !slot_pos || !out) return MOE_ERR_INVALID_ARG;
+  if ((r = check_ws(cfg, ws, ws_bytes)) != MOE_OK) return r;
+  const Shape s = make_shape(*cfg);
+  return cuda_status(launch_combine(s, y_slot, slot_pos, out, (cudaStream_t)stream));
+}
+
+moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const uint16_t* x,
+                             const float* gumbel_u, uint16_t* out, moe_route_out* ro, void* ws,
+                             size_t ws_bytes, moe_stream_t stream) {
+  return layer_impl(cfg, w, x, gumbel_u, out, ro, ws, ws_bytes, (cudaStream_t)stream, nullptr);
+}
+
+moe_status moe_layer_forward_profiled(const moe_config* cfg, const moe_weights* w,
+                                      const uint16_t* x, const float* gumbel_u, uint16_t* out,
+                                      moe_route_out* ro, void* ws, size_t ws_bytes,
+                                      moe_stream_t stream, void* const* events, int n_events) {
+  if (events == nullptr || n_events != 7) return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i < 7; ++i)
+    if (events[i] == nullptr) return MOE_ERR_INVALID_ARG;
+  return layer_impl(cfg, w, x, gumbel_u, out, ro, ws, ws_bytes, (cudaStream_t)stream,
+                    reinterpret_cast<cudaEvent_t const*>(events));
+}
+
+moe_status moe_layer_forward_host(const moe_config* cfg, const moe_weights* w,
+                                  const uint16_t* x_host, const float* gumbel_u_host,
+                                  uint16_t* out_host, void* ws, size_t ws_bytes,
+                                  moe_stream_t stream) {
+  moe_status r = check_cfg(cfg);
+  if (r != MOE_OK) return r;
+  if (!x_host || !out_host) return MOE_ERR_INVALID_ARG;
+  if (cfg->mode == MOE_ROUTE_GUMBEL && !gumbel_u_host) return MOE_ERR_INVALID_ARG;
+  if ((r = check_ws(cfg, ws, ws_bytes)) != MOE_OK) return r;
+  const Shape s = make_shape(*cfg);
+  const WsLayout L = ws_layout(s);
+  cudaStream_t st = (cudaStream_t)stream;
+  uint16_t* xd = at<uint16_t>(ws, L.x_stage);
+  float* ud = cfg->mode == MOE_ROUTE_GUMBEL ? at<float>(ws, L.u_stage) : nullptr;
+  uint16_t* od = at<uint16_t>(ws, L.out_stage);
+  if (cudaMemcpyAsync(xd, x_host, 2ull * s.T * s.d, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (ud && cudaMemcpyAsync(ud, gumbel_u_host, 4ull * s.T * s.E, cudaMemcpyHostToDevice, st) !=
+                cudaSuccess)
+    return MOE_ERR_CUDA;
+  if ((r = moe_layer_forward(cfg, w, xd, ud, od, nullptr, ws, ws_bytes, stream)) != MOE_OK)
+    return r;
+  return cuda_status(
+      cudaMemcpyAsync(out_host, od, 2ull * s.T * s.d, cudaMemcpyDeviceToHost, st));
+}
+
+moe_status moe_pack_f16(const uint16_t* src_bf16, uint16_t* dst_f16, size_t n,
+                        moe_stream_t stream) {
+  if (!src_bf16 || !dst_f16 || n == 0) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(src_bf16) | reinterpret_cast<uintptr_t>(dst_f16)) % 16 != 0)
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_pack_f16(src_bf16, dst_f16, n, (cudaStream_t)stream));
+}
+
+moe_status moe_device_status(void* ws, moe_stream_t stream, int32_t* fault_bits) {
+  if (ws == nullptr) return MOE_ERR_WORKSPACE;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  int32_t v = 0;
+  if (cudaMemcpy(&v, ws, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  if (v != 0 && cudaMemset(ws, 0, sizeof(v)) != cudaSuccess) return MOE_ERR_CUDA;
+  if (fault_bits) *fault_bits = v;
+  return v != 0 ? MOE_ERR_DEVICE_FAULT : MOE_OK;
+}
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported size or option";
+    case MOE_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case MOE_ERR_CUDA: return "CUDA runtime or driver call failed";
+    case MOE_ERR_DEVICE_FAULT: return "a kernel recorded a device-side fault";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,250 @@
+// Dispatch: histogram -> capacity clamp -> exclusive scan -> stable scatter, then the grouped
+// GEMM's row-tile list and the gather of x rows into expert order.
+//
+// Capacity rule: "参数规模与稀疏激活的真相拆解", §3.2 专家容量 (capacity = tokens*k/E*factor;
+// Level 1: slots past the limit are marked overflow). Slots claim capacity in slot order
+// (t ascending, then j), which inside one expert is token order. Dispatch into per-expert
+// contiguous segments follows the dispatch layer of "AI架构演进从稀疏MoE到条件记忆的工程实践"
+// (layered-architecture figure: gather -> expert dispatch).
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kSlotsPerThread = kPermuteBlock / kThreads;  // 4
+constexpr int kMaxE = 256;
+
+// Per-block expert histogram of kPermuteBlock consecutive slots.
+__global__ void __launch_bounds__(kThreads) hist_kernel(const int32_t* __restrict__ topk_idx,
+                                                        long long TK, int E,
+                                                        int32_t* __restrict__ blk_hist,
+                                                        int* status) {
+  __shared__ int h[kMaxE];
+  for (int e = threadIdx.x; e < E; e += kThreads) h[e] = 0;
+  __syncthreads();
+  const long long base = (long long)blockIdx.x * kPermuteBlock;
+  bool bad = false;
+#pragma unroll
+  for (int r = 0; r < kSlotsPerThread; ++r) {
+    const long long s = base + r * kThreads + threadIdx.x;
+    if (s < TK) {
+      const int e = topk_idx[s];
+      if (e >= 0 && e < E)
+        atomicAdd(&h[e], 1);
+      else
+        bad = true;
+    }
+  }
+  if (bad) atomicOr(status, MOE_DEVFAULT_BAD_EXPERT_INDEX);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += kThreads)
+    blk_hist[(size_t)blockIdx.x * E + e] = h[e];
+}
+
+// Single block: per-expert running sums over the dispatch blocks (blk_base), counts, the
+// capacity clamp and the exclusive scan of kept counts (offsets).
+__global__ void __launch_bounds__(kThreads) scan_kernel(const int32_t* __restrict__ blk_hist,
+                                                        int n_blk, int E, int C,
+                                                        int32_t* __restrict__ blk_base,
+                                                        int32_t* __restrict__ counts,
+                                                        int32_t* __restrict__ offsets) {
+  constexpr int kBatchInts = 8192;  // 32 KB staging of blk_hist rows
+  __shared__ int stage[kBatchInts];
+  __shared__ int warp_tot[kThreads / 32];
+  const int e = threadIdx.x;
+  const int rows_per_batch = kBatchInts / E;
+  int run = 0;
+  for (int b0 = 0; b0 < n_blk; b0 += rows_per_batch) {
+    const int nb = min(rows_per_batch, n_blk - b0);
+    __syncthreads();
+    for (int i = threadIdx.x; i < nb * E; i += kThreads) stage[i] = blk_hist[(size_t)b0 * E + i];
+    __syncthreads();
+    if (e < E) {
+      for (int b = 0; b < nb; ++b) {
+        blk_base[(size_t)(b0 + b) * E + e] = run;
+        run += stage[b * E + e];
+      }
+    }
+  }
+  int kept = 0;
+  if (e < E) {
+    counts[e] = run;
+    kept = min(run, C);
+  }
+  // block-wide exclusive scan of kept over experts 0..E-1 (warp shuffles, then warp totals)
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int v = kept;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, v, off);
+    if (lane >= off) v += n;
+  }
+  if (lane == 31) warp_tot[warp] = v;
+  __syncthreads();
+  int wbase = 0;
+  for (int w = 0; w < warp; ++w) wbase += warp_tot[w];
+  const int incl = wbase + v;
+  if (e < E) {
+    offsets[e] = incl - kept;
+    if (e == E - 1) offsets[E] = incl;
+  }
+}
+
+// Stable scatter: the rank of a slot inside its expert is (slots of that expert in earlier
+// blocks) + (earlier slots of this block). Ranks >= C are dropped.
+__global__ void __launch_bounds__(kThreads) scatter_kernel(
+    const int32_t* __restrict__ topk_idx, long long TK, int E, int C,
+    const int32_t* __restrict__ blk_base, const int32_t* __restrict__ offsets,
+    int32_t* __restrict__ perm_slot, int32_t* __restrict__ slot_pos) {
+  __shared__ int wcnt[kThreads / 32][kMaxE];
+  __shared__ int running[kMaxE];
+  __shared__ int base[kMaxE];
+  __shared__ int offs[kMaxE];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int e = threadIdx.x; e < E; e += kThreads) {
+    running[e] = 0;
+    base[e] = blk_base[(size_t)blockIdx.x * E + e];
+    offs[e] = offsets[e];
+  }
+  const unsigned lt_mask = (1u << lane) - 1u;
+  const long long blk0 = (long long)blockIdx.x * kPermuteBlock;
+  for (int r = 0; r < kSlotsPerThread; ++r) {
+    const long long s = blk0 + r * kThreads + threadIdx.x;
+    int e = -1;
+    if (s < TK) {
+      e = topk_idx[s];
+      if (e < 0 || e >= E) e = -1;  // reported by hist_kernel; the slot is dropped
+    }
+    for (int i = threadIdx.x; i < (kThreads / 32) * E; i += kThreads)
+      wcnt[i / E][i % E] = 0;
+    __syncthreads();
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank_w = __popc(peers & lt_mask);
+    if (e >= 0 && (peers & lt_mask) == 0) wcnt[warp][e] = __popc(peers);
+    __syncthreads();
+    if (s < TK) {
+      if (e >= 0) {
+        int rank = base[e] + running[e] + rank_w;
+        for (int w = 0; w < warp; ++w) rank += wcnt[w][e];
+        if (rank < C) {
+          const int pos = offs[e] + rank;
+          perm_slot[pos] = (int32_t)s;
+          slot_pos[s] = pos;
+        } else {
+          slot_pos[s] = -1;
+        }
+      } else {
+        slot_pos[s] = -1;
+      }
+    }
+    __syncthreads();
+    for (int ee = threadIdx.x; ee < E; ee += kThreads) {
+      int add = 0;
+      for (int w = 0; w < kThreads / 32; ++w) add += wcnt[w][ee];
+      running[ee] += add;
+    }
+    __syncthreads();
+  }
+  // positions past the last kept slot hold -1
+  const int n_kept = offsets[E];
+  for (int r = 0; r < kSlotsPerThread; ++r) {
+    const long long p = blk0 + r * kThreads + threadIdx.x;
+    if (p < TK && p >= n_kept) perm_slot[p] = -1;
+  }
+}
+
+// Row-tile list of the grouped GEMMs: routed experts' segments cut into kTileM-row tiles, then
+// each shared expert's identity segment over all T tokens.
+__global__ void __launch_bounds__(kThreads) tiles_kernel(const int32_t* __restrict__ offsets,
+                                                         int E, int S, int T, long long TK,
+                                                         TileEntry* __restrict__ tiles,
+                                                         Meta* meta) {
+  __shared__ int warp_tot[kThreads / 32];
+  const int e = threadIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int o0 = 0, kept = 0;
+  if (e < E) {
+    o0 = offsets[e];
+    kept = offsets[e + 1] - o0;
+  }
+  const int nt = (kept + kTileM - 1) / kTileM;
+  int v = nt;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, v, off);
+    if (lane >= off) v += n;
+  }
+  if (lane == 31) warp_tot[warp] = v;
+  __syncthreads();
+  int wbase = 0, total = 0;
+  for (int w = 0; w < kThreads / 32; ++w) {
+    if (w < warp) wbase += warp_tot[w];
+    total += warp_tot[w];
+  }
+  const int start = wbase + v - nt;
+  for (int i = 0; i < nt; ++i) {
+    TileEntry te;
+    te.expert = e;
+    te.row0 = o0 + i * kTileM;
+    te.rows = min(kTileM, kept - i * kTileM);
+    te.arow0 = te.row0;
+    tiles[start + i] = te;
+  }
+  const int per_shared = (T + kTileM - 1) / kTileM;
+  for (int i = threadIdx.x; i < S * per_shared; i += kThreads) {
+    const int s = i / per_shared, m = i % per_shared;
+    TileEntry te;
+    te.expert = E + s;
+    te.row0 = (int)(TK + (long long)s * T + (long long)m * kTileM);
+    te.rows = min(kTileM, T - m * kTileM);
+    te.arow0 = m * kTileM;
+    tiles[total + i] = te;
+  }
+  if (threadIdx.x == 0) {
+    meta->n_tiles = total + S * per_shared;
+    meta->n_kept = offsets[E];
+  }
+}
+
+// xp[p, :] = x[perm_slot[p] / k, :] for p < N. One warp per row, 16-byte vectors.
+__global__ void __launch_bounds__(kThreads) gather_kernel(const uint16_t* __restrict__ x,
+                                                          const int32_t* __restrict__ perm_slot,
+                                                          const int32_t* __restrict__ offsets,
+                                                          int E, int k, int d, long long TK,
+                                                          uint16_t* __restrict__ xp) {
+  const long long p = (long long)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+  if (p >= TK || p >= offsets[E]) return;
+  const int t = perm_slot[p] / k;
+  const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d);
+  uint4* dst = reinterpret_cast<uint4*>(xp + (size_t)p * d);
+  for (int c = threadIdx.x & 31; c < d / 8; c += 32) dst[c] = src[c];
+}
+
+}  // namespace
+
+cudaError_t launch_permute(const Shape& s, const int32_t* topk_idx, int32_t* counts,
+                           int32_t* offsets, int32_t* perm_slot, int32_t* slot_pos,
+                           int32_t* blk_hist, int32_t* blk_base, int* status, cudaStream_t st) {
+  hist_kernel<<<s.n_pblk, kThreads, 0, st>>>(topk_idx, s.TK, s.E, blk_hist, status);
+  scan_kernel<<<1, kThreads, 0, st>>>(blk_hist, s.n_pblk, s.E, s.C, blk_base, counts, offsets);
+  scatter_kernel<<<s.n_pblk, kThreads, 0, st>>>(topk_idx, s.TK, s.E, s.C, blk_base, offsets,
+                                                perm_slot, slot_pos);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tiles_and_gather(const Shape& s, const uint16_t* x, const int32_t* perm_slot,
+                                    const int32_t* offsets, uint16_t* xp, TileEntry* tiles,
+                                    Meta* meta, cudaStream_t st) {
+  tiles_kernel<<<1, kThreads, 0, st>>>(offsets, s.E, s.S, s.T, s.TK, tiles, meta);
+  const long long rows_per_blk = kThreads / 32;
+  const long long grid = (s.TK + rows_per_blk - 1) / rows_per_blk;
+  gather_kernel<<<(unsigned)grid, kThreads, 0, st>>>(x, perm_slot, offsets, s.E, s.k, s.d, s.TK,
+                                                      xp);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,133 @@
+"""Shared helpers of the parity tests: run the CUDA layer through the C ABI, run the oracle on the
+same bytes, and compare under the parity contract.
+
+Contract (per token):
+  * expert indices bit-exact, except tokens whose oracle top-(k+1) adjacent score gap is below
+    1e-5 (exempt; counted and reported);
+  * gates within 1e-5 of the oracle's gates at the GPU's indices;
+  * counts / offsets / perm_slot / slot_pos bit-exact against the oracle dispatch run on the
+    GPU's indices;
+  * layer output (bf16) against the oracle's float64 output conditioned on the GPU's indices:
+    max-abs <= 2e-2 and relative L2 <= 1e-2.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle as O
+import sparse_moe_layer_route_gb300 as M
+import workloads as W
+
+GATE_ATOL = 1e-5
+OUT_MAXABS = 2e-2
+OUT_RELL2 = 1e-2
+
+
+def bits(t):
+    return W.bf16_bits(t)
+
+
+def f64(t):
+    return O.bf16_bits_to_f64(bits(t))
+
+
+def to_device(inp, dev="cuda"):
+    out = {}
+    for k, v in inp.items():
+        out[k] = v.to(dev) if isinstance(v, torch.Tensor) else v
+    return out
+
+
+def pack_down(inp):
+    """fp16 re-encodings of the down weights for the fp16 down path (one-time preparation)."""
+    if "W_down_f16" not in inp:
+        inp["W_down_f16"] = M.packed_f16(inp["W_down"])
+        inp["Ws_down_f16"] = M.packed_f16(inp["Ws_down"]) if inp.get("Ws_down") is not None \
+            else None
+    return inp
+
+
+def run_layer(cfg, inp, capacity_override=0, stream=None, f16=True):
+    """moe_layer_forward with every routing output requested; returns numpy arrays.
+    f16: use the fp16 down path (W_down re-encoded once), else the bf16 down path."""
+    mc = M.MoeConfig.from_layer(cfg)
+    mc.capacity_override = capacity_override
+    T, k, E, d = cfg.T, cfg.k, cfg.E, cfg.d
+    dev = inp["x"].device
+    i32 = dict(dtype=torch.int32, device=dev)
+    idx = torch.full((T, k), -7, **i32)
+    w = torch.full((T, k), float("nan"), dtype=torch.float32, device=dev)
+    counts = torch.full((E,), -7, **i32)
+    offsets = torch.full((E + 1,), -7, **i32)
+    perm_slot = torch.full((T * k,), -7, **i32)
+    slot_pos = torch.full((T * k,), -7, **i32)
+    out = torch.full((T, d), float("nan"), dtype=torch.bfloat16, device=dev)
+    ws = M.alloc_workspace(mc, dev)
+    if f16:
+        pack_down(inp)
+    weights = M.make_weights(inp["W_g"], inp["bias"], inp["W_gate"], inp["W_up"], inp["W_down"],
+                             inp.get("Ws_gate"), inp.get("Ws_up"), inp.get("Ws_down"),
+                             inp.get("W_down_f16") if f16 else None,
+                             inp.get("Ws_down_f16") if f16 else None)
+    ro = M.make_route_out(idx, w, counts, offsets, perm_slot, slot_pos)
+    M.layer_forward(mc, weights, inp["x"], inp.get("u"), out, ro, ws, stream)
+    status = M.device_status(ws, stream)
+    res = {"topk_idx": idx.cpu().numpy(), "topk_w": w.cpu().numpy(),
+           "counts": counts.cpu().numpy(), "offsets": offsets.cpu().numpy(),
+           "perm_slot": perm_slot.cpu().numpy(), "slot_pos": slot_pos.cpu().numpy(),
+           "out_t": out, "status": status, "ws": ws}
+    return res
+
+
+def expert_getter(inp):
+    def get(e):
+        return (f64(inp["W_gate"][e]), f64(inp["W_up"][e]), f64(inp["W_down"][e]))
+    return get
+
+
+def shared_getter(inp):
+    def get(s):
+        return (f64(inp["Ws_gate"][s]), f64(inp["Ws_up"][s]), f64(inp["Ws_down"][s]))
+    return get
+
+
+def oracle_route(cfg, inp):
+    x64 = f64(inp["x"])
+    Wg64 = f64(inp["W_g"])
+    bias = inp["bias"].double().cpu().numpy() if inp["bias"] is not None else None
+    u = inp["u"].cpu().numpy() if inp.get("u") is not None else None
+    r = O.route(x64, Wg64, cfg.k, cfg.mode, bias, u, cfg.tau)
+    return x64, r
+
+
+def check_layer(cfg, inp, gpu, tokens=None, capacity_override=0, x64=None, r=None):
+    """Assert the parity contract; returns a report dict."""
+    if r is None:
+        x64, r = oracle_route(cfg, inp)
+    T, k, E = cfg.T, cfg.k, cfg.E
+    assert gpu["status"] == 0, f"device status {gpu['status']:#x}"
+    exempt = r["margin"] < O.TIE_MARGIN
+    idx_g = gpu["topk_idx"]
+    assert idx_g.min() >= 0 and idx_g.max() < E
+    flipped = (idx_g != r["topk_idx"]).any(axis=1)
+    bad = np.nonzero(flipped & ~exempt)[0]
+    assert bad.size == 0, f"{bad.size} non-exempt tokens routed differently, e.g. {bad[:5]}"
+    w_cond = O.gates(r["logits"], r["scores"], idx_g, cfg.mode)
+    gerr = np.abs(gpu["topk_w"] - w_cond).max()
+    assert gerr <= GATE_ATOL, f"gate error {gerr}"
+    C = O.capacity(T, k, E, cfg.capacity_factor, capacity_override)
+    p = O.permute(idx_g, E, C)
+    for key in ("counts", "offsets", "perm_slot", "slot_pos"):
+        assert np.array_equal(gpu[key], p[key]), f"{key} differs from the oracle dispatch"
+    out_ref, _ = O.layer_from_routing(x64, idx_g, w_cond, E, C, expert_getter(inp), cfg.S,
+                                      shared_getter(inp), tokens)
+    out_t = gpu["out_t"] if tokens is None else gpu["out_t"][torch.as_tensor(tokens)]
+    out_g = f64(out_t)
+    err = np.abs(out_g - out_ref)
+    maxabs = float(err.max())
+    rel_l2 = float(np.linalg.norm(out_g - out_ref) / max(np.linalg.norm(out_ref), 1e-30))
+    assert np.isfinite(out_g).all()
+    assert maxabs <= OUT_MAXABS and rel_l2 <= OUT_RELL2, (maxabs, rel_l2)
+    return {"exempt": int(exempt.sum()), "flipped": int(flipped.sum()), "gate_err": float(gerr),
+            "maxabs": maxabs, "rel_l2": rel_l2, "n_kept": int(p["n_kept"]), "C": C}

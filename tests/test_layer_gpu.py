@@ -1,0 +1,92 @@
+"""Whole layer (moe_layer_forward) against the oracle at sizes the oracle finishes in seconds,
+plus the identities that tie the entry points together."""
+import numpy as np
+import pytest
+import torch
+
+import sparse_moe_layer_route_gb300 as M
+import workloads as W
+from moe_harness import run_layer, check_layer, to_device
+
+pytestmark = pytest.mark.gpu
+
+SMALL = [
+    dict(T=300, d=256, E=8, k=2, f=512, mode=W.PLAIN),
+    dict(T=257, d=192, E=5, k=3, f=320, S=1, mode=W.BIAS_SELECT, bias="normal", bias_var=0.1),
+    dict(T=1000, d=512, E=16, k=2, f=384, mode=W.GUMBEL, tau=0.5, capacity_factor=1.25),
+    dict(T=2048, d=256, E=64, k=6, f=128, S=2, mode=W.BIAS_SELECT, bias="normal", bias_var=0.1),
+    dict(T=1024, d=256, E=32, k=2, f=256, mode=W.BIAS_SELECT, bias="zipf", capacity_factor=1.25),
+    dict(T=1, d=64, E=1, k=1, f=64),
+    dict(T=100, d=128, E=4, k=4, f=128, S=1, capacity_factor=0.05),
+    dict(T=200, d=128, E=256, k=8, f=64),
+]
+
+
+@pytest.mark.parametrize("kw", SMALL, ids=[f"cfg{i}" for i in range(len(SMALL))])
+def test_layer_matches_oracle(kw):
+    cfg = W.small_config(seed=len(kw) * 13 + kw["T"], **kw)
+    inp = to_device(W.make_inputs(cfg, weights_device="cuda",
+                                  zipf_scale=1.5 if kw.get("bias") == "zipf" else None))
+    gpu = run_layer(cfg, inp)
+    check_layer(cfg, inp, gpu)
+
+
+def test_layer_bf16_down_path():
+    cfg = W.small_config(T=600, d=256, E=16, k=2, f=256, mode=W.GUMBEL, tau=0.5, seed=77)
+    inp = to_device(W.make_inputs(cfg, weights_device="cuda"))
+    check_layer(cfg, inp, run_layer(cfg, inp, f16=False))
+
+
+def test_tiny_config_full():
+    cfg = W.CONFIGS["tiny"]
+    inp = to_device(W.make_inputs(cfg, weights_device="cuda"))
+    rep = check_layer(cfg, inp, run_layer(cfg, inp))
+    assert rep["n_kept"] == cfg.T * cfg.k
+
+
+def test_layer_deterministic_and_entry_points_compose():
+    cfg = W.small_config(T=700, d=256, E=16, k=3, f=256, S=1, mode=W.BIAS_SELECT,
+                         bias="normal", bias_var=0.1, capacity_factor=1.1, seed=5)
+    inp = to_device(W.make_inputs(cfg, weights_device="cuda"))
+    a = run_layer(cfg, inp)
+    b = run_layer(cfg, inp)
+    assert torch.equal(a["out_t"].view(torch.int16), b["out_t"].view(torch.int16))
+    # route -> permute -> grouped_ffn -> combine gives the same bits as the fused sequence
+    mc = M.MoeConfig.from_layer(cfg)
+    ws = M.alloc_workspace(mc)
+    dev = "cuda"
+    T, k, E, d = cfg.T, cfg.k, cfg.E, cfg.d
+    idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+    w = torch.empty((T, k), dtype=torch.float32, device=dev)
+    M.route(mc, inp["x"], inp["W_g"], inp["bias"], None, idx, w, ws)
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    perm_slot = torch.empty(T * k, dtype=torch.int32, device=dev)
+    slot_pos = torch.empty(T * k, dtype=torch.int32, device=dev)
+    M.permute(mc, idx, counts, offsets, perm_slot, slot_pos, ws)
+    y = torch.empty((T * k + cfg.S * T, d), dtype=torch.float32, device=dev)
+    M.grouped_ffn(mc, inp["x"], perm_slot, offsets, w, inp["W_gate"], inp["W_up"],
+                  inp["W_down"], inp["Ws_gate"], inp["Ws_up"], inp["Ws_down"], y, ws,
+                  W_down_f16=inp["W_down_f16"], Wsh_down_f16=inp["Ws_down_f16"])
+    out = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
+    M.combine(mc, y, slot_pos, out, ws)
+    assert M.device_status(ws) == 0
+    assert torch.equal(out.view(torch.int16), a["out_t"].view(torch.int16))
+    assert np.array_equal(idx.cpu().numpy(), a["topk_idx"])
+
+
+def test_host_buffer_entry_point_matches_device_one():
+    cfg = W.small_config(T=513, d=256, E=16, k=2, f=256, mode=W.GUMBEL, tau=0.5, seed=8)
+    inp_cpu = W.make_inputs(cfg, weights_device="cuda")
+    inp = to_device(inp_cpu)
+    ref = run_layer(cfg, inp)["out_t"]
+    mc = M.MoeConfig.from_layer(cfg)
+    ws = M.alloc_workspace(mc)
+    weights = M.make_weights(inp["W_g"], inp["bias"], inp["W_gate"], inp["W_up"], inp["W_down"],
+                             W_down_f16=inp["W_down_f16"])
+    x_h = inp_cpu["x"].pin_memory()
+    u_h = inp_cpu["u"].pin_memory()
+    out_h = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16).pin_memory()
+    M.layer_forward_host(mc, weights, x_h, u_h, out_h, ws)
+    assert M.device_status(ws) == 0
+    assert torch.equal(out_h.view(torch.int16), ref.cpu().view(torch.int16))

@@ -1,0 +1,101 @@
+"""The C-ABI library builds, loads and exports every entry point include/moe.h declares; its
+host-side logic (workspace sizing, argument validation, status strings) runs without a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import sparse_moe_layer_route_gb300 as M
+from sparse_moe_layer_route_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return M.lib()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(M.EXPORTS)
+
+
+def test_workspace_size_and_layout(lib):
+    cfg = M.MoeConfig.make(16384, 7168, 128, 2, 2048, mode=M.ROUTE_BIAS_SELECT,
+                           capacity_factor=1.25)
+    n = M.workspace_size(cfg)
+    TK = 16384 * 2
+    # at least the gathered rows, H and the slot-ordered outputs
+    assert n >= 2 * TK * 7168 + 2 * TK * 2048 + 2 * TK * 7168
+    assert n < 4 * 1024 ** 3
+    small = M.MoeConfig.make(128, 256, 8, 2, 512)
+    assert 0 < M.workspace_size(small) < n
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(T=0), 1), (dict(E=0), 1), (dict(top_k=0), 1), (dict(mode=3), 1),
+    (dict(mode=2, tau=0.0), 1), (dict(E=300), 2), (dict(top_k=9, E=16), 2),
+    (dict(top_k=5, E=4), 2), (dict(d=100), 2), (dict(d_ff=96), 2), (dict(n_shared=5), 2),
+])
+def test_bad_configs_rejected(lib, kw, status):
+    base = dict(T=64, d=128, E=8, top_k=2, d_ff=128, n_shared=0, mode=0, tau=1.0,
+                capacity_factor=0.0, capacity_override=0)
+    base.update(kw)
+    cfg = M.MoeConfig(**base)
+    n = ctypes.c_size_t(0)
+    assert lib.moe_workspace_size(ctypes.byref(cfg), ctypes.byref(n)) == status
+
+
+def test_entry_points_validate_before_any_launch(lib):
+    cfg = M.MoeConfig.make(64, 128, 8, 2, 128)
+    need = M.workspace_size(cfg)
+    fake = 0x10000000  # never dereferenced: every call below must fail validation first
+    # missing tensors
+    assert lib.moe_route(ctypes.byref(cfg), None, fake, None, None, fake, fake, fake, need,
+                         None) == 1
+    # bias mode without a bias
+    bcfg = M.MoeConfig.make(64, 128, 8, 2, 128, mode=M.ROUTE_BIAS_SELECT)
+    assert lib.moe_route(ctypes.byref(bcfg), fake, fake, None, None, fake, fake, fake, need,
+                         None) == 1
+    # workspace: NULL, misaligned, too small
+    assert lib.moe_route(ctypes.byref(cfg), fake, fake, None, None, fake, fake, None, need,
+                         None) == 3
+    assert lib.moe_route(ctypes.byref(cfg), fake, fake, None, None, fake, fake, fake + 8, need,
+                         None) == 3
+    assert lib.moe_permute(ctypes.byref(cfg), fake, fake, fake, fake, fake, fake, need - 1,
+                           None) == 3
+    # shared experts requested without their weights
+    scfg = M.MoeConfig.make(64, 128, 8, 2, 128, n_shared=1)
+    assert lib.moe_grouped_ffn(ctypes.byref(scfg), fake, fake, fake, fake, fake, fake, fake,
+                               None, None, None, None, None, fake, fake,
+                               M.workspace_size(scfg), None) == 1
+    # the fp16 down path with shared experts needs the shared fp16 copy too
+    assert lib.moe_grouped_ffn(ctypes.byref(scfg), fake, fake, fake, fake, fake, fake, fake,
+                               fake, fake, fake, fake, None, fake, fake,
+                               M.workspace_size(scfg), None) == 1
+    # pack: NULL / misaligned pointers
+    assert lib.moe_pack_f16(None, fake, 16, None) == 1
+    assert lib.moe_pack_f16(fake + 2, fake, 16, None) == 1
+    w = M.MoeWeights()
+    assert lib.moe_layer_forward(ctypes.byref(cfg), ctypes.byref(w), fake, None, fake, None,
+                                 fake, need, None) == 1
+    assert lib.moe_workspace_init(None, 0, None) == 3
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert M.status_string(s)
+    assert M.status_string(0) == "ok"
+    assert M.status_string(99) == "unknown status"

@@ -1,0 +1,88 @@
+"""Router kernel (moe_route) against the oracle router on the same bf16 bytes."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import sparse_moe_layer_route_gb300 as M
+import workloads as W
+from moe_harness import f64
+
+pytestmark = pytest.mark.gpu
+
+CASES = [  # T, d, E, k, mode, bias
+    (1, 64, 1, 1, W.PLAIN, "zero"),
+    (37, 64, 3, 2, W.PLAIN, "zero"),
+    (300, 256, 8, 2, W.PLAIN, "zero"),
+    (1000, 512, 16, 2, W.GUMBEL, "zero"),
+    (777, 2048, 64, 6, W.BIAS_SELECT, "normal"),
+    (513, 1024, 128, 2, W.BIAS_SELECT, "zipf"),
+    (200, 128, 256, 8, W.PLAIN, "zero"),
+    (64, 192, 100, 5, W.GUMBEL, "zero"),
+    (96, 128, 8, 8, W.BIAS_SELECT, "normal"),
+]
+
+
+def run_route(cfg, inp):
+    mc = M.MoeConfig.from_layer(cfg)
+    dev = "cuda"
+    x, W_g = inp["x"].to(dev), inp["W_g"].to(dev)
+    bias = inp["bias"].to(dev)
+    u = inp["u"].to(dev) if inp["u"] is not None else None
+    idx = torch.full((cfg.T, cfg.k), -1, dtype=torch.int32, device=dev)
+    w = torch.full((cfg.T, cfg.k), float("nan"), dtype=torch.float32, device=dev)
+    ws = M.alloc_workspace(mc)
+    M.route(mc, x, W_g, bias, u, idx, w, ws)
+    torch.cuda.synchronize()
+    return idx.cpu().numpy(), w.cpu().numpy()
+
+
+def oracle_for(cfg, inp):
+    u = inp["u"].numpy() if inp["u"] is not None else None
+    return O.route(f64(inp["x"]), f64(inp["W_g"]), cfg.k, cfg.mode,
+                   inp["bias"].double().numpy(), u, cfg.tau)
+
+
+@pytest.mark.parametrize("T,d,E,k,mode,bias", CASES)
+def test_route_matches_oracle(T, d, E, k, mode, bias):
+    cfg = W.small_config(T=T, d=d, E=E, k=k, f=64, mode=mode, tau=0.5 if mode == W.GUMBEL else 1.0,
+                         seed=T + E, bias=bias, bias_var=0.1)
+    inp = W.make_routing_inputs(cfg, zipf_scale=0.8 if bias == "zipf" else None)
+    idx, w = run_route(cfg, inp)
+    r = oracle_for(cfg, inp)
+    exempt = r["margin"] < O.TIE_MARGIN
+    diff = (idx != r["topk_idx"]).any(1)
+    assert not (diff & ~exempt).any(), np.nonzero(diff & ~exempt)[0][:10]
+    w_ref = O.gates(r["logits"], r["scores"], idx, mode)
+    assert np.abs(w - w_ref).max() <= 1e-5
+    np.testing.assert_allclose(w.sum(1), 1.0, atol=2e-6)
+
+
+def test_route_exact_ties_lowest_index():
+    """Duplicated router columns give bit-identical logits on both sides; the lower index must
+    win every such tie, in the same order as the oracle."""
+    cfg = W.small_config(T=512, d=256, E=16, k=4, f=64, seed=21)
+    inp = W.make_routing_inputs(cfg)
+    Wg = inp["W_g"].clone()
+    for dst, src in ((3, 1), (7, 1), (12, 5), (15, 0)):
+        Wg[:, dst] = Wg[:, src]
+    inp["W_g"] = Wg
+    idx, w = run_route(cfg, inp)
+    r = oracle_for(cfg, inp)
+    s = -np.sort(-r["scores"], 1)[:, : cfg.k + 1]
+    gaps = s[:, :-1] - s[:, 1:]
+    near = ((gaps > 0) & (gaps < O.TIE_MARGIN)).any(1)      # inexact near-ties stay exempt
+    same = (idx == r["topk_idx"]).all(1)
+    assert (same | near).all()
+    n_exact_tie_tokens = ((gaps == 0).any(1) & ~near).sum()
+    assert n_exact_tie_tokens > 50                           # the ties were really exercised
+
+
+def test_route_k_equals_E_zero_router():
+    """W_g = 0: every score ties, so the order is 0..E-1 and every gate is 1/E."""
+    cfg = W.small_config(T=70, d=128, E=6, k=6, f=64, seed=3)
+    inp = W.make_routing_inputs(cfg)
+    inp["W_g"] = torch.zeros_like(inp["W_g"])
+    idx, w = run_route(cfg, inp)
+    assert (idx == np.arange(6)[None, :]).all()
+    np.testing.assert_allclose(w, 1.0 / 6, atol=1e-7)
