@@ -148,6 +148,29 @@ moe_status moe_permute(const moe_config* cfg, const int32_t* topk_idx, int32_t* 
                        int32_t* offsets, int32_t* perm_slot, int32_t* slot_pos, void* ws,
                        size_t ws_bytes, moe_stream_t stream);
 
+/* Largest T * top_k that moe_permute_noalloc accepts (its scratch is a fixed-size array). */
+#define MOE_NOALLOC_MAX_SLOTS 262144
+
+/* Dispatch (the same computation and outputs as moe_permute) for callers that cannot allocate
+ * device memory at all: a plugin handed only its input and output buffers by a host application
+ * that owns every allocation, or a latency-critical loop where cudaMalloc/cudaFree (which may
+ * synchronise the device) are not allowed. No counterpart in the source pages: this is a
+ * deployment convenience, not a step of the method.
+ *   Takes no workspace and allocates nothing (no cudaMalloc, cudaFree or allocating library
+ *   call). Its scratch (per-block expert histograms and their running sums, 512 KB) is a
+ *   file-scope static __device__ array that every GPU loading this library holds until the
+ *   process exits. The first call on each device looks up that array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call before any stream
+ *   capture. All calls share the one array, so calls whose executions overlap on the GPU
+ *   (different streams, or several host threads) race and must be serialised by the caller.
+ *   fault_bits: optional device int32 the call clears and then ORs MOE_DEVFAULT_* bits into
+ *   (NULL: faults are not reported; a bad index still only drops its slot).
+ *   Returns MOE_ERR_UNSUPPORTED when T * top_k > MOE_NOALLOC_MAX_SLOTS (or the config is
+ *   otherwise unsupported); nothing is enqueued then. */
+moe_status moe_permute_noalloc(const moe_config* cfg, const int32_t* topk_idx, int32_t* counts,
+                               int32_t* offsets, int32_t* perm_slot, int32_t* slot_pos,
+                               int32_t* fault_bits, moe_stream_t stream);
+
 /* Steps 6-9. Gathers x rows into expert order, runs the gate/up grouped GEMM with the fused
  * SiLU*up epilogue and the down grouped GEMM with the fused gate-scale + unpermute epilogue on
  * the tensor cores, and the shared experts over all T tokens.

@@ -19,6 +19,7 @@ ROUTE_PLAIN, ROUTE_BIAS_SELECT, ROUTE_GUMBEL = 0, 1, 2
 DEVFAULT_BAD_EXPERT_INDEX, DEVFAULT_PIPELINE_TIMEOUT, DEVFAULT_BAD_TILE = 0x1, 0x2, 0x4
 
 EXPORTS = ("moe_workspace_size", "moe_workspace_init", "moe_route", "moe_permute",
+           "moe_permute_noalloc",
            "moe_grouped_ffn", "moe_combine", "moe_layer_forward", "moe_layer_forward_profiled",
            "moe_layer_forward_host", "moe_pack_f16", "moe_device_status", "moe_status_string")
 
@@ -74,6 +75,7 @@ def lib():
         L.moe_workspace_init.argtypes = [P, S, P]
         L.moe_route.argtypes = [cfgp, P, P, P, P, P, P, P, S, P]
         L.moe_permute.argtypes = [cfgp, P, P, P, P, P, P, S, P]
+        L.moe_permute_noalloc.argtypes = [cfgp, P, P, P, P, P, P, P]
         L.moe_grouped_ffn.argtypes = [cfgp, P, P, P, P, P, P, P, P, P, P, P, P, P, P, S, P]
         L.moe_combine.argtypes = [cfgp, P, P, P, P, S, P]
         L.moe_layer_forward.argtypes = [cfgp, ctypes.POINTER(MoeWeights), P, P, P,
@@ -146,6 +148,19 @@ def permute(cfg, topk_idx, counts, offsets, perm_slot, slot_pos, ws, stream=None
     _check(lib().moe_permute(ctypes.byref(cfg), _ptr(topk_idx), _ptr(counts), _ptr(offsets),
                              _ptr(perm_slot), _ptr(slot_pos), _ptr(ws), ws.numel(),
                              _stream(stream)), "moe_permute")
+
+
+NOALLOC_MAX_SLOTS = 262144
+
+
+def permute_noalloc(cfg, topk_idx, counts, offsets, perm_slot, slot_pos, fault_bits=None,
+                    stream=None):
+    """moe_permute without a workspace, for callers that cannot allocate device memory: the
+    library's own static device array holds the scratch (shared by every call; calls that
+    overlap on the GPU race). fault_bits: optional int32 device tensor of one element."""
+    _check(lib().moe_permute_noalloc(ctypes.byref(cfg), _ptr(topk_idx), _ptr(counts),
+                                     _ptr(offsets), _ptr(perm_slot), _ptr(slot_pos),
+                                     _ptr(fault_bits), _stream(stream)), "moe_permute_noalloc")
 
 
 def grouped_ffn(cfg, x, perm_slot, offsets, topk_w, W_gate, W_up, W_down, Wsh_gate, Wsh_up,

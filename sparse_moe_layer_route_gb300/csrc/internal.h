@@ -57,6 +57,11 @@ cudaError_t launch_permute(const Shape& s, const int32_t* topk_idx, int32_t* cou
                            int32_t* offsets, int32_t* perm_slot, int32_t* slot_pos,
                            int32_t* blk_hist, int32_t* blk_base, int* status, cudaStream_t st);
 
+// moe_permute_noalloc: the same kernels with their scratch in a static device array.
+cudaError_t launch_permute_noalloc(const Shape& s, const int32_t* topk_idx, int32_t* counts,
+                                   int32_t* offsets, int32_t* perm_slot, int32_t* slot_pos,
+                                   int* fault_bits, cudaStream_t st);
+
 // Builds the row-tile list from offsets (routed) plus the shared experts' identity segments,
 // and gathers x rows into expert order (xp[p] = x[perm_slot[p] / k] for p < offsets[E]).
 cudaError_t launch_tiles_and_gather(const Shape& s, const uint16_t* x, const int32_t* perm_slot,

@@ -267,6 +267,18 @@ moe_status moe_permute(const moe_config* cfg, const int32_t* topk_idx, int32_t* 
                       (cudaStream_t)stream);
 }
 
+moe_status moe_permute_noalloc(const moe_config* cfg, const int32_t* topk_idx, int32_t* counts,
+                               int32_t* offsets, int32_t* perm_slot, int32_t* slot_pos,
+                               int32_t* fault_bits, moe_stream_t stream) {
+  moe_status r = check_cfg(cfg);
+  if (r != MOE_OK) return r;
+  if (!topk_idx || !counts || !offsets || !perm_slot || !slot_pos) return MOE_ERR_INVALID_ARG;
+  const Shape s = make_shape(*cfg);
+  if (s.TK > MOE_NOALLOC_MAX_SLOTS) return MOE_ERR_UNSUPPORTED;
+  return cuda_status(launch_permute_noalloc(s, topk_idx, counts, offsets, perm_slot, slot_pos,
+                                            fault_bits, (cudaStream_t)stream));
+}
+
 moe_status moe_grouped_ffn(const moe_config* cfg, const uint16_t* x, const int32_t* perm_slot,
                            const int32_t* offsets, const float* topk_w, const uint16_t* W_gate,
                            const uint16_t* W_up, const uint16_t* W_down,

@@ -8,6 +8,7 @@
 // (layered-architecture figure: gather -> expert dispatch).
 #include <cuda_runtime.h>
 #include <cstdint>
+#include <mutex>
 
 #include "internal.h"
 
@@ -234,6 +235,58 @@ cudaError_t launch_permute(const Shape& s, const int32_t* topk_idx, int32_t* cou
   scatter_kernel<<<s.n_pblk, kThreads, 0, st>>>(topk_idx, s.TK, s.E, s.C, blk_base, offsets,
                                                 perm_slot, slot_pos);
   return cudaGetLastError();
+}
+
+// ---- allocation-free dispatch -----------------------------------------------------------
+// Scratch of moe_permute_noalloc for callers that cannot allocate: 64 ints (256 B) hold a status
+// word used when the caller passes no fault word, then the per-block histograms and the
+// per-block running sums, each up to (MOE_NOALLOC_MAX_SLOTS / kPermuteBlock) x 256 ints.
+namespace {
+constexpr int kNoallocBlocks = MOE_NOALLOC_MAX_SLOTS / kPermuteBlock;
+constexpr int kNoallocInts = 64 + 2 * kNoallocBlocks * kMaxE;
+static_assert(MOE_NOALLOC_MAX_SLOTS % kPermuteBlock == 0, "whole dispatch blocks");
+static __device__ __align__(256) int32_t g_noalloc_scratch[kNoallocInts];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[64] = {nullptr};
+
+// Device address of g_noalloc_scratch on the current device. In host code the array's name
+// is only a host-side stand-in, so the address is looked up once per device (with that device
+// current) and cached.
+cudaError_t noalloc_scratch(int32_t** out) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  void* p = (dev >= 0 && dev < 64) ? g_noalloc_addr[dev] : nullptr;
+  if (p == nullptr) {
+    err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (err != cudaSuccess) return err;
+    if (dev >= 0 && dev < 64) g_noalloc_addr[dev] = p;
+  }
+  *out = static_cast<int32_t*>(p);
+  return cudaSuccess;
+}
+}  // namespace
+
+cudaError_t launch_permute_noalloc(const Shape& s, const int32_t* topk_idx, int32_t* counts,
+                                   int32_t* offsets, int32_t* perm_slot, int32_t* slot_pos,
+                                   int* fault_bits, cudaStream_t st) {
+  if (s.TK > MOE_NOALLOC_MAX_SLOTS || s.E > kMaxE) return cudaErrorInvalidValue;
+  int32_t* scratch = nullptr;
+  cudaError_t err = noalloc_scratch(&scratch);
+  if (err != cudaSuccess) return err;
+  int* status = fault_bits;
+  if (status != nullptr) {
+    if ((err = cudaMemsetAsync(status, 0, sizeof(int), st)) != cudaSuccess) return err;
+  } else {
+    status = scratch;  // nobody reads it
+  }
+  // every entry of both tables is written before it is read, so nothing needs clearing
+  int32_t* blk_hist = scratch + 64;
+  int32_t* blk_base = blk_hist + (size_t)kNoallocBlocks * kMaxE;
+  return launch_permute(s, topk_idx, counts, offsets, perm_slot, slot_pos, blk_hist, blk_base,
+                        status, st);
 }
 
 cudaError_t launch_tiles_and_gather(const Shape& s, const uint16_t* x, const int32_t* perm_slot,
