@@ -21,8 +21,11 @@
 //   warp 2  TMEM allocator.
 //   warps 4-7 epilogue: tcgen05.ld 32 columns at a time, fused SiLU*up (MODE 0) or gate scale and
 //           scatter to slot order (MODE 1), 16-byte stores.
-// Work units: (row tile from the device-written tile list) x (column tile), row tile fastest so
-// CTAs running at the same time share weight tiles through L2. The host never reads the tile
+// Work units: (row tile of the device-written tile list) x (column tile), ordered expert by
+// expert; inside an expert, in blocks of kNBlock column tiles, every row tile of the expert for
+// the block's columns. CTAs running at the same time then share each weight tile (across the
+// expert's row tiles) and each row tile (across the block's columns) through L2, so both are read
+// from DRAM about once. The host never reads the tile
 // count. Every mbarrier wait is bounded (MOE_DEVFAULT_PIPELINE_TIMEOUT on expiry).
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -44,6 +47,7 @@ constexpr int kABytes = kBM * kBK * 2;             // 16 KB
 constexpr int kChunkBytes = kBK * kChunkN * 2;     // 8 KB
 constexpr int kThreads = 256;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s per wait
+constexpr int kNBlock = 8;                          // column tiles per expert block
 
 template <int NCH>
 struct Cfg {
@@ -66,6 +70,19 @@ struct GemmArgs {
   const float* topk_w;       // MODE 1 (NULL: gate 1)
   int* status;
 };
+
+// Work unit w -> (row tile, column tile) in the expert-major blocked order described above.
+__device__ __forceinline__ void map_unit(long long w, int n_nt, const TileEntry* tiles,
+                                         TileEntry& te, int& nt) {
+  const TileEntry first = tiles[w / n_nt];  // some row tile of the unit's expert
+  const long long u = w - (long long)n_nt * first.g0;
+  const long long blk = (long long)first.gn * kNBlock;
+  const int nb = (int)(u / blk);
+  const int nbs = min(kNBlock, n_nt - nb * kNBlock);
+  const int rr = (int)(u - (long long)nb * blk);
+  te = tiles[first.g0 + rr / nbs];
+  nt = nb * kNBlock + rr % nbs;
+}
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
@@ -148,8 +165,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t issued_mask = 0, last_parity = 0;  // per stage: issued at least once / its parity
     bool ok = true;
     for (long long w = blockIdx.x; w < total && ok; w += gridDim.x) {
-      const TileEntry te = a.tiles[w % n_mt];
-      const int nt = (int)(w / n_mt);
+      TileEntry te;
+      int nt;
+      map_unit(w, a.n_ntiles, a.tiles, te, nt);
       const bool shared = te.expert >= a.E;
       const int ex = shared ? te.expert - a.E : te.expert;
       const CUtensorMap* tA = shared ? &tmA_shared : &tmA_routed;
@@ -256,8 +274,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (long long w = blockIdx.x; w < total; w += gridDim.x) {
-      const TileEntry te = a.tiles[w % n_mt];
-      const int nt = (int)(w / n_mt);
+      TileEntry te;
+      int nt;
+      map_unit(w, a.n_ntiles, a.tiles, te, nt);
       if (!ptx::mbar_wait_bounded(tfull_bar(acc), acc_phase, abort_flag, a.status,
                                   MOE_DEVFAULT_PIPELINE_TIMEOUT, kWaitLimitNs))
         break;
@@ -333,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------------------ host side
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn_impl() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = []() {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -346,30 +365,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D map over a row-major [rows, K] 16-bit matrix; box = 64 (K) x 128 (rows), 128-byte swizzle.
 bool make_map_a(CUtensorMap* m, const void* ptr, long long rows, long long K,
                 CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
-  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-  const cuuint32_t box[2] = {kBK, kBM};
-  const cuuint32_t estr[2] = {1, 1};
-  return encode_fn()(m, dt, 2, const_cast<void*>(ptr), dims, strides,
-                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return make_tmap_2d(m, ptr, rows, K, kBK, kBM, dt);
 }
 
-// 3-D map over row-major [n_exp, K, N] 16-bit weights; box = 64 (N) x 64 (K) x 1, 128-byte swizzle.
 bool make_map_b(CUtensorMap* m, const void* ptr, long long n_exp, long long K, long long N,
                 CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
-  const cuuint64_t dims[3] = {(cuuint64_t)N, (cuuint64_t)K, (cuuint64_t)n_exp};
-  const cuuint64_t strides[2] = {(cuuint64_t)N * 2, (cuuint64_t)K * N * 2};
-  const cuuint32_t box[3] = {kChunkN, kBK, 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  return encode_fn()(m, dt, 3, const_cast<void*>(ptr), dims, strides,
-                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return make_tmap_3d(m, ptr, n_exp, K, N, kChunkN, kBK, dt);
 }
 
 template <int MODE, int NCH, bool HF16>
@@ -454,9 +457,35 @@ cudaError_t launch_pair(const Shape& s, const FfnPtrs& p, cudaStream_t st, cudaE
 
 }  // namespace
 
+bool make_tmap_2d(CUtensorMap* m, const void* ptr, long long rows, long long cols, int box_cols,
+                  int box_rows, CUtensorMapDataType dt) {
+  auto fn = encode_fn_impl();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_tmap_3d(CUtensorMap* m, const void* ptr, long long n, long long rows, long long cols,
+                  int box_cols, int box_rows, CUtensorMapDataType dt) {
+  auto fn = encode_fn_impl();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)n};
+  const cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)rows * cols * 2};
+  const cuuint32_t box[3] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, dt, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t launch_grouped_ffn(const Shape& s, const FfnPtrs& p, cudaStream_t st,
                                cudaEvent_t ev_mid) {
-  if (encode_fn() == nullptr) return cudaErrorNotSupported;
+  if (encode_fn_impl() == nullptr) return cudaErrorNotSupported;
   if (p.W_down_f16 != nullptr) return launch_pair<true>(s, p, st, ev_mid);
   return launch_pair<false>(s, p, st, ev_mid);
 }

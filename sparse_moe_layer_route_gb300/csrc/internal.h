@@ -1,5 +1,6 @@
 // Internal launch interface between the C-ABI layer (moe_api.cu) and the kernels.
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cstddef>
 #include <cstdint>
@@ -23,12 +24,15 @@ struct Shape {
 
 // One grouped-GEMM row tile: rows [row0, row0 + rows) of the expert-ordered buffers belong to
 // `expert` (E + s for shared expert s); the A operand of the gate/up GEMM starts at row `arow0`
-// of its source (the gathered rows for routed experts, x itself for shared ones).
+// of its source (the gathered rows for routed experts, x itself for shared ones). The expert's
+// row tiles are entries [g0, g0 + gn) of the list (the GEMMs' work order is expert-major).
 struct TileEntry {
   int expert;
   int row0;
   int rows;
   int arow0;
+  int g0;
+  int gn;
 };
 
 // Meta block inside the workspace (device ints).
@@ -41,7 +45,7 @@ struct Meta {
 // Offsets of every buffer carved from the caller's workspace (bytes, 256-aligned).
 struct WsLayout {
   size_t status, meta, topk_idx, topk_w, counts, offsets, perm_slot, slot_pos;
-  size_t blk_hist, blk_base, tiles, xp, h, y, x_stage, u_stage, out_stage;
+  size_t blk_hist, blk_base, tiles, wg_pad, wg_t, ncand, cand, xp, h, y, x_stage, u_stage, out_stage;
   size_t total;
 };
 
@@ -49,9 +53,14 @@ Shape make_shape(const moe_config& c);
 WsLayout ws_layout(const Shape& s);
 
 // ---- launchers (all asynchronous on `st`; return cudaGetLastError()) ----
+// wg_pad: workspace buffer of d x round_up(E, 64) bf16 used when E is not a multiple of 64;
+// wg_t: workspace buffer of E x d bf16 (W_g transposed, for the exact near-tie pass);
+// ncand [T] and cand [T, 16]: near-tie tokens and their candidate experts (re-decided exactly).
+constexpr int kRouterMaxCand = 16;
 cudaError_t launch_router(const Shape& s, const uint16_t* x, const uint16_t* W_g,
                           const float* bias, const float* u, int32_t* topk_idx, float* topk_w,
-                          cudaStream_t st);
+                          uint16_t* wg_pad, uint16_t* wg_t, int32_t* ncand, int32_t* cand,
+                          int* status, cudaStream_t st);
 
 cudaError_t launch_permute(const Shape& s, const int32_t* topk_idx, int32_t* counts,
                            int32_t* offsets, int32_t* perm_slot, int32_t* slot_pos,
@@ -92,5 +101,14 @@ cudaError_t launch_combine(const Shape& s, const float* y, const int32_t* slot_p
 cudaError_t launch_pack_f16(const uint16_t* src, uint16_t* dst, size_t n, cudaStream_t st);
 
 int num_sms();
+
+// Tensor maps (cuTensorMapEncodeTiled through the runtime's driver entry point), 128-byte swizzle.
+// 2-D over a row-major [rows, cols] 16-bit matrix with a box of box_cols (inner) x box_rows.
+bool make_tmap_2d(CUtensorMap* m, const void* ptr, long long rows, long long cols, int box_cols,
+                  int box_rows, CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+// 3-D over a row-major [n, rows, cols] 16-bit tensor with a box of box_cols x box_rows x 1.
+bool make_tmap_3d(CUtensorMap* m, const void* ptr, long long n, long long rows, long long cols,
+                  int box_cols, int box_rows,
+                  CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
 
 }  // namespace moe

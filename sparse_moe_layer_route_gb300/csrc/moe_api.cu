@@ -81,6 +81,10 @@ WsLayout ws_layout(const Shape& s) {
   L.blk_hist = take(sizeof(int32_t) * (size_t)s.n_pblk * s.E);
   L.blk_base = take(sizeof(int32_t) * (size_t)s.n_pblk * s.E);
   L.tiles = take(sizeof(TileEntry) * (size_t)s.max_tiles);
+  L.wg_pad = take(2ull * s.d * ((s.E + 63) / 64 * 64));
+  L.wg_t = take(2ull * s.d * s.E);
+  L.ncand = take(sizeof(int32_t) * (size_t)s.T);
+  L.cand = take(sizeof(int32_t) * (size_t)s.T * kRouterMaxCand);
   L.xp = take(2ull * s.TK * s.d);
   L.h = take(2ull * s.rows * s.f);
   L.y = take(4ull * s.rows * s.d);
@@ -138,9 +142,12 @@ T* at(void* ws, size_t off) {
 
 moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
-moe_status route_impl(const Shape& s, const uint16_t* x, const uint16_t* W_g, const float* bias,
-                      const float* u, int32_t* idx, float* w, cudaStream_t st) {
-  return cuda_status(launch_router(s, x, W_g, bias, u, idx, w, st));
+moe_status route_impl(const Shape& s, const WsLayout& L, void* ws, const uint16_t* x,
+                      const uint16_t* W_g, const float* bias, const float* u, int32_t* idx,
+                      float* w, cudaStream_t st) {
+  return cuda_status(launch_router(s, x, W_g, bias, u, idx, w, at<uint16_t>(ws, L.wg_pad),
+                                   at<uint16_t>(ws, L.wg_t), at<int32_t>(ws, L.ncand), at<int32_t>(ws, L.cand),
+                                   at<int>(ws, L.status), st));
 }
 
 moe_status permute_impl(const Shape& s, const WsLayout& L, void* ws, const int32_t* idx,
@@ -207,7 +214,8 @@ moe_status layer_impl(const moe_config* cfg, const moe_weights* w, const uint16_
   int32_t* perm_slot = (ro && ro->perm_slot) ? ro->perm_slot : at<int32_t>(ws, L.perm_slot);
   int32_t* slot_pos = (ro && ro->slot_pos) ? ro->slot_pos : at<int32_t>(ws, L.slot_pos);
   if (!mark(0)) return MOE_ERR_CUDA;
-  if ((r = route_impl(s, x, w->W_g, w->expert_bias, gumbel_u, idx, gw, st)) != MOE_OK) return r;
+  if ((r = route_impl(s, L, ws, x, w->W_g, w->expert_bias, gumbel_u, idx, gw, st)) != MOE_OK)
+    return r;
   if (!mark(1)) return MOE_ERR_CUDA;
   if ((r = permute_impl(s, L, ws, idx, counts, offsets, perm_slot, slot_pos, st)) != MOE_OK)
     return r;
@@ -251,7 +259,9 @@ moe_status moe_route(const moe_config* cfg, const uint16_t* x, const uint16_t* W
   if (cfg->mode == MOE_ROUTE_GUMBEL && !gumbel_u) return MOE_ERR_INVALID_ARG;
   if ((r = check_ws(cfg, ws, ws_bytes)) != MOE_OK) return r;
   const Shape s = make_shape(*cfg);
-  return route_impl(s, x, W_g, expert_bias, gumbel_u, topk_idx, topk_w, (cudaStream_t)stream);
+  const WsLayout L = ws_layout(s);
+  return route_impl(s, L, ws, x, W_g, expert_bias, gumbel_u, topk_idx, topk_w,
+                    (cudaStream_t)stream);
 }
 
 moe_status moe_permute(const moe_config* cfg, const int32_t* topk_idx, int32_t* counts,

@@ -193,6 +193,8 @@ __global__ void __launch_bounds__(kThreads) tiles_kernel(const int32_t* __restri
     te.row0 = o0 + i * kTileM;
     te.rows = min(kTileM, kept - i * kTileM);
     te.arow0 = te.row0;
+    te.g0 = start;
+    te.gn = nt;
     tiles[start + i] = te;
   }
   const int per_shared = (T + kTileM - 1) / kTileM;
@@ -203,6 +205,8 @@ __global__ void __launch_bounds__(kThreads) tiles_kernel(const int32_t* __restri
     te.row0 = (int)(TK + (long long)s * T + (long long)m * kTileM);
     te.rows = min(kTileM, T - m * kTileM);
     te.arow0 = m * kTileM;
+    te.g0 = total + s * per_shared;
+    te.gn = per_shared;
     tiles[total + i] = te;
   }
   if (threadIdx.x == 0) {
