@@ -126,11 +126,11 @@ def kernel_work(cfg, phase, n_touched, n_kept):
     if phase == "gate_up_gemm":
         return 4.0 * rows * d * f, ne * 2.0 * d * f * 2 + rows * d * 2.0 + rows * f * 2.0
     if phase == "down_gemm":
-        return 2.0 * rows * f * d, ne * 1.0 * f * d * 2 + rows * f * 2.0 + rows * d * 4.0
+        return 2.0 * rows * f * d, ne * 1.0 * f * d * 2 + rows * f * 2.0 + rows * d * 2.0
     if phase == "router":
         return 2.0 * T * d * E, T * d * 2.0 + d * E * 2.0 + T * k * 8.0
     if phase == "combine":
-        return 0.0, (n_kept + S * T) * d * 4.0 + T * d * 2.0 + T * k * 4.0
+        return 0.0, (n_kept + S * T) * d * 2.0 + T * d * 2.0 + T * k * 4.0
     if phase == "tiles_gather":
         return 0.0, 2.0 * n_kept * d * 2
     if phase == "dispatch":

@@ -177,20 +177,22 @@ moe_status moe_permute_noalloc(const moe_config* cfg, const int32_t* topk_idx, i
  *   perm_slot, offsets as written by moe_permute; topk_w [T, k] (NULL: every gate is 1).
  *   Shared weights may be NULL when cfg->n_shared == 0. W_down_f16 / Wsh_down_f16: optional
  *   fp16 re-encodings from moe_pack_f16 (see moe_weights); NULL selects the bf16 down path.
- *   Writes y_slot [T * k + S * T, d] fp32: row t*k + j = gate[t,j] * y(t,j) for every kept
- *   slot (rows of dropped slots are not written); row T*k + s*T + t = z_s[t]. */
+ *   Writes y_slot [T * k + S * T, d] fp16 (round to nearest, saturating at +-65504):
+ *   row t*k + j = gate[t,j] * y(t,j) for every kept slot (rows of dropped slots are not
+ *   written); row T*k + s*T + t = z_s[t]. fp16 keeps 11 significant bits per term, so the
+ *   fixed-order sum in moe_combine stays within bf16 rounding of the exact layer output. */
 moe_status moe_grouped_ffn(const moe_config* cfg, const uint16_t* x, const int32_t* perm_slot,
                            const int32_t* offsets, const float* topk_w, const uint16_t* W_gate,
                            const uint16_t* W_up, const uint16_t* W_down,
                            const uint16_t* Wsh_gate, const uint16_t* Wsh_up,
                            const uint16_t* Wsh_down, const uint16_t* W_down_f16,
-                           const uint16_t* Wsh_down_f16, float* y_slot, void* ws,
+                           const uint16_t* Wsh_down_f16, uint16_t* y_slot, void* ws,
                            size_t ws_bytes, moe_stream_t stream);
 
 /* Step 10. out[t] = sum_{j=0..k-1, slot_pos[t*k+j] >= 0} y_slot[t*k+j]
  *                   + sum_{s=0..S-1} y_slot[T*k + s*T + t],
- * summed in fp32 in exactly that order and rounded once to bf16. y_slot fp32, out [T, d] bf16. */
-moe_status moe_combine(const moe_config* cfg, const float* y_slot, const int32_t* slot_pos,
+ * summed in fp32 in exactly that order and rounded once to bf16. y_slot fp16, out [T, d] bf16. */
+moe_status moe_combine(const moe_config* cfg, const uint16_t* y_slot, const int32_t* slot_pos,
                        uint16_t* out, void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* One-time weight preparation (not part of the layer's per-call work): dst[i] = src[i]

@@ -165,7 +165,7 @@ def permute_noalloc(cfg, topk_idx, counts, offsets, perm_slot, slot_pos, fault_b
 
 def grouped_ffn(cfg, x, perm_slot, offsets, topk_w, W_gate, W_up, W_down, Wsh_gate, Wsh_up,
                 Wsh_down, y_slot, ws, stream=None, W_down_f16=None, Wsh_down_f16=None):
-    """y_slot: float32 [T*k + S*T, d]."""
+    """y_slot: float16 [T*k + S*T, d]."""
     _check(lib().moe_grouped_ffn(ctypes.byref(cfg), _ptr(x), _ptr(perm_slot), _ptr(offsets),
                                  _ptr(topk_w), _ptr(W_gate), _ptr(W_up), _ptr(W_down),
                                  _ptr(Wsh_gate), _ptr(Wsh_up), _ptr(Wsh_down),

@@ -1,4 +1,4 @@
-// Combine: out[t] = sum over kept j of y_slot[t*k + j] (already gate-scaled by the down GEMM)
+// Combine: out[t] = sum over kept j of y_slot[t*k + j] (fp16, already gate-scaled by the down GEMM)
 // + sum over shared s of y_slot[T*k + s*T + t], in that fixed order in fp32, one bf16 rounding.
 //
 // Weighted sum of the selected experts' outputs: "大模型MoE稀疏激活原理与工程实践", §3.1
@@ -6,6 +6,7 @@
 // "AI架构演进从稀疏MoE到条件记忆的工程实践" (layered-architecture figure), without its residual.
 // Shared experts always added: "V4" rework page, §2.2.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <cstdint>
 
@@ -16,20 +17,20 @@ namespace {
 
 constexpr int kThreads = 256;
 
-__device__ __forceinline__ void add8(float (&acc)[8], const float* p) {
-  const float4 a = *reinterpret_cast<const float4*>(p);
-  const float4 b = *reinterpret_cast<const float4*>(p + 4);
-  acc[0] += a.x;
-  acc[1] += a.y;
-  acc[2] += a.z;
-  acc[3] += a.w;
-  acc[4] += b.x;
-  acc[5] += b.y;
-  acc[6] += b.z;
-  acc[7] += b.w;
+// acc += 8 fp16 values (exact widening to fp32)
+__device__ __forceinline__ void add8(float (&acc)[8], const uint16_t* p) {
+  const uint4 v = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __half2 h = *reinterpret_cast<const __half2*>(&w[i]);
+    const float2 f = __half22float2(h);
+    acc[2 * i] += f.x;
+    acc[2 * i + 1] += f.y;
+  }
 }
 
-__global__ void __launch_bounds__(kThreads) combine_kernel(const float* __restrict__ y,
+__global__ void __launch_bounds__(kThreads) combine_kernel(const uint16_t* __restrict__ y,
                                                            const int32_t* __restrict__ slot_pos,
                                                            uint16_t* __restrict__ out, int T,
                                                            int d, int k, int S) {
@@ -97,7 +98,7 @@ cudaError_t launch_pack_f16(const uint16_t* src, uint16_t* dst, size_t n, cudaSt
   return cudaGetLastError();
 }
 
-cudaError_t launch_combine(const Shape& s, const float* y, const int32_t* slot_pos,
+cudaError_t launch_combine(const Shape& s, const uint16_t* y, const int32_t* slot_pos,
                            uint16_t* out, cudaStream_t st) {
   const long long total = (long long)s.T * (s.d / 8);
   long long grid = (total + kThreads - 1) / kThreads;

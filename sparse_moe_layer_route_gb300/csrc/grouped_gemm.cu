@@ -1,7 +1,7 @@
 // Grouped GEMM over variable-length expert segments on the 5th-generation tensor cores.
 //
 //   gate/up pass (MODE 0):  H[p, n] = silu(sum_k A[p,k] W_gate[e][k,n]) * (sum_k A[p,k] W_up[e][k,n])
-//   down pass    (MODE 1):  Y[row(p), n] = gate(p) * sum_k H[p,k] W_down[e][k,n]     (Y in fp32)
+//   down pass    (MODE 1):  Y[row(p), n] = gate(p) * sum_k H[p,k] W_down[e][k,n]     (Y in fp16)
 // H is stored in fp16 (HF16, with an fp16 copy of W_down so both down operands share the type)
 // or in bf16.
 //
@@ -64,7 +64,7 @@ struct GemmArgs {
   int n_ntiles;       // column tiles
   int k_blocks;       // K / 64
   int E;              // routed experts; tile.expert >= E is shared expert (expert - E)
-  void* out;          // H (MODE 0: 16-bit) or Y (MODE 1: fp32)
+  uint16_t* out;      // H (MODE 0) or Y (MODE 1, fp16)
   long long out_ld;   // elements per output row
   const int32_t* perm_slot;  // MODE 1
   const float* topk_w;       // MODE 1 (NULL: gate 1)
@@ -285,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool valid = row_in_tile < te.rows;
       const long long p = (long long)te.row0 + row_in_tile;
       if (MODE == 0) {
-        uint16_t* dst = static_cast<uint16_t*>(a.out) + p * a.out_ld + (long long)nt * (BN / 2);
+        uint16_t* dst = a.out + p * a.out_ld + (long long)nt * (BN / 2);
 #pragma unroll 1
         for (int c = 0; c < BN / 2 / 32; ++c) {
           uint32_t g[32], u[32];
@@ -316,20 +316,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           orow = slot;
           if (a.topk_w != nullptr) gate = a.topk_w[slot];
         }
-        float* dst = static_cast<float*>(a.out) + orow * a.out_ld + (long long)nt * BN;
+        uint16_t* dst = a.out + orow * a.out_ld + (long long)nt * BN;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t v[32];
           ptx::tmem_ld_32x32b_x32(taddr + c * 32, v);
           ptx::tmem_wait_ld();
-          if (valid) {
-            float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+          uint32_t yv[16];
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              d4[i] = make_float4(gate * __uint_as_float(v[4 * i]),
-                                  gate * __uint_as_float(v[4 * i + 1]),
-                                  gate * __uint_as_float(v[4 * i + 2]),
-                                  gate * __uint_as_float(v[4 * i + 3]));
+          for (int i = 0; i < 16; ++i)
+            yv[i] = pack_f16x2_sat(gate * __uint_as_float(v[2 * i]),
+                                   gate * __uint_as_float(v[2 * i + 1]));
+          if (valid) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              d4[i] = make_uint4(yv[4 * i], yv[4 * i + 1], yv[4 * i + 2], yv[4 * i + 3]);
           }
         }
       }

@@ -86,7 +86,7 @@ struct FfnPtrs {
   const uint16_t *Wsh_gate, *Wsh_up, *Wsh_down;
   const uint16_t *W_down_f16, *Wsh_down_f16;  // fp16 down path when W_down_f16 != nullptr
   uint16_t* h;                                // H: fp16 on the fp16 down path, else bf16
-  float* y;
+  uint16_t* y;                                // slot-ordered expert outputs, fp16
   const TileEntry* tiles;
   const Meta* meta;
   int* status;
@@ -95,7 +95,7 @@ struct FfnPtrs {
 cudaError_t launch_grouped_ffn(const Shape& s, const FfnPtrs& p, cudaStream_t st,
                                cudaEvent_t ev_mid = nullptr);
 
-cudaError_t launch_combine(const Shape& s, const float* y, const int32_t* slot_pos,
+cudaError_t launch_combine(const Shape& s, const uint16_t* y, const int32_t* slot_pos,
                            uint16_t* out, cudaStream_t st);
 
 cudaError_t launch_pack_f16(const uint16_t* src, uint16_t* dst, size_t n, cudaStream_t st);

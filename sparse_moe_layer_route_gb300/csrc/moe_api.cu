@@ -87,7 +87,7 @@ WsLayout ws_layout(const Shape& s) {
   L.cand = take(sizeof(int32_t) * (size_t)s.T * kRouterMaxCand);
   L.xp = take(2ull * s.TK * s.d);
   L.h = take(2ull * s.rows * s.f);
-  L.y = take(4ull * s.rows * s.d);
+  L.y = take(2ull * s.rows * s.d);
   L.x_stage = take(2ull * s.T * s.d);
   L.u_stage = take(s.mode == MOE_ROUTE_GUMBEL ? 4ull * s.T * s.E : 0);
   L.out_stage = take(2ull * s.T * s.d);
@@ -162,7 +162,7 @@ moe_status ffn_impl(const Shape& s, const WsLayout& L, void* ws, const uint16_t*
                     const int32_t* perm_slot, const int32_t* offsets, const float* topk_w,
                     const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wd,
                     const uint16_t* Wsg, const uint16_t* Wsu, const uint16_t* Wsd,
-                    const uint16_t* Wd16, const uint16_t* Wsd16, float* y,
+                    const uint16_t* Wd16, const uint16_t* Wsd16, uint16_t* y,
                     cudaStream_t st, cudaEvent_t ev_gathered = nullptr,
                     cudaEvent_t ev_gate_up = nullptr) {
   cudaError_t e = launch_tiles_and_gather(s, x, perm_slot, offsets, at<uint16_t>(ws, L.xp),
@@ -220,7 +220,7 @@ moe_status layer_impl(const moe_config* cfg, const moe_weights* w, const uint16_
   if ((r = permute_impl(s, L, ws, idx, counts, offsets, perm_slot, slot_pos, st)) != MOE_OK)
     return r;
   if (!mark(2)) return MOE_ERR_CUDA;
-  float* y = at<float>(ws, L.y);
+  uint16_t* y = at<uint16_t>(ws, L.y);
   if ((r = ffn_impl(s, L, ws, x, perm_slot, offsets, gw, w->W_gate, w->W_up, w->W_down,
                     w->Wsh_gate, w->Wsh_up, w->Wsh_down, w->W_down_f16, w->Wsh_down_f16, y, st,
                     ev ? ev[3] : nullptr,
@@ -294,7 +294,7 @@ moe_status moe_grouped_ffn(const moe_config* cfg, const uint16_t* x, const int32
                            const uint16_t* W_up, const uint16_t* W_down,
                            const uint16_t* Wsh_gate, const uint16_t* Wsh_up,
                            const uint16_t* Wsh_down, const uint16_t* W_down_f16,
-                           const uint16_t* Wsh_down_f16, float* y_slot, void* ws,
+                           const uint16_t* Wsh_down_f16, uint16_t* y_slot, void* ws,
                            size_t ws_bytes, moe_stream_t stream) {
   moe_status r = check_cfg(cfg);
   if (r != MOE_OK) return r;
@@ -309,7 +309,7 @@ moe_status moe_grouped_ffn(const moe_config* cfg, const uint16_t* x, const int32
                   Wsh_up, Wsh_down, W_down_f16, Wsh_down_f16, y_slot, (cudaStream_t)stream);
 }
 
-moe_status moe_combine(const moe_config* cfg, const float* y_slot, const int32_t* slot_pos,
+moe_status moe_combine(const moe_config* cfg, const uint16_t* y_slot, const int32_t* slot_pos,
                        uint16_t* out, void* ws, size_t ws_bytes, moe_stream_t stream) {
   moe_status r = check_cfg(cfg);
   if (r != MOE_OK) return r;

@@ -25,7 +25,7 @@ def run_case(T, d, E, k, f, S, C, skew, seed, f16=True):
     dev = "cuda"
     mc = M.MoeConfig.make(T, d, E, k, f, n_shared=S, capacity_override=C)
     x = inp["x"].to(dev)
-    y = torch.full((T * k + S * T, d), float("nan"), dtype=torch.float32, device=dev)
+    y = torch.full((T * k + S * T, d), float("nan"), dtype=torch.float16, device=dev)
     ws = M.alloc_workspace(mc)
     Wd16 = M.packed_f16(inp["W_down"]) if f16 else None
     Wsd16 = M.packed_f16(inp["Ws_down"]) if (f16 and S > 0) else None

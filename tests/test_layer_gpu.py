@@ -64,7 +64,7 @@ def test_layer_deterministic_and_entry_points_compose():
     perm_slot = torch.empty(T * k, dtype=torch.int32, device=dev)
     slot_pos = torch.empty(T * k, dtype=torch.int32, device=dev)
     M.permute(mc, idx, counts, offsets, perm_slot, slot_pos, ws)
-    y = torch.empty((T * k + cfg.S * T, d), dtype=torch.float32, device=dev)
+    y = torch.empty((T * k + cfg.S * T, d), dtype=torch.float16, device=dev)
     M.grouped_ffn(mc, inp["x"], perm_slot, offsets, w, inp["W_gate"], inp["W_up"],
                   inp["W_down"], inp["Ws_gate"], inp["Ws_up"], inp["Ws_down"], y, ws,
                   W_down_f16=inp["W_down_f16"], Wsh_down_f16=inp["Ws_down_f16"])
