@@ -30,35 +30,32 @@ __device__ __forceinline__ void add8(float (&acc)[8], const uint16_t* p) {
   }
 }
 
+// Grid (column blocks, tokens): thread = one 8-column group of one token. The token's slot
+// flags are the same for the whole block (broadcast loads); every row's 16-byte load of the
+// group is issued before the sum.
 __global__ void __launch_bounds__(kThreads) combine_kernel(const uint16_t* __restrict__ y,
                                                            const int32_t* __restrict__ slot_pos,
                                                            uint16_t* __restrict__ out, int T,
                                                            int d, int k, int S) {
-  const int vec_per_row = d / 8;
-  const long long total = (long long)T * vec_per_row;
+  const int t = blockIdx.y;
+  const int g = blockIdx.x * kThreads + threadIdx.x;
+  if (g >= d / 8) return;
   const long long TK = (long long)T * k;
-  for (long long u = (long long)blockIdx.x * kThreads + threadIdx.x; u < total;
-       u += (long long)gridDim.x * kThreads) {
-    const int t = (int)(u / vec_per_row);
-    const int c = (int)(u % vec_per_row);
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int j = 0; j < k; ++j) {
-      const long long slot = (long long)t * k + j;
-      if (slot_pos[slot] >= 0)
-        add8(acc, y + slot * d + 8 * c);
-    }
-    for (int s = 0; s < S; ++s) {
-      const long long row = TK + (long long)s * T + t;
-      add8(acc, y + row * d + 8 * c);
-    }
-    uint32_t o[4];
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
-      o[i] = *reinterpret_cast<const uint32_t*>(&b);
-    }
-    *reinterpret_cast<uint4*>(out + (size_t)t * d + 8 * c) = make_uint4(o[0], o[1], o[2], o[3]);
+  for (int j = 0; j < 8; ++j)  // top_k <= 8
+    if (j < k && slot_pos[(long long)t * k + j] >= 0)
+      add8(acc, y + ((long long)t * k + j) * d + 8 * g);
+#pragma unroll
+  for (int s = 0; s < 4; ++s)  // n_shared <= 4
+    if (s < S) add8(acc, y + (TK + (long long)s * T + t) * d + 8 * g);
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+    o[i] = *reinterpret_cast<const uint32_t*>(&b);
   }
+  *reinterpret_cast<uint4*>(out + (size_t)t * d + 8 * g) = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 // dst[i] = fp16(bf16 src[i]), round to nearest even, saturating; 8 elements per thread.
@@ -100,12 +97,8 @@ cudaError_t launch_pack_f16(const uint16_t* src, uint16_t* dst, size_t n, cudaSt
 
 cudaError_t launch_combine(const Shape& s, const uint16_t* y, const int32_t* slot_pos,
                            uint16_t* out, cudaStream_t st) {
-  const long long total = (long long)s.T * (s.d / 8);
-  long long grid = (total + kThreads - 1) / kThreads;
-  const long long cap = (long long)num_sms() * 16;
-  if (grid > cap) grid = cap;
-  if (grid < 1) grid = 1;
-  combine_kernel<<<(unsigned)grid, kThreads, 0, st>>>(y, slot_pos, out, s.T, s.d, s.k, s.S);
+  const dim3 grid((s.d / 8 + kThreads - 1) / kThreads, s.T);
+  combine_kernel<<<grid, kThreads, 0, st>>>(y, slot_pos, out, s.T, s.d, s.k, s.S);
   return cudaGetLastError();
 }
 
