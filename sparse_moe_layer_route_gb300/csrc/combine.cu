@@ -37,6 +37,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const uint16_t* __res
                                                            const int32_t* __restrict__ slot_pos,
                                                            uint16_t* __restrict__ out, int T,
                                                            int d, int k, int S) {
+  griddep_wait();
   const int t = blockIdx.y;
   const int g = blockIdx.x * kThreads + threadIdx.x;
   if (g >= d / 8) return;
@@ -98,8 +99,8 @@ cudaError_t launch_pack_f16(const uint16_t* src, uint16_t* dst, size_t n, cudaSt
 cudaError_t launch_combine(const Shape& s, const uint16_t* y, const int32_t* slot_pos,
                            uint16_t* out, cudaStream_t st) {
   const dim3 grid((s.d / 8 + kThreads - 1) / kThreads, s.T);
-  combine_kernel<<<grid, kThreads, 0, st>>>(y, slot_pos, out, s.T, s.d, s.k, s.S);
-  return cudaGetLastError();
+  return launch_k(combine_kernel, grid, dim3(kThreads), 0, st, y, slot_pos, out, s.T, s.d, s.k,
+                  s.S);
 }
 
 }  // namespace moe

@@ -153,6 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  griddep_wait();  // everything above touched only shared memory, TMEM and parameters
 
   const int n_mt = a.meta->n_tiles;
   const long long total = (long long)n_mt * a.n_ntiles;
@@ -384,9 +385,8 @@ cudaError_t launch_one(const CUtensorMap (&maps)[6], const GemmArgs& args, cudaS
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (err != cudaSuccess) return err;
-  kern<<<num_sms(), kThreads, C::kSmemBytes, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4],
-                                                   maps[5], args);
-  return cudaGetLastError();
+  return launch_k(kern, dim3(num_sms()), dim3(kThreads), C::kSmemBytes, st, maps[0], maps[1],
+                  maps[2], maps[3], maps[4], maps[5], args);
 }
 
 template <bool HF16>

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 
 #include "../../include/moe.h"
 
@@ -101,6 +102,32 @@ cudaError_t launch_combine(const Shape& s, const uint16_t* y, const int32_t* slo
 cudaError_t launch_pack_f16(const uint16_t* src, uint16_t* dst, size_t n, cudaStream_t st);
 
 int num_sms();
+
+// Device side of programmatic dependent launch: wait until the preceding kernel in the stream
+// has completed and its memory is visible. Every kernel of the layer calls this before it reads
+// or writes global memory (setup that touches only shared memory, TMEM and parameters may come
+// first), so launching it early (launch_k) is safe whatever precedes it.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Launches `kernel` with programmatic stream serialization: it may begin while the previous
+// kernel on the stream drains (its griddep_wait() provides the ordering).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                     cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Tensor maps (cuTensorMapEncodeTiled through the runtime's driver entry point), 128-byte swizzle.
 // 2-D over a row-major [rows, cols] 16-bit matrix with a box of box_cols (inner) x box_rows.

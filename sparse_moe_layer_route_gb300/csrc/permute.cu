@@ -24,6 +24,7 @@ __global__ void __launch_bounds__(kThreads) hist_kernel(const int32_t* __restric
                                                         long long TK, int E,
                                                         int32_t* __restrict__ blk_hist,
                                                         int* status) {
+  griddep_wait();
   __shared__ int h[kMaxE];
   for (int e = threadIdx.x; e < E; e += kThreads) h[e] = 0;
   __syncthreads();
@@ -56,6 +57,7 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(const int32_t* __restric
   constexpr int kBatchInts = 8192;  // 32 KB staging of blk_hist rows
   __shared__ int stage[kBatchInts];
   __shared__ int warp_tot[kThreads / 32];
+  griddep_wait();
   const int e = threadIdx.x;
   const int rows_per_batch = kBatchInts / E;
   int run = 0;
@@ -105,6 +107,7 @@ __global__ void __launch_bounds__(kThreads) scatter_kernel(
   __shared__ int running[kMaxE];
   __shared__ int base[kMaxE];
   __shared__ int offs[kMaxE];
+  griddep_wait();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int e = threadIdx.x; e < E; e += kThreads) {
     running[e] = 0;
@@ -165,6 +168,7 @@ __global__ void __launch_bounds__(kThreads) tiles_kernel(const int32_t* __restri
                                                          TileEntry* __restrict__ tiles,
                                                          Meta* meta) {
   __shared__ int warp_tot[kThreads / 32];
+  griddep_wait();
   const int e = threadIdx.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int o0 = 0, kept = 0;
@@ -221,6 +225,7 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const uint16_t* __rest
                                                           const int32_t* __restrict__ offsets,
                                                           int E, int k, int d, long long TK,
                                                           uint16_t* __restrict__ xp) {
+  griddep_wait();
   const long long p = (long long)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
   if (p >= TK || p >= offsets[E]) return;
   const int t = perm_slot[p] / k;
@@ -234,11 +239,15 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const uint16_t* __rest
 cudaError_t launch_permute(const Shape& s, const int32_t* topk_idx, int32_t* counts,
                            int32_t* offsets, int32_t* perm_slot, int32_t* slot_pos,
                            int32_t* blk_hist, int32_t* blk_base, int* status, cudaStream_t st) {
-  hist_kernel<<<s.n_pblk, kThreads, 0, st>>>(topk_idx, s.TK, s.E, blk_hist, status);
-  scan_kernel<<<1, kThreads, 0, st>>>(blk_hist, s.n_pblk, s.E, s.C, blk_base, counts, offsets);
-  scatter_kernel<<<s.n_pblk, kThreads, 0, st>>>(topk_idx, s.TK, s.E, s.C, blk_base, offsets,
-                                                perm_slot, slot_pos);
-  return cudaGetLastError();
+  cudaError_t e = launch_k(hist_kernel, dim3(s.n_pblk), dim3(kThreads), 0, st, topk_idx, s.TK,
+                           s.E, blk_hist, status);
+  if (e == cudaSuccess)
+    e = launch_k(scan_kernel, dim3(1), dim3(kThreads), 0, st, (const int32_t*)blk_hist, s.n_pblk,
+                 s.E, s.C, blk_base, counts, offsets);
+  if (e == cudaSuccess)
+    e = launch_k(scatter_kernel, dim3(s.n_pblk), dim3(kThreads), 0, st, topk_idx, s.TK, s.E, s.C,
+                 (const int32_t*)blk_base, (const int32_t*)offsets, perm_slot, slot_pos);
+  return e;
 }
 
 // ---- allocation-free dispatch -----------------------------------------------------------
@@ -296,12 +305,13 @@ cudaError_t launch_permute_noalloc(const Shape& s, const int32_t* topk_idx, int3
 cudaError_t launch_tiles_and_gather(const Shape& s, const uint16_t* x, const int32_t* perm_slot,
                                     const int32_t* offsets, uint16_t* xp, TileEntry* tiles,
                                     Meta* meta, cudaStream_t st) {
-  tiles_kernel<<<1, kThreads, 0, st>>>(offsets, s.E, s.S, s.T, s.TK, tiles, meta);
+  cudaError_t e = launch_k(tiles_kernel, dim3(1), dim3(kThreads), 0, st, offsets, s.E, s.S, s.T,
+                           s.TK, tiles, meta);
+  if (e != cudaSuccess) return e;
   const long long rows_per_blk = kThreads / 32;
   const long long grid = (s.TK + rows_per_blk - 1) / rows_per_blk;
-  gather_kernel<<<(unsigned)grid, kThreads, 0, st>>>(x, perm_slot, offsets, s.E, s.k, s.d, s.TK,
-                                                      xp);
-  return cudaGetLastError();
+  return launch_k(gather_kernel, dim3((unsigned)grid), dim3(kThreads), 0, st, x, perm_slot,
+                  offsets, s.E, s.k, s.d, s.TK, xp);
 }
 
 }  // namespace moe

@@ -142,6 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tmem_alloc(ptx::smem_u32(tmem_slot), C::kTmemCols);
     ptx::tmem_relinquish();
   }
+  griddep_wait();  // the setup above touched only shared memory, TMEM and parameters
   if (warp == 3) {
     for (int e = lane; e < a.E; e += 32)
       bias_s[e] = (a.mode == MOE_ROUTE_BIAS_SELECT) ? a.bias[e] : 0.f;
@@ -380,6 +381,7 @@ __global__ void __launch_bounds__(kThreads) prep_router_kernel(const uint16_t* _
                                                                uint16_t* __restrict__ Wp, int d,
                                                                int E, int EP) {
   __shared__ uint16_t tile[32][33];
+  griddep_wait();
   const int j0 = blockIdx.x * 32, e0 = blockIdx.y * 32;
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
   for (int r = ty; r < 32; r += 8) {
@@ -410,6 +412,7 @@ __global__ void __launch_bounds__(kThreads) refine_kernel(
   __shared__ float cl[256], cs[256];
   __shared__ int flagged[kThreads];
   __shared__ int n_flagged;
+  griddep_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // this CTA's contiguous chunk of tokens; their flags are read 256 at a time in one round
   const int chunk = (T + gridDim.x - 1) / gridDim.x;
@@ -521,8 +524,8 @@ cudaError_t launch_tc(const CUtensorMap& mx, const CUtensorMap& mw, const Router
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmemBytes);
   if (err != cudaSuccess) return err;
-  router_tc_kernel<NCH><<<grid, kThreads, C::kSmemBytes, st>>>(mx, mw, a);
-  return cudaGetLastError();
+  return launch_k(router_tc_kernel<NCH>, dim3(grid), dim3(kThreads), C::kSmemBytes, st, mx, mw,
+                  a);
 }
 
 }  // namespace
@@ -535,8 +538,9 @@ cudaError_t launch_router(const Shape& s, const uint16_t* x, const uint16_t* W_g
   const uint16_t* W = EP != s.E ? wg_pad : W_g;
   {
     const dim3 grid((s.d + 31) / 32, (EP + 31) / 32);
-    prep_router_kernel<<<grid, kThreads, 0, st>>>(W_g, wg_t, EP != s.E ? wg_pad : nullptr, s.d,
-                                                  s.E, EP);
+    const cudaError_t e = launch_k(prep_router_kernel, grid, dim3(kThreads), 0, st, W_g, wg_t,
+                                   EP != s.E ? wg_pad : nullptr, s.d, s.E, EP);
+    if (e != cudaSuccess) return e;
   }
   CUtensorMap mx, mw;
   if (!make_tmap_2d(&mx, x, s.T, s.d, kBK, kBM) || !make_tmap_2d(&mw, W, s.d, EP, 64, kBK))
@@ -566,9 +570,9 @@ cudaError_t launch_router(const Shape& s, const uint16_t* x, const uint16_t* W_g
   }
   if (err != cudaSuccess) return err;
   const int rgrid = s.T < 2 * num_sms() ? s.T : 2 * num_sms();
-  refine_kernel<<<rgrid, kThreads, 0, st>>>(x, wg_t, bias, u, ncand, cand, topk_idx, topk_w, s.T,
-                                            s.d, s.E, s.k, s.mode, s.tau);
-  return cudaGetLastError();
+  return launch_k(refine_kernel, dim3(rgrid), dim3(kThreads), 0, st, x, (const uint16_t*)wg_t,
+                  bias, u, (const int32_t*)ncand, (const int32_t*)cand, topk_idx, topk_w, s.T, s.d,
+                  s.E, s.k, s.mode, s.tau);
 }
 
 }  // namespace moe
