@@ -36,17 +36,20 @@ struct TileEntry {
   int gn;
 };
 
-// Meta block inside the workspace (device ints).
+// Meta block inside the workspace (device ints); moe_workspace_init zeroes it.
 struct Meta {
-  int n_tiles;   // row tiles written by the dispatch scan
-  int n_kept;    // N = kept routed slots
-  int pad[62];
+  int n_tiles;        // row tiles written by the dispatch scan
+  int n_kept;         // N = kept routed slots
+  int refine_count;   // near-tie tokens listed by the router (reset by the refine kernel)
+  int refine_done;    // refine CTAs finished (reset by the last one)
+  int pad[60];
 };
 
 // Offsets of every buffer carved from the caller's workspace (bytes, 256-aligned).
 struct WsLayout {
   size_t status, meta, topk_idx, topk_w, counts, offsets, perm_slot, slot_pos;
-  size_t blk_hist, blk_base, tiles, wg_pad, wg_t, ncand, cand, xp, h, y, x_stage, u_stage, out_stage;
+  size_t blk_hist, blk_base, tiles, wg_pad, wg_t, rpart, ncand, cand, rlist, xp, h, y, x_stage,
+      u_stage, out_stage;
   size_t total;
 };
 
@@ -54,14 +57,23 @@ Shape make_shape(const moe_config& c);
 WsLayout ws_layout(const Shape& s);
 
 // ---- launchers (all asynchronous on `st`; return cudaGetLastError()) ----
-// wg_pad: workspace buffer of d x round_up(E, 64) bf16 used when E is not a multiple of 64;
-// wg_t: workspace buffer of E x d bf16 (W_g transposed, for the exact near-tie pass);
-// ncand [T] and cand [T, 16]: near-tie tokens and their candidate experts (re-decided exactly).
+// Router scratch carved from the workspace.
 constexpr int kRouterMaxCand = 16;
+struct RouterScratch {
+  uint16_t* wg_pad;  // d x round_up(E, 64) bf16, used when E is not a multiple of 64
+  uint16_t* wg_t;    // E x d bf16: W_g transposed (exact near-tie pass)
+  float* part;       // [splits, T, round_up(E, 64)] fp32 partial logits
+  int32_t* ncand;    // [T] near-tie candidate counts
+  int32_t* cand;     // [T, kRouterMaxCand] candidate experts
+  int32_t* rlist;    // [T] near-tie tokens
+  int* rcount;       // their number (zero between calls)
+  int* rdone;        // refine CTAs finished (zero between calls)
+};
+// K slices of the router GEMM for T tokens and hidden size d.
+int router_splits(int T, int d);
 cudaError_t launch_router(const Shape& s, const uint16_t* x, const uint16_t* W_g,
                           const float* bias, const float* u, int32_t* topk_idx, float* topk_w,
-                          uint16_t* wg_pad, uint16_t* wg_t, int32_t* ncand, int32_t* cand,
-                          int* status, cudaStream_t st);
+                          const RouterScratch& rs, int* status, cudaStream_t st);
 
 cudaError_t launch_permute(const Shape& s, const int32_t* topk_idx, int32_t* counts,
                            int32_t* offsets, int32_t* perm_slot, int32_t* slot_pos,

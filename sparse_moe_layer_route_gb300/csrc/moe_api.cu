@@ -83,8 +83,10 @@ WsLayout ws_layout(const Shape& s) {
   L.tiles = take(sizeof(TileEntry) * (size_t)s.max_tiles);
   L.wg_pad = take(2ull * s.d * ((s.E + 63) / 64 * 64));
   L.wg_t = take(2ull * s.d * s.E);
+  L.rpart = take(4ull * router_splits(s.T, s.d) * s.T * ((s.E + 63) / 64 * 64));
   L.ncand = take(sizeof(int32_t) * (size_t)s.T);
   L.cand = take(sizeof(int32_t) * (size_t)s.T * kRouterMaxCand);
+  L.rlist = take(sizeof(int32_t) * (size_t)s.T);
   L.xp = take(2ull * s.TK * s.d);
   L.h = take(2ull * s.rows * s.f);
   L.y = take(2ull * s.rows * s.d);
@@ -145,9 +147,17 @@ moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_E
 moe_status route_impl(const Shape& s, const WsLayout& L, void* ws, const uint16_t* x,
                       const uint16_t* W_g, const float* bias, const float* u, int32_t* idx,
                       float* w, cudaStream_t st) {
-  return cuda_status(launch_router(s, x, W_g, bias, u, idx, w, at<uint16_t>(ws, L.wg_pad),
-                                   at<uint16_t>(ws, L.wg_t), at<int32_t>(ws, L.ncand), at<int32_t>(ws, L.cand),
-                                   at<int>(ws, L.status), st));
+  RouterScratch rs;
+  rs.wg_pad = at<uint16_t>(ws, L.wg_pad);
+  rs.wg_t = at<uint16_t>(ws, L.wg_t);
+  rs.part = at<float>(ws, L.rpart);
+  rs.ncand = at<int32_t>(ws, L.ncand);
+  rs.cand = at<int32_t>(ws, L.cand);
+  rs.rlist = at<int32_t>(ws, L.rlist);
+  Meta* meta = at<Meta>(ws, L.meta);
+  rs.rcount = &meta->refine_count;
+  rs.rdone = &meta->refine_done;
+  return cuda_status(launch_router(s, x, W_g, bias, u, idx, w, rs, at<int>(ws, L.status), st));
 }
 
 moe_status permute_impl(const Shape& s, const WsLayout& L, void* ws, const int32_t* idx,
@@ -244,9 +254,11 @@ moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes) {
 }
 
 moe_status moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream) {
-  if (ws == nullptr || ws_bytes < 256 || (reinterpret_cast<uintptr_t>(ws) % 256) != 0)
+  // the status word (first 256 bytes) and the meta block with the router's near-tie list
+  // counters (next 256 bytes)
+  if (ws == nullptr || ws_bytes < 512 || (reinterpret_cast<uintptr_t>(ws) % 256) != 0)
     return MOE_ERR_WORKSPACE;
-  return cuda_status(cudaMemsetAsync(ws, 0, sizeof(int), (cudaStream_t)stream));
+  return cuda_status(cudaMemsetAsync(ws, 0, 512, (cudaStream_t)stream));
 }
 
 moe_status moe_route(const moe_config* cfg, const uint16_t* x, const uint16_t* W_g,

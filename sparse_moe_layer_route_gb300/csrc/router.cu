@@ -8,12 +8,15 @@
 // (logits - log(-log u)) / tau from "GPT-4 Has 1.8 Trillion Parameters. It Uses 2% of Them Per
 // Token", §3.1 门控网络.
 //
-// One CTA per 128 tokens. Warp 0 streams x tiles [128 x 64] (K-major) and W_g chunks [64 x 64]
-// (expert-major, i.e. N-major) with TMA into a 4-stage ring; warp 1 issues
-// tcgen05.mma (M=128, N=E rounded up to 64, K=16); warps 4-7 each own 32 tokens (TMEM lanes):
-// a thread turns its token's logits into selection scores 32 columns at a time, stages them in
-// shared memory (its own row, bank-conflict-free), then takes the top-(k+1) by k+1 branch-free
-// argmax passes over that row.
+// Three kernels (plus the per-call weight preparation):
+//  * router_gemm_kernel: CTA (row tile of 128 tokens, K slice). Warp 0 streams x tiles [128 x 64]
+//    (K-major) and W_g chunks [64 x 64] (expert-major, i.e. N-major) with TMA; warp 1 issues
+//    tcgen05.mma (M=128, N=E rounded up to 64, K=16) into TMEM; warps 4-7 write the fp32 partial
+//    logits of the slice. Splitting K fills the GPU when T is small (one row tile at decode).
+//  * select_kernel: per token, the K-slice partials summed in slice order, selection scores,
+//    top-(k+1) by k+1 branch-free argmax passes over scores staged in shared memory (two threads
+//    per token, four independent chains each), softmax gates, and the near-tie test.
+//  * refine_kernel: the exact re-decision of the near-tie tokens (below).
 //
 // Exactness. The tensor core's fp32 accumulation differs from an exactly rounded dot product by
 // up to ~4e-5 on unit-scale logits at d = 7168 (measured), which is above the 1e-5 near-tie
@@ -23,7 +26,8 @@
 // expert whose tensor-core score lies within the band of the k-th score (only those can be in
 // the exact top-k). refine_kernel recomputes the candidates' logits as plain fp32 dot products
 // (error ~1e-7) and re-decides the token's top-k and gates. Tokens outside the band cannot change
-// their selection or order under the tensor-core error.
+// their selection or order under the tensor-core error. Flagged tokens are appended to a list
+// (order irrelevant: each token is re-decided on its own), spread over all refine CTAs.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <climits>
@@ -52,22 +56,7 @@ struct RCfg {
   static constexpr int kStageBytes = kABytes + NCH * kChunkBytes;
   static constexpr int kStages = (192 * 1024 / kStageBytes) > 8 ? 8 : (192 * 1024 / kStageBytes);
   static constexpr int kTmemCols = EP <= 64 ? 64 : (EP <= 128 ? 128 : 256);
-  static constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 256 + 256 * 4;
-  // the epilogue stages scores [128 tokens][EP + 1] and the selection scratch (9 x 128 words)
-  // in the (then idle) stage buffers
-  static_assert((128 * (EP + 1) + 9 * 128) * 4 <= kStages * kStageBytes, "score staging fits");
-};
-
-struct RouterArgs {
-  const float* bias;
-  const float* u;
-  int32_t* topk_idx;
-  float* topk_w;
-  int32_t* ncand;  // [T]: 0 = decided; n > 0 = near-tie with n candidates; -1 = recompute all E
-  int32_t* cand;   // [T, kMaxCand] candidate experts of near-tie tokens
-  int* status;
-  int T, E, k, mode, k_blocks, d;
-  float tau;
+  static constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 256;
 };
 
 // Half-width of the band around a gap inside which the tensor-core logits could misorder two
@@ -93,10 +82,12 @@ __device__ __forceinline__ bool beats(float sa, int ea, float sb, int eb) {
   return sa > sb || (sa == sb && ea < eb);
 }
 
+// Partial logits of one K slice: part[split][t][0, EP) (fp32; columns >= E are zero).
 template <int NCH>
 __global__ void __launch_bounds__(kThreads, 1)
-    router_tc_kernel(const __grid_constant__ CUtensorMap tmX,
-                     const __grid_constant__ CUtensorMap tmW, const RouterArgs a) {
+    router_gemm_kernel(const __grid_constant__ CUtensorMap tmX,
+                       const __grid_constant__ CUtensorMap tmW, float* __restrict__ part, int T,
+                       int kb_per_split, int k_blocks, int* status) {
   using C = RCfg<NCH>;
   constexpr int kStages = C::kStages;
   constexpr uint32_t IDESC = ptx::idesc_f16kind_f32(kBM, C::EP, 0, 1, 1);
@@ -114,16 +105,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       reinterpret_cast<uint32_t*>(gbase + kStages * C::kStageBytes + 8 * (2 * kStages + 2));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* never = reinterpret_cast<volatile int*>(tmem_slot + 2);  // stays 0
-  float* bias_s = reinterpret_cast<float*>(gbase + kStages * C::kStageBytes + 256);
-  // selection scratch (valid once the MMAs are done): scores [128][kLD], per-token max |logit|,
-  // and the two halves' per-pass picks (double-buffered by pass parity)
-  constexpr int kLD = C::EP + 1;
-  float* sel_maxl = reinterpret_cast<float*>(gbase) + kBM * kLD;
-  float(*sel_s)[2][kBM] = reinterpret_cast<float(*)[2][kBM]>(sel_maxl + kBM);
-  int(*sel_e)[2][kBM] = reinterpret_cast<int(*)[2][kBM]>(sel_maxl + kBM + 4 * kBM);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m0 = blockIdx.x * kBM;
+  const int split = blockIdx.y;
+  const int kb0 = split * kb_per_split;
+  const int kb1 = min(k_blocks, kb0 + kb_per_split);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -142,23 +129,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tmem_alloc(ptx::smem_u32(tmem_slot), C::kTmemCols);
     ptx::tmem_relinquish();
   }
-  griddep_wait();  // the setup above touched only shared memory, TMEM and parameters
-  if (warp == 3) {
-    for (int e = lane; e < a.E; e += 32)
-      bias_s[e] = (a.mode == MOE_ROUTE_BIAS_SELECT) ? a.bias[e] : 0.f;
-  }
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  griddep_wait();  // the setup above touched only shared memory, TMEM and parameters
 
   if (warp == 0) {
     if (lane == 0) {
       // -------------------------------------------------------------- TMA producer
       int stage = 0;
       uint32_t phase = 0, issued = 0, last_par = 0;
-      for (int kb = 0; kb < a.k_blocks; ++kb) {
-        if (!ptx::mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, a.status,
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!ptx::mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, status,
                                     MOE_DEVFAULT_PIPELINE_TIMEOUT, kWaitLimitNs))
           break;
         const uint32_t sA = base + stage * C::kStageBytes;
@@ -176,10 +159,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       for (int s = 0; s < kStages; ++s)
-        if (issued & (1u << s)) {
-          ptx::mbar_wait_bounded(full_bar(s), (last_par >> s) & 1u, never, a.status,
+        if (issued & (1u << s))
+          ptx::mbar_wait_bounded(full_bar(s), (last_par >> s) & 1u, never, status,
                                  MOE_DEVFAULT_PIPELINE_TIMEOUT, kWaitLimitNs / 4);
-        }
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -188,8 +170,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int kb = 0; kb < a.k_blocks; ++kb) {
-        if (!ptx::mbar_wait_bounded(full_bar(stage), phase, abort_flag, a.status,
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!ptx::mbar_wait_bounded(full_bar(stage), phase, abort_flag, status,
                                     MOE_DEVFAULT_PIPELINE_TIMEOUT, kWaitLimitNs)) {
           ok = false;
           break;
@@ -201,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < kBK / 16; ++kk) {
           const uint64_t adesc = ptx::smem_desc_sw128(sA + kk * 32, 16, 1024);
           const uint64_t bdesc = ptx::smem_desc_sw128(sB + kk * 2048, kChunkBytes, 1024);
-          ptx::umma_f16(tmem_base, adesc, bdesc, IDESC, (kb | kk) != 0 ? 1u : 0u);
+          ptx::umma_f16(tmem_base, adesc, bdesc, IDESC, (kb > kb0 || kk) ? 1u : 0u);
         }
         ptx::umma_commit(empty_bar(stage));
         if (++stage == kStages) {
@@ -211,154 +193,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (ok) ptx::umma_commit(acc_bar);
       ptx::umma_commit(done_bar);
-      ptx::mbar_wait_bounded(done_bar, 0, never, a.status, MOE_DEVFAULT_PIPELINE_TIMEOUT,
+      ptx::mbar_wait_bounded(done_bar, 0, never, status, MOE_DEVFAULT_PIPELINE_TIMEOUT,
                              kWaitLimitNs / 4);
     }
     __syncwarp();
   } else if (warp >= 4) {
-    // ---------------------------------------------------------------- epilogue 1: stage scores
+    // ---------------------------------------------------------------- epilogue: partials out
     const int q = warp - 4;
-    const int r = 32 * q + lane;  // this thread's token within the tile
-    const int t = m0 + r;
-    const bool ok = ptx::mbar_wait_bounded(acc_bar, 0, abort_flag, a.status,
-                                           MOE_DEVFAULT_PIPELINE_TIMEOUT, kWaitLimitNs);
-    if (ok) {
+    const int t = m0 + 32 * q + lane;
+    if (ptx::mbar_wait_bounded(acc_bar, 0, abort_flag, status, MOE_DEVFAULT_PIPELINE_TIMEOUT,
+                               kWaitLimitNs)) {
       ptx::tc_fence_after();
-      // every MMA has completed, so the stage buffers are free: scores [128][EP + 1]
-      float* srow = reinterpret_cast<float*>(gbase) + r * kLD;
       const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16);
-      const bool row_ok = t < a.T;
-      const bool gumbel = a.mode == MOE_ROUTE_GUMBEL;
-      float max_abs_l = 0.f;
+      float* dst = part + ((size_t)split * T + t) * C::EP;
 #pragma unroll 1
       for (int c = 0; c < C::EP / 32; ++c) {
         uint32_t v[32];
         ptx::tmem_ld_32x32b_x32(taddr + c * 32, v);
         ptx::tmem_wait_ld();
+        if (t < T) {
+          float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int e = c * 32 + i;
-          const float l = __uint_as_float(v[i]);
-          float sc = -INFINITY;
-          if (row_ok && e < a.E) {
-            max_abs_l = fmaxf(max_abs_l, fabsf(l));
-            sc = selection_score(a.mode, l, bias_s[e], gumbel ? a.u[(size_t)t * a.E + e] : 0.f,
-                                 a.tau);
-          }
-          srow[e] = sc;
-        }
-      }
-      sel_maxl[r] = max_abs_l;
-    }
-  }
-
-  // ------------------------------------------------------------------ epilogue 2: selection
-  // All 256 threads: thread (r, h) scans half h of token r's experts; each pass picks the best
-  // expert strictly after the previous pick in (score desc, index asc) order, with four
-  // independent chains per thread; the two halves merge through shared memory.
-  __syncthreads();
-  if (!*abort_flag) {
-    const int r = threadIdx.x & (kBM - 1), h = threadIdx.x >> 7;
-    const int t = m0 + r;
-    const bool row_ok = t < a.T;
-    const float* srow = reinterpret_cast<const float*>(gbase) + r * kLD;
-    const int k = a.k;
-    const int nl = k < a.E ? k + 1 : k;  // top-(k+1), or all E when k == E
-    const int half = (a.E + 1) / 2;
-    const int e_lo = h * half, e_hi = min(a.E, e_lo + half);
-    float ts[kList];
-    int te[kList];
-    float ps = INFINITY;
-    int pe = -1;
-#pragma unroll
-    for (int j = 0; j < kList; ++j) {
-      ts[j] = -INFINITY;
-      te[j] = INT_MAX;
-      if (j < nl) {  // uniform: nl depends on k and E only
-        float bs[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        int be[4] = {INT_MAX, INT_MAX, INT_MAX, INT_MAX};
-        if (row_ok) {
-          for (int e = e_lo; e < e_hi; e += 4) {
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              const int ee = e + c;
-              if (ee < e_hi) {
-                const float sc = srow[ee];
-                const bool after = sc < ps || (sc == ps && ee > pe);
-                if (after && beats(sc, ee, bs[c], be[c])) {
-                  bs[c] = sc;
-                  be[c] = ee;
-                }
-              }
-            }
-          }
-        }
-#pragma unroll
-        for (int c = 1; c < 4; ++c)
-          if (beats(bs[c], be[c], bs[0], be[0])) {
-            bs[0] = bs[c];
-            be[0] = be[c];
-          }
-        sel_s[j & 1][h][r] = bs[0];
-        sel_e[j & 1][h][r] = be[0];
-        __syncthreads();
-        const float os = sel_s[j & 1][h ^ 1][r];
-        const int oe = sel_e[j & 1][h ^ 1][r];
-        if (beats(os, oe, bs[0], be[0])) {
-          bs[0] = os;
-          be[0] = oe;
-        }
-        ts[j] = bs[0];
-        te[j] = be[0];
-        ps = bs[0];
-        pe = be[0];
-      }
-    }
-    if (row_ok && h == 0) {
-      const bool gumbel = a.mode == MOE_ROUTE_GUMBEL;
-      // near-tie test (scores in their own units: GUMBEL scores carry 1/tau)
-      float min_gap = INFINITY, sk = ts[0];
-#pragma unroll
-      for (int j = 1; j < kList; ++j) {
-        if (j < nl) min_gap = fminf(min_gap, ts[j - 1] - ts[j]);
-        if (j == k - 1) sk = ts[j];
-      }
-      float band = router_band(a.d, sel_maxl[r]);
-      if (gumbel) band /= a.tau;
-      int nc = 0;
-      if (min_gap < band) {
-        // candidates: every expert scoring within the band of the k-th score
-        for (int e = 0; e < a.E; ++e) {
-          if (srow[e] >= sk - band) {
-            if (nc < kMaxCand) a.cand[(size_t)t * kMaxCand + nc] = e;
-            ++nc;
-          }
-        }
-        nc = nc <= kMaxCand ? nc : -1;
-      }
-      a.ncand[t] = nc;
-      // gates: softmax over the selected logits (PLAIN: the score; BIAS_SELECT: score - bias,
-      // within one rounding of the logit) or over the selected scores (GUMBEL)
-      float av[kMaxK];
-#pragma unroll
-      for (int j = 0; j < kMaxK; ++j)
-        av[j] = (a.mode == MOE_ROUTE_BIAS_SELECT && j < k) ? ts[j] - bias_s[te[j]] : ts[j];
-      float mx = av[0];
-#pragma unroll
-      for (int j = 1; j < kMaxK; ++j)
-        if (j < k) mx = fmaxf(mx, av[j]);
-      float sum = 0.f;
-#pragma unroll
-      for (int j = 0; j < kMaxK; ++j) {
-        av[j] = (j < k) ? expf(av[j] - mx) : 0.f;
-        sum += av[j];
-      }
-      const float inv = 1.0f / sum;
-#pragma unroll
-      for (int j = 0; j < kMaxK; ++j) {
-        if (j < k) {
-          a.topk_idx[(size_t)t * k + j] = te[j];
-          a.topk_w[(size_t)t * k + j] = av[j] * inv;
+          for (int i = 0; i < 8; ++i)
+            d4[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
         }
       }
     }
@@ -369,6 +227,175 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 2) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+struct SelectArgs {
+  const float* part;
+  const float* bias;
+  const float* u;
+  int32_t* topk_idx;
+  float* topk_w;
+  int32_t* ncand;     // [T]: 0 = decided; n > 0 = near-tie with n candidates; -1 = all E
+  int32_t* cand;      // [T, kMaxCand]
+  int32_t* rlist;     // near-tie tokens, appended
+  int* rcount;        // their number (reset to 0 by the refine kernel when it finishes)
+  int T, E, EP, k, mode, d, splits;
+  float tau;
+};
+
+// Two threads per token (scores [128][EP + 1] staged in dynamic shared memory).
+__global__ void __launch_bounds__(kThreads) select_kernel(const SelectArgs a) {
+  extern __shared__ float ssm[];
+  const int LD = a.EP + 1;
+  float* scores = ssm;                                   // [128][LD]
+  float* maxl = scores + kBM * LD;                       // [128] (+128 spare)
+  float* sel_s = maxl + 2 * kBM;                         // [2 parity][2 halves][128]
+  int* sel_e = reinterpret_cast<int*>(sel_s + 4 * kBM);  // [2][2][128]
+  griddep_wait();
+  const bool gumbel = a.mode == MOE_ROUTE_GUMBEL;
+  const int t0 = blockIdx.x * kBM;
+  // phase 1: all threads read the block's partial-logit tiles with coalesced 16-byte loads,
+  // adding the K slices in slice order, and turn each logit into its selection score
+  int* maxl_bits = reinterpret_cast<int*>(maxl);  // |logit| >= 0: int order = float order
+  if (threadIdx.x < kBM) maxl_bits[threadIdx.x] = 0;
+  __syncthreads();
+  {
+    const int ep4 = a.EP / 4;
+    const float4* P = reinterpret_cast<const float4*>(a.part);
+    for (int i = threadIdx.x; i < kBM * ep4; i += kThreads) {
+      const int rr = i / ep4, c = (i - rr * ep4) * 4;
+      const int tt = t0 + rr;
+      if (tt >= a.T) continue;
+      float4 acc = P[(size_t)tt * ep4 + c / 4];
+#pragma unroll 4
+      for (int sp = 1; sp < a.splits; ++sp) {
+        const float4 v = P[((size_t)sp * a.T + tt) * ep4 + c / 4];
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
+      }
+      const float lv[4] = {acc.x, acc.y, acc.z, acc.w};
+      float m = 0.f;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int e = c + q;
+        float sc = -INFINITY;
+        if (e < a.E) {
+          m = fmaxf(m, fabsf(lv[q]));
+          sc = selection_score(a.mode, lv[q],
+                               a.mode == MOE_ROUTE_BIAS_SELECT ? a.bias[e] : 0.f,
+                               gumbel ? a.u[(size_t)tt * a.E + e] : 0.f, a.tau);
+        }
+        scores[rr * LD + e] = sc;
+      }
+      atomicMax(&maxl_bits[rr], __float_as_int(m));
+    }
+  }
+  __syncthreads();
+  const int r = threadIdx.x & (kBM - 1), h = threadIdx.x >> 7;
+  const int t = t0 + r;
+  const bool row_ok = t < a.T;
+  const float* srow = scores + r * LD;
+  const int half = (a.E + 1) / 2;
+  const int e_lo = h * half, e_hi = min(a.E, e_lo + half);
+  const int k = a.k;
+  const int nl = k < a.E ? k + 1 : k;  // top-(k+1), or all E when k == E
+  float ts[kList];
+  int te[kList];
+  float ps = INFINITY;
+  int pe = -1;
+#pragma unroll
+  for (int j = 0; j < kList; ++j) {
+    ts[j] = -INFINITY;
+    te[j] = INT_MAX;
+    if (j < nl) {  // uniform across the CTA
+      float bs[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      int be[4] = {INT_MAX, INT_MAX, INT_MAX, INT_MAX};
+      if (row_ok) {
+        for (int e = e_lo; e < e_hi; e += 4) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int ee = e + c;
+            if (ee < e_hi) {
+              const float sc = srow[ee];
+              const bool after = sc < ps || (sc == ps && ee > pe);
+              if (after && beats(sc, ee, bs[c], be[c])) {
+                bs[c] = sc;
+                be[c] = ee;
+              }
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int c = 1; c < 4; ++c)
+        if (beats(bs[c], be[c], bs[0], be[0])) {
+          bs[0] = bs[c];
+          be[0] = be[c];
+        }
+      sel_s[((j & 1) * 2 + h) * kBM + r] = bs[0];
+      sel_e[((j & 1) * 2 + h) * kBM + r] = be[0];
+      __syncthreads();
+      const float os = sel_s[((j & 1) * 2 + (h ^ 1)) * kBM + r];
+      const int oe = sel_e[((j & 1) * 2 + (h ^ 1)) * kBM + r];
+      if (beats(os, oe, bs[0], be[0])) {
+        bs[0] = os;
+        be[0] = oe;
+      }
+      ts[j] = bs[0];
+      te[j] = be[0];
+      ps = bs[0];
+      pe = be[0];
+    }
+  }
+  if (!row_ok || h != 0) return;
+  // near-tie test (scores in their own units: GUMBEL scores carry 1/tau)
+  float min_gap = INFINITY, sk = ts[0];
+#pragma unroll
+  for (int j = 1; j < kList; ++j) {
+    if (j < nl) min_gap = fminf(min_gap, ts[j - 1] - ts[j]);
+    if (j == k - 1) sk = ts[j];
+  }
+  float band = router_band(a.d, maxl[r]);
+  if (gumbel) band /= a.tau;
+  int nc = 0;
+  if (min_gap < band) {
+    // candidates: every expert scoring within the band of the k-th score
+    for (int e = 0; e < a.E; ++e) {
+      if (srow[e] >= sk - band) {
+        if (nc < kMaxCand) a.cand[(size_t)t * kMaxCand + nc] = e;
+        ++nc;
+      }
+    }
+    nc = nc <= kMaxCand ? nc : -1;
+    a.rlist[atomicAdd(a.rcount, 1)] = t;
+  }
+  a.ncand[t] = nc;
+  // gates: softmax over the selected logits (PLAIN: the score; BIAS_SELECT: score - bias,
+  // within one rounding of the logit) or over the selected scores (GUMBEL)
+  float av[kMaxK];
+#pragma unroll
+  for (int j = 0; j < kMaxK; ++j)
+    av[j] = (a.mode == MOE_ROUTE_BIAS_SELECT && j < k) ? ts[j] - a.bias[te[j]] : ts[j];
+  float mx = av[0];
+#pragma unroll
+  for (int j = 1; j < kMaxK; ++j)
+    if (j < k) mx = fmaxf(mx, av[j]);
+  float sum = 0.f;
+#pragma unroll
+  for (int j = 0; j < kMaxK; ++j) {
+    av[j] = (j < k) ? expf(av[j] - mx) : 0.f;
+    sum += av[j];
+  }
+  const float inv = 1.0f / sum;
+#pragma unroll
+  for (int j = 0; j < kMaxK; ++j) {
+    if (j < k) {
+      a.topk_idx[(size_t)t * k + j] = te[j];
+      a.topk_w[(size_t)t * k + j] = av[j] * inv;
+    }
   }
 }
 
@@ -405,30 +432,17 @@ __global__ void __launch_bounds__(kThreads) prep_router_kernel(const uint16_t* _
 __global__ void __launch_bounds__(kThreads) refine_kernel(
     const uint16_t* __restrict__ x, const uint16_t* __restrict__ WT, const float* __restrict__ bias,
     const float* __restrict__ u, const int32_t* __restrict__ ncand,
-    const int32_t* __restrict__ cand, int32_t* __restrict__ topk_idx,
-    float* __restrict__ topk_w, int T, int d, int E, int k, int mode, float tau) {
+    const int32_t* __restrict__ cand, const int32_t* __restrict__ rlist, int* rcount, int* rdone,
+    int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, int T, int d, int E, int k,
+    int mode, float tau) {
   __shared__ float red[kThreads / 32][kMaxCand];
   __shared__ int ce[256];
   __shared__ float cl[256], cs[256];
-  __shared__ int flagged[kThreads];
-  __shared__ int n_flagged;
   griddep_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // this CTA's contiguous chunk of tokens; their flags are read 256 at a time in one round
-  const int chunk = (T + gridDim.x - 1) / gridDim.x;
-  const int t_begin = blockIdx.x * chunk;
-  const int t_end = min(T, t_begin + chunk);
-  for (int base = t_begin; base < t_end; base += kThreads) {
-    if (threadIdx.x == 0) n_flagged = 0;
-    __syncthreads();
-    {
-      const int tt = base + threadIdx.x;
-      if (tt < t_end && ncand[tt] != 0) flagged[atomicAdd(&n_flagged, 1)] = tt;
-    }
-    __syncthreads();
-    const int nf = n_flagged;
-  for (int fi = 0; fi < nf; ++fi) {
-    const int t = flagged[fi];
+  const int nf = *(volatile int*)rcount;
+  for (int fi = blockIdx.x; fi < nf; fi += gridDim.x) {
+    const int t = rlist[fi];
     const int n_c = ncand[t];
     const int nc = n_c > 0 ? n_c : E;
     for (int i = threadIdx.x; i < nc; i += kThreads)
@@ -512,67 +526,98 @@ __global__ void __launch_bounds__(kThreads) refine_kernel(
     }
     __syncthreads();
   }
-    __syncthreads();  // the flag list is rebuilt for the next chunk only after every reader
+  // the last CTA to finish resets the list for the next call (all CTAs have read the count)
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(rdone, 1) == (int)gridDim.x - 1) {
+      *rcount = 0;
+      *rdone = 0;
+    }
   }
 }
 
 template <int NCH>
-cudaError_t launch_tc(const CUtensorMap& mx, const CUtensorMap& mw, const RouterArgs& a, int grid,
-                      cudaStream_t st) {
+cudaError_t launch_gemm(const CUtensorMap& mx, const CUtensorMap& mw, float* part, int T,
+                        int n_mt, int splits, int kb_per_split, int k_blocks, int* status,
+                        cudaStream_t st) {
   using C = RCfg<NCH>;
-  cudaError_t err = cudaFuncSetAttribute(router_tc_kernel<NCH>,
+  cudaError_t err = cudaFuncSetAttribute(router_gemm_kernel<NCH>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmemBytes);
   if (err != cudaSuccess) return err;
-  return launch_k(router_tc_kernel<NCH>, dim3(grid), dim3(kThreads), C::kSmemBytes, st, mx, mw,
-                  a);
+  return launch_k(router_gemm_kernel<NCH>, dim3(n_mt, splits), dim3(kThreads), C::kSmemBytes, st,
+                  mx, mw, part, T, kb_per_split, k_blocks, status);
 }
 
 }  // namespace
 
+int router_splits(int T, int d) {
+  const int n_mt = (T + kBM - 1) / kBM;
+  const int k_blocks = d / kBK;
+  int sp = 152 / n_mt;  // fill the GPU's SMs with (row tile, K slice) CTAs
+  // at most 8 slices (the selection reads every slice) and at least 4 K blocks per slice
+  const int cap = k_blocks / 4 < 8 ? (k_blocks / 4 > 1 ? k_blocks / 4 : 1) : 8;
+  if (sp > cap) sp = cap;
+  if (sp < 1) sp = 1;
+  const int kbs = (k_blocks + sp - 1) / sp;  // no empty slice
+  return (k_blocks + kbs - 1) / kbs;
+}
+
 cudaError_t launch_router(const Shape& s, const uint16_t* x, const uint16_t* W_g,
                           const float* bias, const float* u, int32_t* topk_idx, float* topk_w,
-                          uint16_t* wg_pad, uint16_t* wg_t, int32_t* ncand, int32_t* cand,
-                          int* status, cudaStream_t st) {
+                          const RouterScratch& rs, int* status, cudaStream_t st) {
   const int EP = (s.E + 63) / 64 * 64;
-  const uint16_t* W = EP != s.E ? wg_pad : W_g;
+  const uint16_t* W = EP != s.E ? rs.wg_pad : W_g;
   {
     const dim3 grid((s.d + 31) / 32, (EP + 31) / 32);
-    const cudaError_t e = launch_k(prep_router_kernel, grid, dim3(kThreads), 0, st, W_g, wg_t,
-                                   EP != s.E ? wg_pad : nullptr, s.d, s.E, EP);
+    const cudaError_t e = launch_k(prep_router_kernel, grid, dim3(kThreads), 0, st, W_g, rs.wg_t,
+                                   EP != s.E ? rs.wg_pad : nullptr, s.d, s.E, EP);
     if (e != cudaSuccess) return e;
   }
   CUtensorMap mx, mw;
   if (!make_tmap_2d(&mx, x, s.T, s.d, kBK, kBM) || !make_tmap_2d(&mw, W, s.d, EP, 64, kBK))
     return cudaErrorInvalidValue;
-  RouterArgs a;
+  const int n_mt = (s.T + kBM - 1) / kBM;
+  const int k_blocks = s.d / kBK;
+  const int splits = router_splits(s.T, s.d);
+  const int kbs = (k_blocks + splits - 1) / splits;
+  cudaError_t err;
+  switch (EP / 64) {
+    case 1: err = launch_gemm<1>(mx, mw, rs.part, s.T, n_mt, splits, kbs, k_blocks, status, st); break;
+    case 2: err = launch_gemm<2>(mx, mw, rs.part, s.T, n_mt, splits, kbs, k_blocks, status, st); break;
+    case 3: err = launch_gemm<3>(mx, mw, rs.part, s.T, n_mt, splits, kbs, k_blocks, status, st); break;
+    default: err = launch_gemm<4>(mx, mw, rs.part, s.T, n_mt, splits, kbs, k_blocks, status, st); break;
+  }
+  if (err != cudaSuccess) return err;
+  SelectArgs a;
+  a.part = rs.part;
   a.bias = bias;
   a.u = u;
   a.topk_idx = topk_idx;
   a.topk_w = topk_w;
-  a.ncand = ncand;
-  a.cand = cand;
-  a.status = status;
-  a.d = s.d;
+  a.ncand = rs.ncand;
+  a.cand = rs.cand;
+  a.rlist = rs.rlist;
+  a.rcount = rs.rcount;
   a.T = s.T;
   a.E = s.E;
+  a.EP = EP;
   a.k = s.k;
   a.mode = s.mode;
-  a.k_blocks = s.d / kBK;
+  a.d = s.d;
+  a.splits = splits;
   a.tau = s.tau;
-  const int grid = (s.T + kBM - 1) / kBM;
-  cudaError_t err;
-  switch (EP / 64) {
-    case 1: err = launch_tc<1>(mx, mw, a, grid, st); break;
-    case 2: err = launch_tc<2>(mx, mw, a, grid, st); break;
-    case 3: err = launch_tc<3>(mx, mw, a, grid, st); break;
-    default: err = launch_tc<4>(mx, mw, a, grid, st); break;
-  }
+  const size_t smem = sizeof(float) * ((size_t)kBM * (EP + 1) + 2 * kBM + 8 * kBM);
+  err = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
   if (err != cudaSuccess) return err;
-  const int rgrid = s.T < 2 * num_sms() ? s.T : 2 * num_sms();
-  return launch_k(refine_kernel, dim3(rgrid), dim3(kThreads), 0, st, x, (const uint16_t*)wg_t,
-                  bias, u, (const int32_t*)ncand, (const int32_t*)cand, topk_idx, topk_w, s.T, s.d,
-                  s.E, s.k, s.mode, s.tau);
+  err = launch_k(select_kernel, dim3(n_mt), dim3(kThreads), smem, st, a);
+  if (err != cudaSuccess) return err;
+  const int rgrid = 2 * num_sms();
+  return launch_k(refine_kernel, dim3(rgrid), dim3(kThreads), 0, st, x, (const uint16_t*)rs.wg_t,
+                  bias, u, (const int32_t*)rs.ncand, (const int32_t*)rs.cand,
+                  (const int32_t*)rs.rlist, rs.rcount, rs.rdone, topk_idx, topk_w, s.T, s.d, s.E,
+                  s.k, s.mode, s.tau);
 }
 
 }  // namespace moe
