@@ -244,38 +244,48 @@ struct SelectArgs {
   float tau;
 };
 
-// Two threads per token (scores [128][EP + 1] staged in dynamic shared memory).
+// Two threads per token (scores [128][EP + 4] staged in dynamic shared memory: rows stay 16-byte
+// aligned and 128-bit reads of consecutive rows hit distinct banks). The pass loop is kept rolled
+// (its picks live in shared memory) so the kernel's code stays small.
 __global__ void __launch_bounds__(kThreads) select_kernel(const SelectArgs a) {
-  extern __shared__ float ssm[];
-  const int LD = a.EP + 1;
-  float* scores = ssm;                                   // [128][LD]
-  float* maxl = scores + kBM * LD;                       // [128] (+128 spare)
-  float* sel_s = maxl + 2 * kBM;                         // [2 parity][2 halves][128]
-  int* sel_e = reinterpret_cast<int*>(sel_s + 4 * kBM);  // [2][2][128]
+  extern __shared__ __align__(16) float ssm[];
+  const int LD = a.EP + 4;
+  float* scores = ssm;                                      // [128][LD]
+  float* maxl = scores + kBM * LD;                          // [128]
+  float* sel_s = maxl + kBM;                                // [2 parity][2 halves][128]
+  int* sel_e = reinterpret_cast<int*>(sel_s + 4 * kBM);     // [2][2][128]
+  float* pick_s = reinterpret_cast<float*>(sel_e + 4 * kBM);  // [kList][128]
+  int* pick_e = reinterpret_cast<int*>(pick_s + kList * kBM);  // [kList][128]
   griddep_wait();
   const bool gumbel = a.mode == MOE_ROUTE_GUMBEL;
   const int t0 = blockIdx.x * kBM;
-  // phase 1: all threads read the block's partial-logit tiles with coalesced 16-byte loads,
-  // adding the K slices in slice order, and turn each logit into its selection score
+  // phase 1: all threads read the block's partial-logit tiles with coalesced 16-byte loads
+  // (every K slice of four groups in flight together), add the slices in slice order, and turn
+  // each logit into its selection score
   int* maxl_bits = reinterpret_cast<int*>(maxl);  // |logit| >= 0: int order = float order
   if (threadIdx.x < kBM) maxl_bits[threadIdx.x] = 0;
   __syncthreads();
   {
     const int ep4 = a.EP / 4;
-    const float4* P = reinterpret_cast<const float4*>(a.part);
-    for (int i = threadIdx.x; i < kBM * ep4; i += kThreads) {
+    const float4* __restrict__ P = reinterpret_cast<const float4*>(a.part);
+    const int rows = min(kBM, a.T - t0);
+#pragma unroll 4
+    for (int i = threadIdx.x; i < rows * ep4; i += kThreads) {
       const int rr = i / ep4, c = (i - rr * ep4) * 4;
       const int tt = t0 + rr;
-      if (tt >= a.T) continue;
-      float4 acc = P[(size_t)tt * ep4 + c / 4];
-#pragma unroll 4
-      for (int sp = 1; sp < a.splits; ++sp) {
-        const float4 v = P[((size_t)sp * a.T + tt) * ep4 + c / 4];
-        acc.x += v.x;
-        acc.y += v.y;
-        acc.z += v.z;
-        acc.w += v.w;
-      }
+      float4 v[8];
+#pragma unroll
+      for (int sp = 0; sp < 8; ++sp)
+        if (sp < a.splits) v[sp] = __ldg(P + ((size_t)sp * a.T + tt) * ep4 + c / 4);
+      float4 acc = v[0];
+#pragma unroll
+      for (int sp = 1; sp < 8; ++sp)
+        if (sp < a.splits) {
+          acc.x += v[sp].x;
+          acc.y += v[sp].y;
+          acc.z += v[sp].z;
+          acc.w += v[sp].w;
+        }
       const float lv[4] = {acc.x, acc.y, acc.z, acc.w};
       float m = 0.f;
 #pragma unroll
@@ -285,8 +295,8 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const SelectArgs a) {
         if (e < a.E) {
           m = fmaxf(m, fabsf(lv[q]));
           sc = selection_score(a.mode, lv[q],
-                               a.mode == MOE_ROUTE_BIAS_SELECT ? a.bias[e] : 0.f,
-                               gumbel ? a.u[(size_t)tt * a.E + e] : 0.f, a.tau);
+                               a.mode == MOE_ROUTE_BIAS_SELECT ? __ldg(a.bias + e) : 0.f,
+                               gumbel ? __ldg(a.u + (size_t)tt * a.E + e) : 0.f, a.tau);
         }
         scores[rr * LD + e] = sc;
       }
@@ -298,66 +308,71 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const SelectArgs a) {
   const int t = t0 + r;
   const bool row_ok = t < a.T;
   const float* srow = scores + r * LD;
-  const int half = (a.E + 1) / 2;
+  const int half = ((a.E + 1) / 2 + 3) & ~3;  // multiple of 4: float4 reads
   const int e_lo = h * half, e_hi = min(a.E, e_lo + half);
   const int k = a.k;
   const int nl = k < a.E ? k + 1 : k;  // top-(k+1), or all E when k == E
-  float ts[kList];
-  int te[kList];
+  // pass j: the best expert strictly after pick j-1 in (score desc, index asc) order
   float ps = INFINITY;
   int pe = -1;
+#pragma unroll 1
+  for (int j = 0; j < nl; ++j) {
+    float bs[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    int be[4] = {INT_MAX, INT_MAX, INT_MAX, INT_MAX};
+    if (row_ok) {
+      // 16 scores per step: four 128-bit reads issued together, one chain per read
+      const float4* s4 = reinterpret_cast<const float4*>(srow);
+#pragma unroll 1
+      for (int e = e_lo; e < e_hi; e += 16) {
+        float4 v[4];
 #pragma unroll
-  for (int j = 0; j < kList; ++j) {
-    ts[j] = -INFINITY;
-    te[j] = INT_MAX;
-    if (j < nl) {  // uniform across the CTA
-      float bs[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-      int be[4] = {INT_MAX, INT_MAX, INT_MAX, INT_MAX};
-      if (row_ok) {
-        for (int e = e_lo; e < e_hi; e += 4) {
+        // may read up to 12 floats past this row (the next row, or for the last row the arrays
+        // that follow it in shared memory); those lanes fail the ee < e_hi test below
+        for (int c = 0; c < 4; ++c) v[c] = s4[(e >> 2) + c];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int ee = e + c;
-            if (ee < e_hi) {
-              const float sc = srow[ee];
-              const bool after = sc < ps || (sc == ps && ee > pe);
-              if (after && beats(sc, ee, bs[c], be[c])) {
-                bs[c] = sc;
-                be[c] = ee;
-              }
+        for (int c = 0; c < 4; ++c) {
+          const float vv[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int ee = e + 4 * c + q;
+            const float sc = vv[q];
+            const bool after = sc < ps || (sc == ps && ee > pe);
+            if (ee < e_hi && after && beats(sc, ee, bs[c], be[c])) {
+              bs[c] = sc;
+              be[c] = ee;
             }
           }
         }
       }
-#pragma unroll
-      for (int c = 1; c < 4; ++c)
-        if (beats(bs[c], be[c], bs[0], be[0])) {
-          bs[0] = bs[c];
-          be[0] = be[c];
-        }
-      sel_s[((j & 1) * 2 + h) * kBM + r] = bs[0];
-      sel_e[((j & 1) * 2 + h) * kBM + r] = be[0];
-      __syncthreads();
-      const float os = sel_s[((j & 1) * 2 + (h ^ 1)) * kBM + r];
-      const int oe = sel_e[((j & 1) * 2 + (h ^ 1)) * kBM + r];
-      if (beats(os, oe, bs[0], be[0])) {
-        bs[0] = os;
-        be[0] = oe;
-      }
-      ts[j] = bs[0];
-      te[j] = be[0];
-      ps = bs[0];
-      pe = be[0];
     }
-  }
-  if (!row_ok || h != 0) return;
-  // near-tie test (scores in their own units: GUMBEL scores carry 1/tau)
-  float min_gap = INFINITY, sk = ts[0];
 #pragma unroll
-  for (int j = 1; j < kList; ++j) {
-    if (j < nl) min_gap = fminf(min_gap, ts[j - 1] - ts[j]);
-    if (j == k - 1) sk = ts[j];
+    for (int c = 1; c < 4; ++c)
+      if (beats(bs[c], be[c], bs[0], be[0])) {
+        bs[0] = bs[c];
+        be[0] = be[c];
+      }
+    sel_s[((j & 1) * 2 + h) * kBM + r] = bs[0];
+    sel_e[((j & 1) * 2 + h) * kBM + r] = be[0];
+    __syncthreads();
+    const float os = sel_s[((j & 1) * 2 + (h ^ 1)) * kBM + r];
+    const int oe = sel_e[((j & 1) * 2 + (h ^ 1)) * kBM + r];
+    if (beats(os, oe, bs[0], be[0])) {
+      bs[0] = os;
+      be[0] = oe;
+    }
+    if (h == 0) {
+      pick_s[j * kBM + r] = bs[0];
+      pick_e[j * kBM + r] = be[0];
+    }
+    ps = bs[0];
+    pe = be[0];
   }
+  if (!row_ok || h != 0) return;  // after the last barrier
+  // near-tie test (scores in their own units: GUMBEL scores carry 1/tau)
+  float min_gap = INFINITY;
+  for (int j = 1; j < nl; ++j)
+    min_gap = fminf(min_gap, pick_s[(j - 1) * kBM + r] - pick_s[j * kBM + r]);
+  const float sk = pick_s[(k - 1) * kBM + r];
   float band = router_band(a.d, maxl[r]);
   if (gumbel) band /= a.tau;
   int nc = 0;
@@ -375,27 +390,25 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const SelectArgs a) {
   a.ncand[t] = nc;
   // gates: softmax over the selected logits (PLAIN: the score; BIAS_SELECT: score - bias,
   // within one rounding of the logit) or over the selected scores (GUMBEL)
-  float av[kMaxK];
-#pragma unroll
-  for (int j = 0; j < kMaxK; ++j)
-    av[j] = (a.mode == MOE_ROUTE_BIAS_SELECT && j < k) ? ts[j] - a.bias[te[j]] : ts[j];
-  float mx = av[0];
-#pragma unroll
-  for (int j = 1; j < kMaxK; ++j)
-    if (j < k) mx = fmaxf(mx, av[j]);
+  float mx = -INFINITY;
+  for (int j = 0; j < k; ++j) {
+    const float s = pick_s[j * kBM + r];
+    const float av = a.mode == MOE_ROUTE_BIAS_SELECT ? s - a.bias[pick_e[j * kBM + r]] : s;
+    mx = fmaxf(mx, av);
+  }
   float sum = 0.f;
-#pragma unroll
-  for (int j = 0; j < kMaxK; ++j) {
-    av[j] = (j < k) ? expf(av[j] - mx) : 0.f;
-    sum += av[j];
+  for (int j = 0; j < k; ++j) {
+    const float s = pick_s[j * kBM + r];
+    const float av = a.mode == MOE_ROUTE_BIAS_SELECT ? s - a.bias[pick_e[j * kBM + r]] : s;
+    sum += expf(av - mx);
   }
   const float inv = 1.0f / sum;
-#pragma unroll
-  for (int j = 0; j < kMaxK; ++j) {
-    if (j < k) {
-      a.topk_idx[(size_t)t * k + j] = te[j];
-      a.topk_w[(size_t)t * k + j] = av[j] * inv;
-    }
+  for (int j = 0; j < k; ++j) {
+    const float s = pick_s[j * kBM + r];
+    const int e = pick_e[j * kBM + r];
+    const float av = a.mode == MOE_ROUTE_BIAS_SELECT ? s - a.bias[e] : s;
+    a.topk_idx[(size_t)t * k + j] = e;
+    a.topk_w[(size_t)t * k + j] = expf(av - mx) * inv;
   }
 }
 
@@ -607,7 +620,7 @@ cudaError_t launch_router(const Shape& s, const uint16_t* x, const uint16_t* W_g
   a.d = s.d;
   a.splits = splits;
   a.tau = s.tau;
-  const size_t smem = sizeof(float) * ((size_t)kBM * (EP + 1) + 2 * kBM + 8 * kBM);
+  const size_t smem = sizeof(float) * ((size_t)kBM * (EP + 4) + kBM + 8 * kBM + 2 * kList * kBM);
   err = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);
   if (err != cudaSuccess) return err;
