@@ -34,6 +34,10 @@ METRIC = "MoE-layer tokens/s (bf16, 1 GB300) and achieved fraction of roofline"
 DEFAULT_CONFIG = "fine_grained"
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# DRAM bytes (read + write) per launch from one ncu capture of the current kernel, by
+# (workload, phase): profiles/grouped_gemm_fine_grained.md. Re-capture after changing the kernel.
+NCU_TRAFFIC = {("fine_grained", "gate_up_gemm"): (878.894336e6 + 67.953920e6),
+               ("fine_grained", "down_gemm"): (473.472000e6 + 93.796352e6)}
 # router, histogram, scan, scatter, tile list, gather, gate/up, down, combine (+ router weight
 # padding when E is not a multiple of 64)
 def launches_per_step(cfg):
@@ -414,7 +418,7 @@ def main():
     fl, by = kernel_work(cfg, dom, n_touched, n_kept)
     roof = roofline_for(dom, fl, by, phase_ms[dom] / 1e3, peaks)
     roof["kernel"] = dom
-    roof["traffic"] = None
+    roof["traffic"] = NCU_TRAFFIC.get((cfg.name, dom))
     roof["peak_source"] = f"{peak_src} ({'bf16 burst' if roof['unit'] == 'TFLOP/s' else 'copy'})"
     kernels = {}
     for ph in M.PROFILE_PHASES:
