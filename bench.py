@@ -369,6 +369,7 @@ def main():
     wall = time.perf_counter() - wall0
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms = sum(step_ms) / len(step_ms)
+    ms_median = statistics.median(step_ms)
 
     # ---- phase breakdown through the profiled entry point (same kernels, events in between)
     n_prof = min(args.steps, 200)
@@ -377,7 +378,8 @@ def main():
         flush.fill_(i & 0xFF)
         M.layer_forward_profiled(mc, weights, inp["x"], u, out, ro, ws, evs[i])
     torch.cuda.synchronize()
-    phase_ms = {ph: sum(e[j].elapsed_time(e[j + 1]) for e in evs) / n_prof
+    # medians: a host stall that lets the queue drain inflates one step's phase, not the median
+    phase_ms = {ph: statistics.median(e[j].elapsed_time(e[j + 1]) for e in evs)
                 for j, ph in enumerate(M.PROFILE_PHASES)}
 
     # ---- e2e: host buffers through moe_layer_forward_host
@@ -404,11 +406,8 @@ def main():
     h2d = T * d * 2 + (T * E * 4 if u_h is not None else 0)
     d2h = T * d * 2
 
-    # ---- max over ranks
-    if dist is not None:
-        tt = torch.tensor([ms, e2e_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms, e2e_ms = tt.tolist()
+    # ---- max over ranks (replicas: no data-path collective, only this timing reduction)
+    ms, e2e_ms = max_over_ranks([ms, e2e_ms], dist, dev)
 
     counts_h = counts.cpu().tolist()
     C = M_capacity(cfg)
@@ -429,7 +428,7 @@ def main():
 
     if rank != 0:
         return
-    line = {"metric": METRIC, "value": world * T / (ms / 1e3), "unit": "tokens/s",
+    line = {"metric": METRIC, "value": replica_throughput(world, T, ms), "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded inputs, random-init weights)",
@@ -437,13 +436,14 @@ def main():
             "roofline": roof,
             "layer_roofline": lr,
             "kernels": kernels,
-            "e2e": {"value": world * T / (e2e_ms / 1e3), "unit": "tokens/s",
+            "e2e": {"value": replica_throughput(world, T, e2e_ms), "unit": "tokens/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
             "gpu_launches": launches_per_step(cfg) * args.steps,
             "clocks": clk,
             "routing": {"experts_hit": n_touched, "kept_slots": n_kept, "capacity": C,
                         "dropped_slots": T * k - n_kept,
                         "max_load": max(counts_h), "mean_load": T * k / E},
+            "ms_per_step_median": ms_median,
             "weight_pack_ms": pack_ms,
             "wall_s_timed": wall}
     if world == 1 and not args.no_cpu_baseline:
@@ -451,6 +451,21 @@ def main():
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+def max_over_ranks(values, dist=None, device="cpu"):
+    """Element-wise max of per-rank timings over the process group (identity for one process)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return list(values)
+    import torch
+    tt = torch.tensor(values, device=device, dtype=torch.float64)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return tt.tolist()
+
+
+def replica_throughput(world, tokens_per_replica, ms):
+    """Whole-job tokens/s when every rank runs one replica in `ms` milliseconds (max over ranks)."""
+    return world * tokens_per_replica / (ms / 1e3)
 
 
 def M_capacity(cfg):

@@ -227,6 +227,16 @@ moe_status moe_layer_forward_profiled(const moe_config* cfg, const moe_weights* 
                                       moe_route_out* route_out, void* ws, size_t ws_bytes,
                                       moe_stream_t stream, void* const* events, int n_events);
 
+/* Aux-loss-free expert-bias update, the step that follows a forward pass with bias-adjusted
+ * selection ("AI架构演进从稀疏MoE到条件记忆的工程实践", gating-network code, its no_grad block):
+ *   load[e] = counts[e] (selections of expert e over all top-k picks, before any capacity limit,
+ *   as written by moe_permute or moe_layer_forward's route_out), then
+ *   expert_bias[e] <- decay * expert_bias[e] - rate * load[e] / (mean(load) + 1e-8),
+ * in place on the device (mean and ratio in fp64). The page uses decay 0.99 and rate 0.01.
+ * counts [E] int32, expert_bias [E] fp32. Enqueued on stream. */
+moe_status moe_bias_update(int32_t E, const int32_t* counts, float* expert_bias, float decay,
+                           float rate, moe_stream_t stream);
+
 /* Synchronises stream, reads the device status word of ws into *fault_bits (MOE_DEVFAULT_*),
  * clears it, and returns MOE_ERR_DEVICE_FAULT if any bit was set, MOE_ERR_CUDA if the stream
  * reported an error, else MOE_OK. */

@@ -21,7 +21,8 @@ DEVFAULT_BAD_EXPERT_INDEX, DEVFAULT_PIPELINE_TIMEOUT, DEVFAULT_BAD_TILE = 0x1, 0
 EXPORTS = ("moe_workspace_size", "moe_workspace_init", "moe_route", "moe_permute",
            "moe_permute_noalloc",
            "moe_grouped_ffn", "moe_combine", "moe_layer_forward", "moe_layer_forward_profiled",
-           "moe_layer_forward_host", "moe_pack_f16", "moe_device_status", "moe_status_string")
+           "moe_layer_forward_host", "moe_pack_f16", "moe_bias_update", "moe_device_status",
+           "moe_status_string")
 
 
 class MoeError(RuntimeError):
@@ -85,6 +86,7 @@ def lib():
                                                  ctypes.POINTER(ctypes.c_void_p), I]
         L.moe_layer_forward_host.argtypes = [cfgp, ctypes.POINTER(MoeWeights), P, P, P, P, S, P]
         L.moe_pack_f16.argtypes = [P, P, S, P]
+        L.moe_bias_update.argtypes = [ctypes.c_int32, P, P, ctypes.c_float, ctypes.c_float, P]
         L.moe_device_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_int32)]
         L.moe_status_string.argtypes = [I]
         L.moe_status_string.restype = ctypes.c_char_p
@@ -235,6 +237,12 @@ def layer_forward_host(cfg, weights: MoeWeights, x_host, gumbel_u_host, out_host
     _check(lib().moe_layer_forward_host(ctypes.byref(cfg), ctypes.byref(weights), _ptr(x_host),
                                         _ptr(gumbel_u_host), _ptr(out_host), _ptr(ws),
                                         ws.numel(), _stream(stream)), "moe_layer_forward_host")
+
+
+def bias_update(counts, expert_bias, decay=0.99, rate=0.01, stream=None):
+    """In place: expert_bias <- decay*expert_bias - rate*counts/(mean(counts)+1e-8)."""
+    _check(lib().moe_bias_update(expert_bias.numel(), _ptr(counts), _ptr(expert_bias), decay, rate,
+                                 _stream(stream)), "moe_bias_update")
 
 
 def device_status(ws, stream=None) -> int:

@@ -278,13 +278,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       TileEntry te;
       int nt;
       map_unit(w, a.n_ntiles, a.tiles, te, nt);
+      const bool valid = row_in_tile < te.rows;
+      const long long p = (long long)te.row0 + row_in_tile;
+      // MODE 1: the row's slot and gate are loaded before waiting for the accumulator
+      long long orow = p;
+      float gate = 1.0f;
+      if (MODE == 1 && valid && te.expert < a.E) {
+        const int slot = a.perm_slot[p];
+        orow = slot;
+        if (a.topk_w != nullptr) gate = a.topk_w[slot];
+      }
       if (!ptx::mbar_wait_bounded(tfull_bar(acc), acc_phase, abort_flag, a.status,
                                   MOE_DEVFAULT_PIPELINE_TIMEOUT, kWaitLimitNs))
         break;
       ptx::tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN);
-      const bool valid = row_in_tile < te.rows;
-      const long long p = (long long)te.row0 + row_in_tile;
       if (MODE == 0) {
         uint16_t* dst = a.out + p * a.out_ld + (long long)nt * (BN / 2);
 #pragma unroll 1
@@ -310,13 +318,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else {
-        long long orow = p;
-        float gate = 1.0f;
-        if (valid && te.expert < a.E) {
-          const int slot = a.perm_slot[p];
-          orow = slot;
-          if (a.topk_w != nullptr) gate = a.topk_w[slot];
-        }
         uint16_t* dst = a.out + orow * a.out_ld + (long long)nt * BN;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {

@@ -113,6 +113,9 @@ cudaError_t launch_combine(const Shape& s, const uint16_t* y, const int32_t* slo
 
 cudaError_t launch_pack_f16(const uint16_t* src, uint16_t* dst, size_t n, cudaStream_t st);
 
+cudaError_t launch_bias_update(int E, const int32_t* counts, float* bias, float decay, float rate,
+                               cudaStream_t st);
+
 int num_sms();
 
 // Device side of programmatic dependent launch: wait until the preceding kernel in the stream

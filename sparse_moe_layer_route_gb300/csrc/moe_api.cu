@@ -382,6 +382,13 @@ moe_status moe_pack_f16(const uint16_t* src_bf16, uint16_t* dst_f16, size_t n,
   return cuda_status(launch_pack_f16(src_bf16, dst_f16, n, (cudaStream_t)stream));
 }
 
+moe_status moe_bias_update(int32_t E, const int32_t* counts, float* expert_bias, float decay,
+                           float rate, moe_stream_t stream) {
+  if (E < 1 || !counts || !expert_bias) return MOE_ERR_INVALID_ARG;
+  if (!std::isfinite(decay) || !std::isfinite(rate)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_bias_update(E, counts, expert_bias, decay, rate, (cudaStream_t)stream));
+}
+
 moe_status moe_device_status(void* ws, moe_stream_t stream, int32_t* fault_bits) {
   if (ws == nullptr) return MOE_ERR_WORKSPACE;
   cudaStream_t st = (cudaStream_t)stream;
