@@ -7,6 +7,7 @@
  *                                logits + expert_bias[e]    (MOE_ROUTE_BIAS_SELECT)
  *                                (logits - log(-log u)) / tau   (MOE_ROUTE_GUMBEL)
  *   3. top-k           the k largest s, ordered by s descending, ties to the lower index
+ *                      (optionally only among the experts of the best expert groups)
  *   4. gates           softmax over the k selected logits (PLAIN, BIAS_SELECT) or over the k
  *                      selected scores s (GUMBEL)
  *   5. dispatch        per-expert segments, tokens in ascending order; with a capacity C an
@@ -88,6 +89,14 @@ typedef struct {
   float tau;                 /* Gumbel temperature (> 0); ignored otherwise */
   float capacity_factor;     /* <= 0: no capacity limit; else C = ceil(cf * T * top_k / E) */
   int32_t capacity_override; /* > 0: use this capacity C instead of the factor */
+  /* Group-limited (two-level) routing, "大模型MoE稀疏激活原理与工程实践" (routing outlook: first pick
+   * one of 8 groups, then 2 experts inside it): experts form n_groups consecutive groups of
+   * E / n_groups; a group scores its largest selection score; the topk_groups best groups (ties to
+   * the lower group index) are kept and top-k picks among their experts. n_groups = 0: off.
+   * Requires E % n_groups == 0, n_groups <= 64, 1 <= topk_groups <= n_groups and
+   * top_k <= topk_groups * E / n_groups. */
+  int32_t n_groups;
+  int32_t topk_groups;
 } moe_config;
 
 typedef struct {

@@ -137,6 +137,34 @@ def tie_margin(s: np.ndarray, k: int) -> np.ndarray:
     return np.min(srt[:, : m - 1] - srt[:, 1:m], axis=1)
 
 
+def group_limit(s: np.ndarray, n_groups: int, topk_groups: int) -> np.ndarray:
+    """Two-level (group-limited) routing ("大模型MoE稀疏激活原理与工程实践", routing outlook: first
+    pick one of 8 groups, then 2 experts inside it). Reading where the page is silent: experts
+    e = 0..E-1 form n_groups consecutive groups of E / n_groups; a group's score is the largest
+    selection score of its experts; the topk_groups best groups (ties to the lower group index)
+    stay and every other expert's score becomes -inf, so top-k then picks inside them."""
+    s = np.asarray(s, np.float64)
+    T, E = s.shape
+    size = E // n_groups
+    out = np.full_like(s, -np.inf)
+    for t in range(T):
+        gs = [max(s[t, g * size:(g + 1) * size]) for g in range(n_groups)]
+        order = sorted(range(n_groups), key=lambda g: (-gs[g], g))
+        for g in order[:topk_groups]:
+            out[t, g * size:(g + 1) * size] = s[t, g * size:(g + 1) * size]
+    return out
+
+
+def group_margin(s: np.ndarray, n_groups: int, topk_groups: int) -> np.ndarray:
+    """Gap between the topk_groups-th and the next group score (inf when every group is kept)."""
+    s = np.asarray(s, np.float64)
+    T, E = s.shape
+    if topk_groups >= n_groups:
+        return np.full(T, np.inf)
+    gs = -np.sort(-s.reshape(T, n_groups, E // n_groups).max(axis=2), axis=1)
+    return gs[:, topk_groups - 1] - gs[:, topk_groups]
+
+
 def gates(logits, s, idx, mode) -> np.ndarray:
     """Softmax over the k selected values.
 
@@ -149,14 +177,24 @@ def gates(logits, s, idx, mode) -> np.ndarray:
     return ea / ea.sum(axis=1, keepdims=True)
 
 
-def route(x, W_g, k, mode=PLAIN, expert_bias=None, gumbel_u=None, tau=1.0):
-    """Full router: returns dict(logits, scores, topk_idx [T,k] int32, topk_w [T,k] f64, margin)."""
+def route(x, W_g, k, mode=PLAIN, expert_bias=None, gumbel_u=None, tau=1.0, n_groups=0,
+          topk_groups=0):
+    """Full router: returns dict(logits, scores, topk_idx [T,k] int32, topk_w [T,k] f64, margin).
+
+    With n_groups > 0 the selection is group-limited (see group_limit); `scores` are then the
+    masked scores and `margin` also covers the group decision."""
     logits = router_logits(x, W_g)
     s = selection_scores(logits, mode, expert_bias, gumbel_u, tau)
+    margin = None
+    if n_groups > 0:
+        margin = group_margin(s, n_groups, topk_groups)
+        s = group_limit(s, n_groups, topk_groups)
     idx = topk(s, k)
     w = gates(logits, s, idx, mode)
-    return {"logits": logits, "scores": s, "topk_idx": idx, "topk_w": w,
-            "margin": tie_margin(s, k)}
+    m = tie_margin(s, k)
+    if margin is not None:
+        m = np.minimum(m, margin)
+    return {"logits": logits, "scores": s, "topk_idx": idx, "topk_w": w, "margin": m}
 
 
 # ----------------------------------------------------------------------------------------
@@ -320,7 +358,8 @@ def layer_from_routing(x, topk_idx, topk_w, E, C, get_expert, n_shared=0, get_sh
 
 
 def layer(x, W_g, k, get_expert, E, mode=PLAIN, expert_bias=None, gumbel_u=None, tau=1.0,
-          capacity_factor=0.0, capacity_override=0, n_shared=0, get_shared=None, tokens=None):
+          capacity_factor=0.0, capacity_override=0, n_shared=0, get_shared=None, tokens=None,
+          n_groups=0, topk_groups=0):
     """The whole layer: route -> permute (with capacity) -> SwiGLU experts -> combine.
 
     `tokens` restricts the expert and combine work to those tokens (routing and the capacity
@@ -329,7 +368,7 @@ def layer(x, W_g, k, get_expert, E, mode=PLAIN, expert_bias=None, gumbel_u=None,
     """
     x = np.asarray(x, np.float64)
     T = x.shape[0]
-    r = route(x, W_g, k, mode, expert_bias, gumbel_u, tau)
+    r = route(x, W_g, k, mode, expert_bias, gumbel_u, tau, n_groups, topk_groups)
     C = capacity(T, k, E, capacity_factor, capacity_override)
     out, perm = layer_from_routing(x, r["topk_idx"], r["topk_w"], E, C, get_expert, n_shared,
                                    get_shared, tokens)

@@ -35,17 +35,22 @@ class MoeConfig(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int32), ("d", ctypes.c_int32), ("E", ctypes.c_int32),
                 ("top_k", ctypes.c_int32), ("d_ff", ctypes.c_int32),
                 ("n_shared", ctypes.c_int32), ("mode", ctypes.c_int32), ("tau", ctypes.c_float),
-                ("capacity_factor", ctypes.c_float), ("capacity_override", ctypes.c_int32)]
+                ("capacity_factor", ctypes.c_float), ("capacity_override", ctypes.c_int32),
+                ("n_groups", ctypes.c_int32), ("topk_groups", ctypes.c_int32)]
 
     @classmethod
     def make(cls, T, d, E, top_k, d_ff, n_shared=0, mode=ROUTE_PLAIN, tau=1.0,
-             capacity_factor=0.0, capacity_override=0):
-        return cls(T, d, E, top_k, d_ff, n_shared, mode, tau, capacity_factor, capacity_override)
+             capacity_factor=0.0, capacity_override=0, n_groups=0, topk_groups=0):
+        return cls(T, d, E, top_k, d_ff, n_shared, mode, tau, capacity_factor, capacity_override,
+                   n_groups, topk_groups)
 
     @classmethod
     def from_layer(cls, c):
-        """From any object with T, d, E, k, f, S, mode, tau, capacity_factor attributes."""
-        return cls.make(c.T, c.d, c.E, c.k, c.f, c.S, c.mode, c.tau, c.capacity_factor)
+        """From any object with T, d, E, k, f, S, mode, tau, capacity_factor (and optionally
+        n_groups, topk_groups) attributes."""
+        return cls.make(c.T, c.d, c.E, c.k, c.f, c.S, c.mode, c.tau, c.capacity_factor,
+                        n_groups=getattr(c, "n_groups", 0),
+                        topk_groups=getattr(c, "topk_groups", 0))
 
 
 class MoeWeights(ctypes.Structure):

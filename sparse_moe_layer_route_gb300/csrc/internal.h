@@ -15,6 +15,7 @@ constexpr int kPermuteBlock = 256; // slots per dispatch block
 
 struct Shape {
   int T, d, E, k, f, S, mode;
+  int G, Gk;      // group-limited routing: groups, groups kept (G = 0: off)
   float tau;
   int C;          // capacity, or INT32_MAX for no limit
   long long TK;   // T * k

@@ -45,6 +45,8 @@ Shape make_shape(const moe_config& c) {
   s.f = c.d_ff;
   s.S = c.n_shared;
   s.mode = c.mode;
+  s.G = c.n_groups;
+  s.Gk = c.topk_groups;
   s.tau = c.tau;
   s.TK = (long long)c.T * c.top_k;
   s.rows = s.TK + (long long)c.n_shared * c.T;
@@ -126,6 +128,13 @@ moe_status check_cfg(const moe_config* c) {
   if (!std::isfinite(c->capacity_factor)) return MOE_ERR_INVALID_ARG;
   if (c->E > 256 || c->top_k > 8 || c->top_k > c->E || c->n_shared > 4) return MOE_ERR_UNSUPPORTED;
   if (c->d % 64 != 0 || c->d_ff % 64 != 0) return MOE_ERR_UNSUPPORTED;
+  if (c->n_groups < 0) return MOE_ERR_INVALID_ARG;
+  if (c->n_groups > 0) {
+    if (c->n_groups > 64 || c->E % c->n_groups != 0) return MOE_ERR_UNSUPPORTED;
+    if (c->topk_groups < 1 || c->topk_groups > c->n_groups) return MOE_ERR_INVALID_ARG;
+    if ((long long)c->top_k > (long long)c->topk_groups * (c->E / c->n_groups))
+      return MOE_ERR_INVALID_ARG;
+  }
   const long long rows = (long long)c->T * (c->top_k + c->n_shared);
   if (rows >= (1ll << 31)) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;

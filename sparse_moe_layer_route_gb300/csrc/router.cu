@@ -241,6 +241,7 @@ struct SelectArgs {
   int32_t* rlist;     // near-tie tokens, appended
   int* rcount;        // their number (reset to 0 by the refine kernel when it finishes)
   int T, E, EP, k, mode, d, splits;
+  int G, Gk;          // group-limited routing (G = 0: off)
   float tau;
 };
 
@@ -256,6 +257,9 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const SelectArgs a) {
   int* sel_e = reinterpret_cast<int*>(sel_s + 4 * kBM);     // [2][2][128]
   float* pick_s = reinterpret_cast<float*>(sel_e + 4 * kBM);  // [kList][128]
   int* pick_e = reinterpret_cast<int*>(pick_s + kList * kBM);  // [kList][128]
+  float* gmax = reinterpret_cast<float*>(pick_e + kList * kBM);  // [128][G] group scores
+  unsigned long long* gsel = reinterpret_cast<unsigned long long*>(gmax + kBM * a.G);  // [128]
+  float* gmarg = reinterpret_cast<float*>(gsel + kBM);          // [128] group-decision gap
   griddep_wait();
   const bool gumbel = a.mode == MOE_ROUTE_GUMBEL;
   const int t0 = blockIdx.x * kBM;
@@ -307,9 +311,56 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const SelectArgs a) {
   const int r = threadIdx.x & (kBM - 1), h = threadIdx.x >> 7;
   const int t = t0 + r;
   const bool row_ok = t < a.T;
-  const float* srow = scores + r * LD;
+  float* srow = scores + r * LD;
   const int half = ((a.E + 1) / 2 + 3) & ~3;  // multiple of 4: float4 reads
   const int e_lo = h * half, e_hi = min(a.E, e_lo + half);
+  if (a.G > 0) {
+    // group-limited routing: group score = largest score of its experts; keep the Gk best
+    // groups (ties to the lower group), the other experts' scores become -inf
+    const int gsz = a.E / a.G;
+    if (row_ok)
+      for (int gi = h; gi < a.G; gi += 2) {
+        float m = -INFINITY;
+        for (int e = gi * gsz; e < (gi + 1) * gsz; ++e) m = fmaxf(m, srow[e]);
+        gmax[r * a.G + gi] = m;
+      }
+    __syncthreads();
+    if (row_ok && h == 0) {
+      unsigned long long sel = 0ull;
+      float ps_g = INFINITY, kth = INFINITY, next = -INFINITY;
+      int pg = -1;
+      const int passes = a.Gk < a.G ? a.Gk + 1 : a.Gk;
+      for (int j = 0; j < passes; ++j) {
+        float bs = -INFINITY;
+        int bg = INT_MAX;
+        for (int gi = 0; gi < a.G; ++gi) {
+          const float v = gmax[r * a.G + gi];
+          const bool after = v < ps_g || (v == ps_g && gi > pg);
+          if (after && beats(v, gi, bs, bg)) {
+            bs = v;
+            bg = gi;
+          }
+        }
+        if (j < a.Gk) {
+          sel |= 1ull << bg;
+          kth = bs;
+        } else {
+          next = bs;
+        }
+        ps_g = bs;
+        pg = bg;
+      }
+      gsel[r] = sel;
+      gmarg[r] = a.Gk < a.G ? kth - next : INFINITY;
+    }
+    __syncthreads();
+    if (row_ok) {
+      const unsigned long long sel = gsel[r];
+      for (int e = e_lo; e < e_hi; ++e)
+        if (!((sel >> (e / gsz)) & 1ull)) srow[e] = -INFINITY;
+    }
+    __syncthreads();
+  }
   const int k = a.k;
   const int nl = k < a.E ? k + 1 : k;  // top-(k+1), or all E when k == E
   // pass j: the best expert strictly after pick j-1 in (score desc, index asc) order
@@ -376,7 +427,10 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const SelectArgs a) {
   float band = router_band(a.d, maxl[r]);
   if (gumbel) band /= a.tau;
   int nc = 0;
-  if (min_gap < band) {
+  if (a.G > 0 && gmarg[r] < band) {
+    nc = -1;  // the group decision itself is uncertain: recompute every expert exactly
+    a.rlist[atomicAdd(a.rcount, 1)] = t;
+  } else if (min_gap < band) {
     // candidates: every expert scoring within the band of the k-th score
     for (int e = 0; e < a.E; ++e) {
       if (srow[e] >= sk - band) {
@@ -447,7 +501,7 @@ __global__ void __launch_bounds__(kThreads) refine_kernel(
     const float* __restrict__ u, const int32_t* __restrict__ ncand,
     const int32_t* __restrict__ cand, const int32_t* __restrict__ rlist, int* rcount, int* rdone,
     int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, int T, int d, int E, int k,
-    int mode, float tau) {
+    int mode, float tau, int G, int Gk) {
   __shared__ float red[kThreads / 32][kMaxCand];
   __shared__ int ce[256];
   __shared__ float cl[256], cs[256];
@@ -508,6 +562,31 @@ __global__ void __launch_bounds__(kThreads) refine_kernel(
                             mode == MOE_ROUTE_GUMBEL ? u[(size_t)t * E + e] : 0.f, tau);
       }
       __syncthreads();
+    }
+    if (threadIdx.x == 0 && n_c < 0 && G > 0) {
+      // all experts recomputed (candidates are 0..E-1 in order): redo the group decision
+      const int gsz = E / G;
+      unsigned long long sel = 0ull;
+      float ps_g = INFINITY;
+      int pg = -1;
+      for (int j = 0; j < Gk; ++j) {
+        float bs = -INFINITY;
+        int bg = INT_MAX;
+        for (int gi = 0; gi < G; ++gi) {
+          float v = -INFINITY;
+          for (int e = gi * gsz; e < (gi + 1) * gsz; ++e) v = fmaxf(v, cs[e]);
+          const bool after = v < ps_g || (v == ps_g && gi > pg);
+          if (after && beats(v, gi, bs, bg)) {
+            bs = v;
+            bg = gi;
+          }
+        }
+        sel |= 1ull << bg;
+        ps_g = bs;
+        pg = bg;
+      }
+      for (int e = 0; e < E; ++e)
+        if (!((sel >> (e / gsz)) & 1ull)) cs[e] = -INFINITY;
     }
     if (threadIdx.x == 0) {
       // selection among the candidates by (score desc, index asc)
@@ -619,8 +698,12 @@ cudaError_t launch_router(const Shape& s, const uint16_t* x, const uint16_t* W_g
   a.mode = s.mode;
   a.d = s.d;
   a.splits = splits;
+  a.G = s.G;
+  a.Gk = s.Gk;
   a.tau = s.tau;
-  const size_t smem = sizeof(float) * ((size_t)kBM * (EP + 4) + kBM + 8 * kBM + 2 * kList * kBM);
+  // group-limited routing adds the group scores, the kept-group masks and the group gaps
+  const size_t smem = sizeof(float) * ((size_t)kBM * (EP + 4) + kBM + 8 * kBM + 2 * kList * kBM +
+                                       (s.G > 0 ? (size_t)kBM * (s.G + 3) : 0));
   err = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);
   if (err != cudaSuccess) return err;
@@ -630,7 +713,7 @@ cudaError_t launch_router(const Shape& s, const uint16_t* x, const uint16_t* W_g
   return launch_k(refine_kernel, dim3(rgrid), dim3(kThreads), 0, st, x, (const uint16_t*)rs.wg_t,
                   bias, u, (const int32_t*)rs.ncand, (const int32_t*)rs.cand,
                   (const int32_t*)rs.rlist, rs.rcount, rs.rdone, topk_idx, topk_w, s.T, s.d, s.E,
-                  s.k, s.mode, s.tau);
+                  s.k, s.mode, s.tau, s.G, s.Gk);
 }
 
 }  // namespace moe

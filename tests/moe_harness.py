@@ -100,7 +100,7 @@ def oracle_route(cfg, inp):
     Wg64 = f64(inp["W_g"])
     bias = inp["bias"].double().cpu().numpy() if inp["bias"] is not None else None
     u = inp["u"].cpu().numpy() if inp.get("u") is not None else None
-    r = O.route(x64, Wg64, cfg.k, cfg.mode, bias, u, cfg.tau)
+    r = O.route(x64, Wg64, cfg.k, cfg.mode, bias, u, cfg.tau, cfg.n_groups, cfg.topk_groups)
     return x64, r
 
 

@@ -19,6 +19,8 @@ SMALL = [
     dict(T=1, d=64, E=1, k=1, f=64),
     dict(T=100, d=128, E=4, k=4, f=128, S=1, capacity_factor=0.05),
     dict(T=200, d=128, E=256, k=8, f=64),
+    dict(T=1024, d=256, E=64, k=6, f=128, S=2, mode=W.BIAS_SELECT, bias="normal", bias_var=0.1,
+         n_groups=8, topk_groups=3, capacity_factor=1.0),
 ]
 
 

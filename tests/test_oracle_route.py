@@ -142,3 +142,50 @@ def test_bf16_widening_roundtrip():
     assert O.f64_to_bf16_bits([1.0])[0] == 0x3F80
     assert O.f64_to_bf16_bits([1.0 + 2 ** -8])[0] == 0x3F80     # tie -> even
     assert O.f64_to_bf16_bits([1.0 + 3 * 2 ** -8])[0] == 0x3F82
+
+
+def brute_group_topk(s_row, k, n_groups, g):
+    """Group-limited top-k by enumeration of group subsets (definition, no sorting)."""
+    E = len(s_row)
+    size = E // n_groups
+    gs = [max(s_row[i * size:(i + 1) * size]) for i in range(n_groups)]
+    before_g = lambda a, b: gs[a] > gs[b] or (gs[a] == gs[b] and a < b)
+    chosen = None
+    for sub in itertools.combinations(range(n_groups), g):
+        rest = [x for x in range(n_groups) if x not in sub]
+        if all(before_g(a, b) for a in sub for b in rest):
+            chosen = sub
+    allowed = [e for e in range(E) if e // size in chosen]
+    masked = [s_row[e] if e in allowed else -math.inf for e in range(E)]
+    return brute_topk(masked, k)
+
+
+def test_group_limited_fixture():
+    from golden_io import read_kv
+    g = read_kv("group_limited.txt")
+    s = np.array([[0.9, 0.1, 0.8, 0.85, 0.3, 0.2, 0.95, -1.0]])
+    for gk, key in ((1, "g1"), (2, "g2"), (3, "g3")):
+        assert O.topk(O.group_limit(s, 4, gk), 2)[0].tolist() == g[key]
+    s2 = np.array([[0.5, 0.0, 0.5, 0.4, 0.1, 0.1, 0.2, 0.2]])
+    assert O.topk(O.group_limit(s2, 4, 1), 2)[0].tolist() == g["tie1"]
+
+
+def test_group_limited_bruteforce():
+    rng = np.random.default_rng(17)
+    for _ in range(60):
+        n_groups = int(rng.choice([2, 3, 4]))
+        size = int(rng.integers(1, 4))
+        E = n_groups * size
+        g = int(rng.integers(1, n_groups + 1))
+        k = int(rng.integers(1, g * size + 1))
+        s = rng.integers(-2, 3, size=(5, E)).astype(np.float64)
+        got = O.topk(O.group_limit(s, n_groups, g), k)
+        for t in range(5):
+            assert list(got[t]) == brute_group_topk(list(s[t]), k, n_groups, g)
+
+
+def test_group_limited_all_groups_is_plain_topk():
+    rng = np.random.default_rng(2)
+    s = rng.standard_normal((30, 12))
+    assert np.array_equal(O.topk(O.group_limit(s, 4, 4), 3), O.topk(s, 3))
+    np.testing.assert_array_equal(O.group_margin(s, 4, 4), np.inf)

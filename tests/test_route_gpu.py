@@ -40,7 +40,7 @@ def run_route(cfg, inp):
 def oracle_for(cfg, inp):
     u = inp["u"].numpy() if inp["u"] is not None else None
     return O.route(f64(inp["x"]), f64(inp["W_g"]), cfg.k, cfg.mode,
-                   inp["bias"].double().numpy(), u, cfg.tau)
+                   inp["bias"].double().numpy(), u, cfg.tau, cfg.n_groups, cfg.topk_groups)
 
 
 @pytest.mark.parametrize("T,d,E,k,mode,bias", CASES)
@@ -107,5 +107,54 @@ def test_route_near_ties_are_decided_exactly():
     both = np.isin(r["topk_idx"], [2, 5]).sum(1) == 2
     close = both & ~exempt
     assert close.sum() > 100             # many non-exempt near-ties were exercised
+    diff = (idx != r["topk_idx"]).any(1)
+    assert not (diff & ~exempt).any(), np.nonzero(diff & ~exempt)[0][:10]
+
+
+GROUP_CASES = [  # T, d, E, k, mode, bias, n_groups, topk_groups
+    (1000, 1024, 64, 6, W.BIAS_SELECT, "normal", 8, 3),
+    (513, 2048, 256, 8, W.BIAS_SELECT, "normal", 8, 4),
+    (300, 256, 64, 2, W.PLAIN, "zero", 8, 1),
+    (700, 512, 16, 2, W.GUMBEL, "zero", 4, 2),
+    (129, 128, 12, 3, W.PLAIN, "zero", 3, 3),       # every group kept: plain top-k
+    (64, 192, 64, 4, W.PLAIN, "zero", 64, 4),       # one expert per group: plain top-k
+]
+
+
+@pytest.mark.parametrize("T,d,E,k,mode,bias,G,Gk", GROUP_CASES)
+def test_group_limited_route_matches_oracle(T, d, E, k, mode, bias, G, Gk):
+    cfg = W.small_config(T=T, d=d, E=E, k=k, f=64, mode=mode, tau=0.5 if mode == W.GUMBEL else 1.0,
+                         seed=T + E + G, bias=bias, bias_var=0.1, n_groups=G, topk_groups=Gk)
+    inp = W.make_routing_inputs(cfg)
+    idx, w = run_route(cfg, inp)
+    r = oracle_for(cfg, inp)
+    exempt = r["margin"] < O.TIE_MARGIN
+    diff = (idx != r["topk_idx"]).any(1)
+    assert not (diff & ~exempt).any(), np.nonzero(diff & ~exempt)[0][:10]
+    # every selected expert lies in one of the token's topk_groups kept groups
+    assert (np.array([len(set(row)) for row in (idx // (E // G))]) <= Gk).all()
+    w_ref = O.gates(r["logits"], r["scores"], idx, mode)
+    assert np.abs(w - w_ref).max() <= GATE_ATOL
+
+
+def test_group_near_ties_are_decided_exactly():
+    """The best experts of groups 0 and 1 are two router columns 16 bf16 ulps apart in one
+    weight, so the group decision of many tokens hangs on a logit difference inside the tensor
+    core's error yet above the exemption margin. The full exact recompute must decide it."""
+    cfg = W.small_config(T=2048, d=2048, E=32, k=2, f=64, seed=41, n_groups=4, topk_groups=1)
+    inp = W.make_routing_inputs(cfg)
+    Wg = inp["W_g"].float()
+    Wg[:, 3] *= 3.0
+    Wg[:, 8 + 4] = Wg[:, 3]
+    Wg[100, 3] = 2.0 ** -12
+    Wg[100, 8 + 4] = 2.0 ** -12 + 16 * 2.0 ** -19
+    inp["W_g"] = Wg.to(torch.bfloat16)
+    idx, w = run_route(cfg, inp)
+    r = oracle_for(cfg, inp)
+    exempt = r["margin"] < O.TIE_MARGIN
+    s = f64(inp["x"]) @ f64(inp["W_g"])
+    gs = np.sort(s.reshape(cfg.T, 4, 8).max(2), 1)
+    top_is_pair = (np.abs(s[:, 3] - s[:, 12]) < 1e-4) & (np.maximum(s[:, 3], s[:, 12]) == gs[:, -1])
+    assert (top_is_pair & ~exempt).sum() > 100     # many non-exempt group near-ties exercised
     diff = (idx != r["topk_idx"]).any(1)
     assert not (diff & ~exempt).any(), np.nonzero(diff & ~exempt)[0][:10]

@@ -50,6 +50,8 @@ class LayerConfig:
     bias: str = "zero"         # "zero" | "normal" | "zipf"
     bias_var: float = 0.0
     zipf_s: float = 1.1
+    n_groups: int = 0          # group-limited routing (0: off)
+    topk_groups: int = 0
     description: str = ""
 
     def as_dict(self):
@@ -80,11 +82,13 @@ CONFIGS = {
 
 
 def small_config(name="small", T=64, d=128, E=8, k=2, f=128, S=0, mode=PLAIN, tau=1.0,
-                 capacity_factor=0.0, seed=0, bias="zero", bias_var=0.0, zipf_s=1.1):
+                 capacity_factor=0.0, seed=0, bias="zero", bias_var=0.0, zipf_s=1.1,
+                 n_groups=0, topk_groups=0):
     """A config for tests at sizes the oracle finishes in seconds."""
     return LayerConfig(name, T=T, d=d, E=E, k=k, f=f, S=S, mode=mode, tau=tau,
                        capacity_factor=capacity_factor, seed=seed, bias=bias,
-                       bias_var=bias_var, zipf_s=zipf_s)
+                       bias_var=bias_var, zipf_s=zipf_s, n_groups=n_groups,
+                       topk_groups=topk_groups)
 
 
 def skew_scale() -> float:
