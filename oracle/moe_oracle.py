@@ -19,6 +19,10 @@ order the pages give it:
              ("GPT-4 Has 1.8 Trillion Parameters. It Uses 2% of Them Per Token", §3.1 门控网络).
   capacity : capacity = tokens * k / E * capacity_factor, overflow slots marked and dropped
              ("参数规模与稀疏激活的真相拆解", §3.2 专家容量, Level 1 hard limit).
+  reroute  : optional Level 2 of the same section: a dropped slot moves to the best-scoring
+             expert that still has room and that its token does not already use.
+  groups   : optional group-limited selection: keep the best groups of experts, then top-k
+             inside them ("大模型MoE稀疏激活原理与工程实践", routing outlook).
   expert   : SwiGLU FFN  y = (silu(x W_gate) * (x W_up)) W_down
              ("GPT-4 ... 2% ...", §3.3 专家内部结构; "大模型MoE稀疏激活原理与工程实践", §3.2 专家).
   shared   : always-on shared experts added to the routed output
@@ -277,6 +281,94 @@ def permute_by_sort(topk_idx: np.ndarray, E: int, C=None):
 # ----------------------------------------------------------------------------------------
 # experts and combine
 # ----------------------------------------------------------------------------------------
+def overflow_reroute(topk_idx, slot_pos, scores, E: int, C: int):
+    """Level-2 capacity protection ("参数规模与稀疏激活的真相拆解", §3.2 专家容量: overflow tokens
+    are not dropped but handed to a fallback router that picks the next-best expert that is not
+    full). Reading where the page is silent: after the Level-1 walk (`permute`), the dropped
+    slots are visited in slot order (t ascending, then j); each takes the expert with the best
+    selection score (ties to the lower index) among those that still have room and that its token
+    does not already use; the slot stays dropped when there is none. Each taken expert's room
+    shrinks by one before the next dropped slot is visited.
+
+    Returns dict(topk_idx [T, k] with the re-routed experts in place, rerouted [T, k] bool,
+    margin [T]: the smallest gap, over the token's re-routed slots, between the chosen score and
+    the best other eligible score (inf when none))."""
+    idx = np.array(topk_idx, np.int64)
+    T, k = idx.shape
+    s = np.asarray(scores, np.float64)
+    sp = np.asarray(slot_pos, np.int64)
+    fill = np.zeros(E, np.int64)
+    for t in range(T):
+        for j in range(k):
+            if sp[t * k + j] >= 0:
+                fill[idx[t, j]] += 1
+    out = idx.copy()
+    rerouted = np.zeros((T, k), bool)
+    margin = np.full(T, np.inf)
+    for t in range(T):
+        used = {int(idx[t, j]) for j in range(k) if sp[t * k + j] >= 0}
+        for j in range(k):
+            if sp[t * k + j] >= 0:
+                continue
+            elig = sorted((e for e in range(E) if fill[e] < C and e not in used),
+                          key=lambda e: (-s[t, e], e))
+            if not elig:
+                continue
+            best = elig[0]
+            if len(elig) > 1:
+                a, b = s[t, best], s[t, elig[1]]
+                margin[t] = min(margin[t], a - b if a != b else 0.0)
+            out[t, j] = best
+            rerouted[t, j] = True
+            fill[best] += 1
+            used.add(best)
+    return {"topk_idx": out.astype(np.int32), "rerouted": rerouted, "margin": margin}
+
+
+def overflow_reroute_by_proposals(topk_idx, slot_pos, scores, E: int, C: int):
+    """Second, independent construction of `overflow_reroute`, used only to pin it: every token
+    with dropped slots proposes to its best untried experts (one per unmet slot); each expert
+    keeps the proposals of the lowest-numbered tokens up to its room and turns the others away;
+    turned-away tokens propose again, until no proposal is turned away. With one priority order
+    (token number) shared by all experts this ends in the same assignment as the slot-order walk.
+    Returns the final topk_idx."""
+    idx = np.array(topk_idx, np.int64)
+    T, k = idx.shape
+    s = np.asarray(scores, np.float64)
+    sp = np.asarray(slot_pos, np.int64).reshape(T, k)
+    room = np.full(E, C, np.int64)
+    for t in range(T):
+        for j in range(k):
+            if sp[t, j] >= 0:
+                room[idx[t, j]] -= 1
+    want = {t: int((sp[t] < 0).sum()) for t in range(T) if (sp[t] < 0).any()}
+    pref = {t: [e for e in sorted(range(E), key=lambda e: (-s[t, e], e))
+                if e not in {int(idx[t, j]) for j in range(k) if sp[t, j] >= 0}] for t in want}
+    nxt = {t: 0 for t in want}
+    held = {e: set() for e in range(E)}
+    while True:
+        for t in want:
+            have = sum(t in held[e] for e in range(E))
+            while have < want[t] and nxt[t] < len(pref[t]):
+                held[pref[t][nxt[t]]].add(t)
+                nxt[t] += 1
+                have += 1
+        turned = False
+        for e in range(E):
+            if len(held[e]) > room[e]:
+                keep = sorted(held[e])[:max(room[e], 0)]
+                turned = True
+                held[e] = set(keep)
+        if not turned:
+            break
+    out = idx.copy()
+    for t in want:
+        got = sorted((e for e in range(E) if t in held[e]), key=lambda e: (-s[t, e], e))
+        for j, e in zip([j for j in range(k) if sp[t, j] < 0], got):
+            out[t, j] = e
+    return out.astype(np.int32)
+
+
 def silu(z):
     z = np.asarray(z, np.float64)
     with np.errstate(over="ignore"):
@@ -359,7 +451,7 @@ def layer_from_routing(x, topk_idx, topk_w, E, C, get_expert, n_shared=0, get_sh
 
 def layer(x, W_g, k, get_expert, E, mode=PLAIN, expert_bias=None, gumbel_u=None, tau=1.0,
           capacity_factor=0.0, capacity_override=0, n_shared=0, get_shared=None, tokens=None,
-          n_groups=0, topk_groups=0):
+          n_groups=0, topk_groups=0, reroute=False):
     """The whole layer: route -> permute (with capacity) -> SwiGLU experts -> combine.
 
     `tokens` restricts the expert and combine work to those tokens (routing and the capacity
@@ -370,9 +462,15 @@ def layer(x, W_g, k, get_expert, E, mode=PLAIN, expert_bias=None, gumbel_u=None,
     T = x.shape[0]
     r = route(x, W_g, k, mode, expert_bias, gumbel_u, tau, n_groups, topk_groups)
     C = capacity(T, k, E, capacity_factor, capacity_override)
-    out, perm = layer_from_routing(x, r["topk_idx"], r["topk_w"], E, C, get_expert, n_shared,
-                                   get_shared, tokens)
-    return {"out": out, "route": r, "perm": perm, "C": C}
+    idx, w = r["topk_idx"], r["topk_w"]
+    if reroute and C is not None:
+        # Level 2: dropped slots move to the best expert with room; gates over the final experts
+        rr = overflow_reroute(idx, permute(idx, E, C)["slot_pos"], r["scores"], E, C)
+        idx = rr["topk_idx"]
+        w = gates(r["logits"], r["scores"], idx, mode)
+        r = dict(r, reroute=rr)
+    out, perm = layer_from_routing(x, idx, w, E, C, get_expert, n_shared, get_shared, tokens)
+    return {"out": out, "route": r, "perm": perm, "C": C, "topk_idx": idx, "topk_w": w}
 
 
 def layer_dense(x, W_g, k, experts, mode=PLAIN, expert_bias=None, gumbel_u=None, tau=1.0,

@@ -87,3 +87,115 @@ def test_capacity_at_least_all_slots_drops_nothing():
     b = O.permute(idx, 8, None)
     assert np.array_equal(a["slot_pos"], b["slot_pos"])
     assert a["n_kept"] == 120
+
+
+# ---------------------------------------------------------------------------- Level-2 re-route
+def _level1(s, k, E, C):
+    idx = O.topk(s, k)
+    return idx, O.permute(idx, E, C)["slot_pos"]
+
+
+def test_reroute_fixture_single_slot():
+    g = read_kv("reroute_small.txt")
+    s = np.array(g["a_scores"], float).reshape(5, 3)
+    idx, sp = _level1(s, 1, 3, 2)
+    rr = O.overflow_reroute(idx, sp, s, 3, 2)
+    assert rr["topk_idx"][:, 0].tolist() == g["a_final"]
+    p = O.permute(rr["topk_idx"], 3, 2)
+    assert p["offsets"].tolist() == g["a_offsets"]
+    assert p["perm_slot"].tolist() == g["a_perm_slot"]
+    assert (p["slot_pos"] >= 0).all()
+    assert rr["margin"].tolist() == g["a_margin"]
+
+
+def test_reroute_fixture_token_keeps_distinct_experts():
+    g = read_kv("reroute_small.txt")
+    s = np.array(g["b_scores"], float).reshape(3, 4)
+    idx, sp = _level1(s, 2, 4, 2)
+    assert sp.tolist() == [0, 2, 1, 3, -1, 4]
+    rr = O.overflow_reroute(idx, sp, s, 4, 2)
+    assert rr["topk_idx"].reshape(-1).tolist() == g["b_final"]
+    w = O.gates(s, s, rr["topk_idx"], O.PLAIN)
+    np.testing.assert_allclose(w[2], g["b_t2_gates"], rtol=0, atol=1e-15)
+
+
+def _random_case(rng, T, E, k, C, integer):
+    s = rng.integers(0, 4, (T, E)).astype(float) if integer else rng.normal(size=(T, E))
+    s += np.log(np.arange(1, E + 1))[rng.permutation(E)] * -1.5   # skewed, so slots overflow
+    return s
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_reroute_walk_equals_proposals(seed):
+    rng = np.random.default_rng(seed)
+    T, E = int(rng.integers(5, 60)), int(rng.integers(2, 12))
+    k = int(rng.integers(1, min(E, 4) + 1))
+    C = int(rng.integers(1, max(2, T * k // E) + 1))
+    s = _random_case(rng, T, E, k, C, integer=seed % 2 == 0)
+    idx, sp = _level1(s, k, E, C)
+    a = O.overflow_reroute(idx, sp, s, E, C)["topk_idx"]
+    b = O.overflow_reroute_by_proposals(idx, sp, s, E, C)
+    assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_reroute_invariants(seed):
+    """Checked on the final assignment alone: capacity, distinct experts per token, and that no
+    re-routed slot passed over an expert it prefers that still had room at its turn."""
+    rng = np.random.default_rng(100 + seed)
+    T, E, k = 80, 8, 2
+    C = int(rng.integers(4, 22))
+    s = _random_case(rng, T, E, k, C, integer=seed % 2 == 1)
+    idx, sp = _level1(s, k, E, C)
+    rr = O.overflow_reroute(idx, sp, s, E, C)
+    fin, rer = rr["topk_idx"], rr["rerouted"]
+    dropped1 = (sp < 0).reshape(T, k)
+    assert not (rer & ~dropped1).any()                       # only dropped slots move
+    assert np.array_equal(fin[~rer], idx[~rer])
+    p = O.permute(fin, E, C)
+    live = (p["slot_pos"] >= 0).reshape(T, k)
+    assert np.array_equal(live, ~dropped1 | rer)             # every re-routed slot is kept
+    for t in range(T):
+        es = fin[t][live[t]]
+        assert len(set(es.tolist())) == len(es)
+    kept1 = np.bincount(idx[~dropped1], minlength=E)
+    for t in range(T):
+        for j in np.nonzero(rer[t])[0]:
+            e = fin[t, j]
+            # load of each expert when (t, j) took its turn: Level-1 slots + earlier re-routes
+            before = kept1.copy()
+            for (tt, jj) in zip(*np.nonzero(rer)):
+                if (tt, jj) < (t, j):
+                    before[fin[tt, jj]] += 1
+            mine = set(fin[t][live[t]].tolist()) - {e}
+            for e2 in range(E):
+                better = s[t, e2] > s[t, e] or (s[t, e2] == s[t, e] and e2 < e)
+                if better and e2 not in mine:
+                    assert before[e2] >= C, (t, j, e, e2)
+
+
+def test_reroute_without_overflow_is_identity():
+    rng = np.random.default_rng(5)
+    s = rng.normal(size=(40, 6))
+    idx, sp = _level1(s, 2, 6, 40)
+    rr = O.overflow_reroute(idx, sp, s, 6, 40)
+    assert np.array_equal(rr["topk_idx"], idx) and not rr["rerouted"].any()
+
+
+def test_reroute_layer_reduces_to_level1_when_nothing_overflows():
+    rng = np.random.default_rng(9)
+    T, d, E, k, f = 24, 16, 4, 2, 8
+    x = rng.normal(size=(T, d))
+    Wg = rng.normal(size=(d, E)) / 4
+    ex = [tuple(rng.normal(size=sh) / 4 for sh in ((d, f), (d, f), (f, d))) for _ in range(E)]
+    a = O.layer(x, Wg, k, lambda e: ex[e], E, capacity_override=T * k, reroute=True)
+    b = O.layer(x, Wg, k, lambda e: ex[e], E, capacity_override=T * k)
+    np.testing.assert_array_equal(a["out"], b["out"])
+    Wg2 = Wg.copy()
+    Wg2[:, 0] += 1.0                                     # every token now prefers experts 0, 1
+    Wg2[:, 1] += 0.9
+    x2 = x + 1.0
+    c = O.layer(x2, Wg2, k, lambda e: ex[e], E, capacity_override=4, reroute=True)
+    c1 = O.layer(x2, Wg2, k, lambda e: ex[e], E, capacity_override=4)
+    assert c1["perm"]["n_kept"] < E * 4                  # Level 1 leaves room unused ...
+    assert c["perm"]["n_kept"] == E * 4                  # ... that Level 2 fills (16 < T*k = 48)
