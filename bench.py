@@ -41,7 +41,13 @@ NCU_TRAFFIC = {("fine_grained", "gate_up_gemm"): (878.894336e6 + 67.953920e6),
 # router, histogram, scan, scatter, tile list, gather, gate/up, down, combine (+ router weight
 # padding when E is not a multiple of 64)
 def launches_per_step(cfg):
-    return 9 + (1 if cfg.E % 64 else 0)
+    """Kernels of one layer call: router (weight prep, GEMM, selection, near-tie pass), dispatch
+    (histogram, scan, scatter), tile list, gather, the two grouped GEMMs and the combine; the
+    overflow re-route adds its three kernels and a second dispatch."""
+    n = 12
+    if getattr(cfg, "reroute", False) and cfg.capacity_factor > 0:
+        n += 3 + 3
+    return n
 
 
 def load_peaks():
@@ -166,7 +172,8 @@ def oracle_sample_run(cfg, x_bits, Wg_bits, bias, u, get_expert, get_shared, n_t
     uu = u[sl] if u is not None else None
     t0 = time.perf_counter()
     O.layer(x64, Wg64, cfg.k, get_expert, cfg.E, cfg.mode, bias, uu, cfg.tau,
-            cfg.capacity_factor, n_shared=cfg.S, get_shared=get_shared)
+            cfg.capacity_factor, n_shared=cfg.S, get_shared=get_shared,
+            n_groups=cfg.n_groups, topk_groups=cfg.topk_groups, reroute=cfg.reroute)
     return time.perf_counter() - t0
 
 
@@ -277,6 +284,8 @@ def config_dict(cfg):
     return {"workload": cfg.name + ": " + cfg.description, "T": cfg.T, "d": cfg.d, "E": cfg.E,
             "n_shared": cfg.S, "top_k": cfg.k, "d_ff": cfg.f, "mode": cfg.mode, "tau": cfg.tau,
             "capacity_factor": cfg.capacity_factor, "seed": cfg.seed,
+            "n_groups": cfg.n_groups, "topk_groups": cfg.topk_groups,
+            "overflow_reroute": cfg.reroute,
             "l2": "flushed between timed steps (256 MB write)", "parallelism": "replicas"}
 
 
@@ -382,6 +391,9 @@ def main():
     phase_ms = {ph: statistics.median(e[j].elapsed_time(e[j + 1]) for e in evs)
                 for j, ph in enumerate(M.PROFILE_PHASES)}
 
+    # ---- the same step replayed from a CUDA graph (launch overhead removed; L2 still flushed)
+    graph = graph_replay(step, flush, stream, min(args.steps, 200))
+
     # ---- e2e: host buffers through moe_layer_forward_host
     x_h = inp_host["x"].pin_memory()
     u_h = inp_host["u"].pin_memory() if inp_host.get("u") is not None else None
@@ -444,6 +456,7 @@ def main():
                         "dropped_slots": T * k - n_kept,
                         "max_load": max(counts_h), "mean_load": T * k / E},
             "ms_per_step_median": ms_median,
+            "graph_replay": graph,
             "weight_pack_ms": pack_ms,
             "wall_s_timed": wall}
     if world == 1 and not args.no_cpu_baseline:
@@ -451,6 +464,31 @@ def main():
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+def graph_replay(step, flush, stream, n):
+    """Median per-step time of `step` captured once in a CUDA graph and replayed n times, with the
+    L2 flushed between replays (outside the graph)."""
+    import torch
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step()
+        torch.cuda.synchronize()
+        for _ in range(3):
+            g.replay()
+        st = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        en = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        for i in range(n):
+            flush.fill_(i & 0xFF)
+            st[i].record(stream)
+            g.replay()
+            en[i].record(stream)
+        torch.cuda.synchronize()
+        ms = statistics.median(a.elapsed_time(b) for a, b in zip(st, en))
+        return {"ms_per_step_median": ms, "steps": n}
+    except RuntimeError as exc:  # a capture the driver refuses is reported, not fatal
+        return {"error": str(exc).splitlines()[0][:200]}
 
 
 def max_over_ranks(values, dist=None, device="cpu"):

@@ -97,6 +97,14 @@ typedef struct {
    * top_k <= topk_groups * E / n_groups. */
   int32_t n_groups;
   int32_t topk_groups;
+  /* Level-2 capacity protection, "参数规模与稀疏激活的真相拆解" §3.2 专家容量 (overflow tokens are
+   * not dropped; a fallback router picks the next-best expert that is not full). 1: after the
+   * Level-1 dispatch, the dropped slots, in slot order, each take the best-scoring expert that
+   * still has room and that their token does not already use (ties to the lower index); a slot
+   * with no such expert stays dropped. The re-routed experts replace the dropped ones in topk_idx
+   * and a re-routed token's gates become the softmax over its final experts. 0: Level 1 only.
+   * Needs a capacity limit to have an effect; not supported together with n_groups > 0. */
+  int32_t overflow_reroute;
 } moe_config;
 
 typedef struct {
@@ -157,6 +165,22 @@ moe_status moe_permute(const moe_config* cfg, const int32_t* topk_idx, int32_t* 
                        int32_t* offsets, int32_t* perm_slot, int32_t* slot_pos, void* ws,
                        size_t ws_bytes, moe_stream_t stream);
 
+/* Level-2 overflow re-route (cfg->overflow_reroute = 1; see moe_config). Must follow moe_route and
+ * moe_permute on the same workspace and config: it reads the selection scores that moe_route kept
+ * in the workspace, and the Level-1 counts [E] and slot_pos [T * k] that moe_permute wrote.
+ *   x [T, d] bf16 and expert_bias / gumbel_u as given to moe_route (the exact re-ordering of
+ *   experts whose tensor-core scores are too close to call recomputes their logits).
+ *   topk_idx [T, k] is updated in place (dropped slots get their new expert), topk_w [T, k] is
+ *   rewritten for the re-routed tokens. Run moe_permute again on the updated topk_idx for the
+ *   final dispatch. Returns MOE_ERR_INVALID_ARG when cfg->overflow_reroute is 0, and does nothing
+ *   when the config has no capacity limit. The proposal rounds run as one cooperative kernel whose
+ *   grid barriers wait at most 2 s each (MOE_DEVFAULT_PIPELINE_TIMEOUT on expiry). */
+moe_status moe_overflow_reroute(const moe_config* cfg, const uint16_t* x,
+                                const float* expert_bias, const float* gumbel_u,
+                                int32_t* topk_idx, float* topk_w, const int32_t* counts,
+                                const int32_t* slot_pos, void* ws, size_t ws_bytes,
+                                moe_stream_t stream);
+
 /* Largest T * top_k that moe_permute_noalloc accepts (its scratch is a fixed-size array). */
 #define MOE_NOALLOC_MAX_SLOTS 262144
 
@@ -212,7 +236,9 @@ moe_status moe_pack_f16(const uint16_t* src_bf16, uint16_t* dst_f16, size_t n,
                         moe_stream_t stream);
 
 /* Steps 1-10 on device buffers: route -> permute -> grouped FFN -> combine, all enqueued on
- * stream with no host synchronisation. gumbel_u is required for GUMBEL. route_out may be NULL. */
+ * stream with no host synchronisation. gumbel_u is required for GUMBEL. route_out may be NULL.
+ * With cfg->overflow_reroute the dispatch is Level 1, the re-route, then the final dispatch;
+ * route_out then holds the final experts, gates and dispatch. */
 moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const uint16_t* x,
                              const float* gumbel_u, uint16_t* out, moe_route_out* route_out,
                              void* ws, size_t ws_bytes, moe_stream_t stream);

@@ -19,7 +19,7 @@ ROUTE_PLAIN, ROUTE_BIAS_SELECT, ROUTE_GUMBEL = 0, 1, 2
 DEVFAULT_BAD_EXPERT_INDEX, DEVFAULT_PIPELINE_TIMEOUT, DEVFAULT_BAD_TILE = 0x1, 0x2, 0x4
 
 EXPORTS = ("moe_workspace_size", "moe_workspace_init", "moe_route", "moe_permute",
-           "moe_permute_noalloc",
+           "moe_permute_noalloc", "moe_overflow_reroute",
            "moe_grouped_ffn", "moe_combine", "moe_layer_forward", "moe_layer_forward_profiled",
            "moe_layer_forward_host", "moe_pack_f16", "moe_bias_update", "moe_device_status",
            "moe_status_string")
@@ -36,21 +36,24 @@ class MoeConfig(ctypes.Structure):
                 ("top_k", ctypes.c_int32), ("d_ff", ctypes.c_int32),
                 ("n_shared", ctypes.c_int32), ("mode", ctypes.c_int32), ("tau", ctypes.c_float),
                 ("capacity_factor", ctypes.c_float), ("capacity_override", ctypes.c_int32),
-                ("n_groups", ctypes.c_int32), ("topk_groups", ctypes.c_int32)]
+                ("n_groups", ctypes.c_int32), ("topk_groups", ctypes.c_int32),
+                ("overflow_reroute", ctypes.c_int32)]
 
     @classmethod
     def make(cls, T, d, E, top_k, d_ff, n_shared=0, mode=ROUTE_PLAIN, tau=1.0,
-             capacity_factor=0.0, capacity_override=0, n_groups=0, topk_groups=0):
+             capacity_factor=0.0, capacity_override=0, n_groups=0, topk_groups=0,
+             overflow_reroute=0):
         return cls(T, d, E, top_k, d_ff, n_shared, mode, tau, capacity_factor, capacity_override,
-                   n_groups, topk_groups)
+                   n_groups, topk_groups, int(bool(overflow_reroute)))
 
     @classmethod
     def from_layer(cls, c):
         """From any object with T, d, E, k, f, S, mode, tau, capacity_factor (and optionally
-        n_groups, topk_groups) attributes."""
+        n_groups, topk_groups, reroute) attributes."""
         return cls.make(c.T, c.d, c.E, c.k, c.f, c.S, c.mode, c.tau, c.capacity_factor,
                         n_groups=getattr(c, "n_groups", 0),
-                        topk_groups=getattr(c, "topk_groups", 0))
+                        topk_groups=getattr(c, "topk_groups", 0),
+                        overflow_reroute=getattr(c, "reroute", False))
 
 
 class MoeWeights(ctypes.Structure):
@@ -82,6 +85,7 @@ def lib():
         L.moe_route.argtypes = [cfgp, P, P, P, P, P, P, P, S, P]
         L.moe_permute.argtypes = [cfgp, P, P, P, P, P, P, S, P]
         L.moe_permute_noalloc.argtypes = [cfgp, P, P, P, P, P, P, P]
+        L.moe_overflow_reroute.argtypes = [cfgp, P, P, P, P, P, P, P, P, S, P]
         L.moe_grouped_ffn.argtypes = [cfgp, P, P, P, P, P, P, P, P, P, P, P, P, P, P, S, P]
         L.moe_combine.argtypes = [cfgp, P, P, P, P, S, P]
         L.moe_layer_forward.argtypes = [cfgp, ctypes.POINTER(MoeWeights), P, P, P,
@@ -168,6 +172,14 @@ def permute_noalloc(cfg, topk_idx, counts, offsets, perm_slot, slot_pos, fault_b
     _check(lib().moe_permute_noalloc(ctypes.byref(cfg), _ptr(topk_idx), _ptr(counts),
                                      _ptr(offsets), _ptr(perm_slot), _ptr(slot_pos),
                                      _ptr(fault_bits), _stream(stream)), "moe_permute_noalloc")
+
+
+def overflow_reroute(cfg, x, expert_bias, gumbel_u, topk_idx, topk_w, counts, slot_pos, ws,
+                     stream=None):
+    _check(lib().moe_overflow_reroute(ctypes.byref(cfg), _ptr(x), _ptr(expert_bias),
+                                      _ptr(gumbel_u), _ptr(topk_idx), _ptr(topk_w), _ptr(counts),
+                                      _ptr(slot_pos), _ptr(ws), ws.numel(), _stream(stream)),
+           "moe_overflow_reroute")
 
 
 def grouped_ffn(cfg, x, perm_slot, offsets, topk_w, W_gate, W_up, W_down, Wsh_gate, Wsh_up,

@@ -16,6 +16,7 @@ constexpr int kPermuteBlock = 256; // slots per dispatch block
 struct Shape {
   int T, d, E, k, f, S, mode;
   int G, Gk;      // group-limited routing: groups, groups kept (G = 0: off)
+  bool reroute;   // Level-2 overflow re-route (only with a capacity limit)
   float tau;
   int C;          // capacity, or INT32_MAX for no limit
   long long TK;   // T * k
@@ -43,7 +44,8 @@ struct Meta {
   int n_kept;         // N = kept routed slots
   int refine_count;   // near-tie tokens listed by the router (reset by the refine kernel)
   int refine_done;    // refine CTAs finished (reset by the last one)
-  int pad[60];
+  int reroute_rounds; // proposal rounds of the last overflow re-route (diagnostic)
+  int pad[59];
 };
 
 // Offsets of every buffer carved from the caller's workspace (bytes, 256-aligned).
@@ -51,6 +53,8 @@ struct WsLayout {
   size_t status, meta, topk_idx, topk_w, counts, offsets, perm_slot, slot_pos;
   size_t blk_hist, blk_base, tiles, wg_pad, wg_t, rpart, ncand, cand, rlist, xp, h, y, x_stage,
       u_stage, out_stage;
+  // overflow re-route (zero-sized unless enabled)
+  size_t sfull, maxl, pref, rr_tok, rr_exp, rr_bits, rr_ctl;
   size_t total;
 };
 
@@ -69,12 +73,43 @@ struct RouterScratch {
   int32_t* rlist;    // [T] near-tie tokens
   int* rcount;       // their number (zero between calls)
   int* rdone;        // refine CTAs finished (zero between calls)
+  float* sfull;      // [T, E] selection scores kept for the overflow re-route, or nullptr
+  float* maxl;       // [T] largest |logit| per token (with sfull)
 };
 // K slices of the router GEMM for T tokens and hidden size d.
 int router_splits(int T, int d);
 cudaError_t launch_router(const Shape& s, const uint16_t* x, const uint16_t* W_g,
                           const float* bias, const float* u, int32_t* topk_idx, float* topk_w,
                           const RouterScratch& rs, int* status, cudaStream_t st);
+
+// Level-2 overflow re-route (reroute.cu). Per-token and per-expert state lives in the workspace;
+// the preceding router call left the selection scores (sfull), the row scales (maxl) and the
+// transposed router weights (WgT) there, and the preceding dispatch left counts and slot_pos.
+struct RerouteArgs {
+  const uint16_t* x;       // [T, d] bf16
+  const uint16_t* WgT;     // [E, d] bf16
+  const float* bias;       // [E] (BIAS_SELECT)
+  const float* u;          // [T, E] (GUMBEL)
+  const float* sfull;      // [T, E] tensor-core selection scores
+  const float* maxl;       // [T] largest |logit| per token
+  int32_t* topk_idx;       // [T, k] in/out: dropped slots get their new expert
+  float* topk_w;           // [T, k] out for re-routed tokens: softmax over the final experts
+  const int32_t* counts;   // [E] Level-1 counts (before the capacity clamp)
+  const int32_t* slot_pos; // [T * k] Level-1 positions (-1: dropped)
+  uint8_t* pref;           // [T, PS] preference lists (expert ids < 256), PS = E rounded up to 16
+  int32_t *plen, *dem, *ptr, *held;  // [T] each: list length, dropped slots, next position, kept
+  int32_t *rlen, *ext_list;          // [T] each: exactly ordered prefix, tokens needing more
+  int32_t *room, *cut, *touched;     // [E] each
+  uint32_t* bits;          // [E, W] proposals held by each expert, bit t of word t / 32
+  int32_t* rejected;       // [1024] turn-aways per round
+  int32_t* extended;       // [1024] tokens listed for their next exact window, per round
+  int32_t* ctl;            // [2] grid barrier: arrivals, generation
+  int32_t* rounds_out;     // proposal rounds of the last call
+  int* status;
+  int T, d, E, k, mode, C, W, PS;
+  float tau;
+};
+cudaError_t launch_reroute(const RerouteArgs& a, cudaStream_t st);
 
 cudaError_t launch_permute(const Shape& s, const int32_t* topk_idx, int32_t* counts,
                            int32_t* offsets, int32_t* perm_slot, int32_t* slot_pos,

@@ -58,6 +58,7 @@ Shape make_shape(const moe_config& c) {
   if (C > INT_MAX) C = INT_MAX;
   if (C < 1) C = 1;
   s.C = (int)C;
+  s.reroute = c.overflow_reroute != 0 && s.C != INT_MAX;
   s.n_pblk = (int)((s.TK + kPermuteBlock - 1) / kPermuteBlock);
   s.max_tiles = (int)((s.TK + kTileM - 1) / kTileM + s.E +
                       (long long)s.S * ((s.T + kTileM - 1) / kTileM));
@@ -95,6 +96,15 @@ WsLayout ws_layout(const Shape& s) {
   L.x_stage = take(2ull * s.T * s.d);
   L.u_stage = take(s.mode == MOE_ROUTE_GUMBEL ? 4ull * s.T * s.E : 0);
   L.out_stage = take(2ull * s.T * s.d);
+  const bool rr = s.reroute;
+  const size_t W = ((size_t)s.T + 31) / 32;
+  L.sfull = take(rr ? 4ull * s.T * s.E : 0);
+  L.maxl = take(rr ? 4ull * s.T : 0);
+  L.pref = take(rr ? (size_t)s.T * ((s.E + 15) / 16 * 16) : 0);
+  L.rr_tok = take(rr ? 4ull * 6 * s.T : 0);     // plen, dem, ptr, held, rlen, ext_list
+  L.rr_exp = take(rr ? 4ull * 3 * s.E : 0);     // room, cut, touched
+  L.rr_bits = take(rr ? 4ull * s.E * W : 0);
+  L.rr_ctl = take(rr ? 4ull * (2 * 1024 + 2) : 0);  // per-round counters, barrier
   L.total = o;
   return L;
 }
@@ -135,6 +145,8 @@ moe_status check_cfg(const moe_config* c) {
     if ((long long)c->top_k > (long long)c->topk_groups * (c->E / c->n_groups))
       return MOE_ERR_INVALID_ARG;
   }
+  if (c->overflow_reroute != 0 && c->overflow_reroute != 1) return MOE_ERR_INVALID_ARG;
+  if (c->overflow_reroute && c->n_groups > 0) return MOE_ERR_UNSUPPORTED;
   const long long rows = (long long)c->T * (c->top_k + c->n_shared);
   if (rows >= (1ll << 31)) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
@@ -166,6 +178,8 @@ moe_status route_impl(const Shape& s, const WsLayout& L, void* ws, const uint16_
   Meta* meta = at<Meta>(ws, L.meta);
   rs.rcount = &meta->refine_count;
   rs.rdone = &meta->refine_done;
+  rs.sfull = s.reroute ? at<float>(ws, L.sfull) : nullptr;
+  rs.maxl = s.reroute ? at<float>(ws, L.maxl) : nullptr;
   return cuda_status(launch_router(s, x, W_g, bias, u, idx, w, rs, at<int>(ws, L.status), st));
 }
 
@@ -175,6 +189,50 @@ moe_status permute_impl(const Shape& s, const WsLayout& L, void* ws, const int32
   return cuda_status(launch_permute(s, idx, counts, offsets, perm_slot, slot_pos,
                                     at<int32_t>(ws, L.blk_hist), at<int32_t>(ws, L.blk_base),
                                     at<int>(ws, L.status), st));
+}
+
+moe_status reroute_impl(const Shape& s, const WsLayout& L, void* ws, const uint16_t* x,
+                        const float* bias, const float* u, int32_t* idx, float* w,
+                        const int32_t* counts, const int32_t* slot_pos, cudaStream_t st) {
+  RerouteArgs a;
+  a.x = x;
+  a.WgT = at<uint16_t>(ws, L.wg_t);
+  a.bias = bias;
+  a.u = u;
+  a.sfull = at<float>(ws, L.sfull);
+  a.maxl = at<float>(ws, L.maxl);
+  a.topk_idx = idx;
+  a.topk_w = w;
+  a.counts = counts;
+  a.slot_pos = slot_pos;
+  a.pref = at<uint8_t>(ws, L.pref);
+  int32_t* tok = at<int32_t>(ws, L.rr_tok);
+  a.plen = tok;
+  a.dem = tok + s.T;
+  a.ptr = tok + 2 * (size_t)s.T;
+  a.held = tok + 3 * (size_t)s.T;
+  a.rlen = tok + 4 * (size_t)s.T;
+  a.ext_list = tok + 5 * (size_t)s.T;
+  int32_t* ex = at<int32_t>(ws, L.rr_exp);
+  a.room = ex;
+  a.cut = ex + s.E;
+  a.touched = ex + 2 * s.E;
+  a.bits = at<uint32_t>(ws, L.rr_bits);
+  a.rejected = at<int32_t>(ws, L.rr_ctl);
+  a.extended = a.rejected + 1024;
+  a.ctl = a.rejected + 2048;
+  a.rounds_out = &at<Meta>(ws, L.meta)->reroute_rounds;
+  a.status = at<int>(ws, L.status);
+  a.T = s.T;
+  a.d = s.d;
+  a.E = s.E;
+  a.k = s.k;
+  a.mode = s.mode;
+  a.C = s.C;
+  a.W = (s.T + 31) / 32;
+  a.PS = (s.E + 15) / 16 * 16;
+  a.tau = s.tau;
+  return cuda_status(launch_reroute(a, st));
 }
 
 moe_status ffn_impl(const Shape& s, const WsLayout& L, void* ws, const uint16_t* x,
@@ -238,6 +296,14 @@ moe_status layer_impl(const moe_config* cfg, const moe_weights* w, const uint16_
   if (!mark(1)) return MOE_ERR_CUDA;
   if ((r = permute_impl(s, L, ws, idx, counts, offsets, perm_slot, slot_pos, st)) != MOE_OK)
     return r;
+  if (s.reroute) {
+    // Level 2: dropped slots move to the best expert with room, then the final dispatch
+    if ((r = reroute_impl(s, L, ws, x, w->expert_bias, gumbel_u, idx, gw, counts, slot_pos,
+                          st)) != MOE_OK)
+      return r;
+    if ((r = permute_impl(s, L, ws, idx, counts, offsets, perm_slot, slot_pos, st)) != MOE_OK)
+      return r;
+  }
   if (!mark(2)) return MOE_ERR_CUDA;
   uint16_t* y = at<uint16_t>(ws, L.y);
   if ((r = ffn_impl(s, L, ws, x, perm_slot, offsets, gw, w->W_gate, w->W_up, w->W_down,
@@ -295,6 +361,25 @@ moe_status moe_permute(const moe_config* cfg, const int32_t* topk_idx, int32_t* 
   const Shape s = make_shape(*cfg);
   const WsLayout L = ws_layout(s);
   return permute_impl(s, L, ws, topk_idx, counts, offsets, perm_slot, slot_pos,
+                      (cudaStream_t)stream);
+}
+
+moe_status moe_overflow_reroute(const moe_config* cfg, const uint16_t* x,
+                                const float* expert_bias, const float* gumbel_u,
+                                int32_t* topk_idx, float* topk_w, const int32_t* counts,
+                                const int32_t* slot_pos, void* ws, size_t ws_bytes,
+                                moe_stream_t stream) {
+  moe_status r = check_cfg(cfg);
+  if (r != MOE_OK) return r;
+  if (cfg->overflow_reroute == 0) return MOE_ERR_INVALID_ARG;
+  if (!x || !topk_idx || !topk_w || !counts || !slot_pos) return MOE_ERR_INVALID_ARG;
+  if (cfg->mode == MOE_ROUTE_BIAS_SELECT && !expert_bias) return MOE_ERR_INVALID_ARG;
+  if (cfg->mode == MOE_ROUTE_GUMBEL && !gumbel_u) return MOE_ERR_INVALID_ARG;
+  if ((r = check_ws(cfg, ws, ws_bytes)) != MOE_OK) return r;
+  const Shape s = make_shape(*cfg);
+  if (!s.reroute) return MOE_OK;  // no capacity limit: nothing can overflow
+  const WsLayout L = ws_layout(s);
+  return reroute_impl(s, L, ws, x, expert_bias, gumbel_u, topk_idx, topk_w, counts, slot_pos,
                       (cudaStream_t)stream);
 }
 

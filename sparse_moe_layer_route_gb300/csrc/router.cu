@@ -36,6 +36,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "route_common.cuh"
 
 namespace moe {
 namespace {
@@ -58,29 +59,6 @@ struct RCfg {
   static constexpr int kTmemCols = EP <= 64 ? 64 : (EP <= 128 ? 128 : 256);
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 256;
 };
-
-// Half-width of the band around a gap inside which the tensor-core logits could misorder two
-// experts (see the file comment).
-__device__ __forceinline__ float router_band(int d, float max_abs_logit) {
-  return 2.5e-4f * sqrtf((float)d * (1.0f / 7168.0f)) * fmaxf(1.0f, max_abs_logit);
-}
-
-__device__ __forceinline__ float selection_score(int mode, float l, float bias_e, float u_te,
-                                                 float tau) {
-  float s = l;
-  if (mode == MOE_ROUTE_BIAS_SELECT) {
-    s = l + bias_e;
-  } else if (mode == MOE_ROUTE_GUMBEL) {
-    const float g = -logf(-logf(u_te));
-    s = (l + g) / tau;
-  }
-  return (s != s) ? -INFINITY : s;  // NaN ranks last
-}
-
-// a beats b: higher score, or equal score and lower expert index
-__device__ __forceinline__ bool beats(float sa, int ea, float sb, int eb) {
-  return sa > sb || (sa == sb && ea < eb);
-}
 
 // Partial logits of one K slice: part[split][t][0, EP) (fp32; columns >= E are zero).
 template <int NCH>
@@ -240,6 +218,8 @@ struct SelectArgs {
   int32_t* cand;      // [T, kMaxCand]
   int32_t* rlist;     // near-tie tokens, appended
   int* rcount;        // their number (reset to 0 by the refine kernel when it finishes)
+  float* sfull;       // [T, E] selection scores for the overflow re-route, or nullptr
+  float* maxl_out;    // [T] largest |logit| of each row (with sfull)
   int T, E, EP, k, mode, d, splits;
   int G, Gk;          // group-limited routing (G = 0: off)
   float tau;
@@ -308,6 +288,15 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const SelectArgs a) {
     }
   }
   __syncthreads();
+  if (a.sfull != nullptr) {
+    // the overflow re-route ranks every expert of a token: keep the scores and the row scale
+    const int rows = min(kBM, a.T - t0);
+    for (int i = threadIdx.x; i < rows * a.E; i += kThreads) {
+      const int rr = i / a.E, e = i - rr * a.E;
+      a.sfull[(size_t)(t0 + rr) * a.E + e] = scores[rr * LD + e];
+    }
+    if (threadIdx.x < rows) a.maxl_out[t0 + threadIdx.x] = maxl[threadIdx.x];
+  }
   const int r = threadIdx.x & (kBM - 1), h = threadIdx.x >> 7;
   const int t = t0 + r;
   const bool row_ok = t < a.T;
@@ -700,6 +689,8 @@ cudaError_t launch_router(const Shape& s, const uint16_t* x, const uint16_t* W_g
   a.splits = splits;
   a.G = s.G;
   a.Gk = s.Gk;
+  a.sfull = rs.sfull;
+  a.maxl_out = rs.maxl;
   a.tau = s.tau;
   // group-limited routing adds the group scores, the kept-group masks and the group gaps
   const size_t smem = sizeof(float) * ((size_t)kBM * (EP + 4) + kBM + 8 * kBM + 2 * kList * kBM +

@@ -12,6 +12,11 @@ Contract (per token):
     GPU's indices;
   * layer output (bf16) against the oracle's float64 output conditioned on the GPU's indices:
     max-abs <= 2e-2 and relative L2 <= 1e-2.
+  * with the Level-2 overflow re-route: the router's own indices (before the re-route) follow
+    the rule above; the oracle's re-route walk, run on those indices, must give the GPU's final
+    indices, unless the first token where they differ had an oracle re-route decision gap below
+    1e-5 (a near-tie, counted; everything after it is compared conditioned on the GPU's final
+    indices, as above).
 """
 from __future__ import annotations
 
@@ -74,12 +79,19 @@ def run_layer(cfg, inp, capacity_override=0, stream=None, f16=True):
                              inp.get("W_down_f16") if f16 else None,
                              inp.get("Ws_down_f16") if f16 else None)
     ro = M.make_route_out(idx, w, counts, offsets, perm_slot, slot_pos)
+    primary = None
+    if getattr(cfg, "reroute", False):
+        # the router's own choice, before the re-route (deterministic: the layer computes the same)
+        p_idx = torch.empty((T, k), **i32)
+        p_w = torch.empty((T, k), dtype=torch.float32, device=dev)
+        M.route(mc, inp["x"], inp["W_g"], inp["bias"], inp.get("u"), p_idx, p_w, ws, stream)
+        primary = p_idx.cpu().numpy()
     M.layer_forward(mc, weights, inp["x"], inp.get("u"), out, ro, ws, stream)
     status = M.device_status(ws, stream)
     res = {"topk_idx": idx.cpu().numpy(), "topk_w": w.cpu().numpy(),
            "counts": counts.cpu().numpy(), "offsets": offsets.cpu().numpy(),
            "perm_slot": perm_slot.cpu().numpy(), "slot_pos": slot_pos.cpu().numpy(),
-           "out_t": out, "status": status, "ws": ws}
+           "out_t": out, "status": status, "ws": ws, "primary_idx": primary}
     return res
 
 
@@ -113,13 +125,23 @@ def check_layer(cfg, inp, gpu, tokens=None, capacity_override=0, x64=None, r=Non
     exempt = r["margin"] < O.TIE_MARGIN
     idx_g = gpu["topk_idx"]
     assert idx_g.min() >= 0 and idx_g.max() < E
-    flipped = (idx_g != r["topk_idx"]).any(axis=1)
+    C = O.capacity(T, k, E, cfg.capacity_factor, capacity_override)
+    idx_p = gpu["primary_idx"] if gpu.get("primary_idx") is not None else idx_g
+    flipped = (idx_p != r["topk_idx"]).any(axis=1)
     bad = np.nonzero(flipped & ~exempt)[0]
     assert bad.size == 0, f"{bad.size} non-exempt tokens routed differently, e.g. {bad[:5]}"
+    rr_report = {}
+    if gpu.get("primary_idx") is not None and C is not None:
+        rr = O.overflow_reroute(idx_p, O.permute(idx_p, E, C)["slot_pos"], r["scores"], E, C)
+        diff = (idx_g != rr["topk_idx"]).any(axis=1)
+        first = int(np.argmax(diff)) if diff.any() else -1
+        if first >= 0:
+            assert rr["margin"][first] < O.TIE_MARGIN, \
+                f"re-route differs first at token {first} (decision gap {rr['margin'][first]})"
+        rr_report = {"rerouted_slots": int(rr["rerouted"].sum()), "reroute_first_diff": first}
     w_cond = O.gates(r["logits"], r["scores"], idx_g, cfg.mode)
     gerr = np.abs(gpu["topk_w"] - w_cond).max()
     assert gerr <= GATE_ATOL, f"gate error {gerr}"
-    C = O.capacity(T, k, E, cfg.capacity_factor, capacity_override)
     p = O.permute(idx_g, E, C)
     for key in ("counts", "offsets", "perm_slot", "slot_pos"):
         assert np.array_equal(gpu[key], p[key]), f"{key} differs from the oracle dispatch"
@@ -133,4 +155,4 @@ def check_layer(cfg, inp, gpu, tokens=None, capacity_override=0, x64=None, r=Non
     assert np.isfinite(out_g).all()
     assert maxabs <= OUT_MAXABS and rel_l2 <= OUT_RELL2, (maxabs, rel_l2)
     return {"exempt": int(exempt.sum()), "flipped": int(flipped.sum()), "gate_err": float(gerr),
-            "maxabs": maxabs, "rel_l2": rel_l2, "n_kept": int(p["n_kept"]), "C": C}
+            "maxabs": maxabs, "rel_l2": rel_l2, "n_kept": int(p["n_kept"]), "C": C, **rr_report}

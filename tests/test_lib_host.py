@@ -48,6 +48,9 @@ def test_workspace_size_and_layout(lib):
     (dict(T=0), 1), (dict(E=0), 1), (dict(top_k=0), 1), (dict(mode=3), 1),
     (dict(mode=2, tau=0.0), 1), (dict(E=300), 2), (dict(top_k=9, E=16), 2),
     (dict(top_k=5, E=4), 2), (dict(d=100), 2), (dict(d_ff=96), 2), (dict(n_shared=5), 2),
+    (dict(overflow_reroute=2), 1), (dict(overflow_reroute=1, n_groups=4, topk_groups=2), 2),
+    (dict(n_groups=3), 2), (dict(n_groups=4, topk_groups=0), 1),
+    (dict(n_groups=4, topk_groups=1, top_k=3), 1),
 ])
 def test_bad_configs_rejected(lib, kw, status):
     base = dict(T=64, d=128, E=8, top_k=2, d_ff=128, n_shared=0, mode=0, tau=1.0,
@@ -99,3 +102,25 @@ def test_status_strings(lib):
         assert M.status_string(s)
     assert M.status_string(0) == "ok"
     assert M.status_string(99) == "unknown status"
+
+
+def test_reroute_workspace_and_validation(lib):
+    kw = dict(mode=M.ROUTE_BIAS_SELECT, capacity_factor=1.25)
+    base = M.workspace_size(M.MoeConfig.make(4096, 1024, 64, 2, 512, **kw))
+    rr = M.workspace_size(M.MoeConfig.make(4096, 1024, 64, 2, 512, overflow_reroute=1, **kw))
+    # scores [T, E] fp32 + preference lists [T, E] bytes + per-token and per-expert state
+    assert rr - base >= 4096 * 64 * 5
+    # without a capacity limit there is nothing to re-route and no extra workspace
+    nocap = dict(mode=M.ROUTE_BIAS_SELECT)
+    assert M.workspace_size(M.MoeConfig.make(4096, 1024, 64, 2, 512, overflow_reroute=1,
+                                             **nocap)) == \
+        M.workspace_size(M.MoeConfig.make(4096, 1024, 64, 2, 512, **nocap))
+    off = M.MoeConfig.make(64, 128, 8, 2, 128, capacity_factor=1.0)
+    P = ctypes.c_void_p(0x1000)
+    assert lib.moe_overflow_reroute(ctypes.byref(off), P, None, None, P, P, P, P, P, 1 << 30,
+                                    None) == 1     # re-route not enabled in the config
+    on = M.MoeConfig.make(64, 128, 8, 2, 128, capacity_factor=1.0, overflow_reroute=1)
+    assert lib.moe_overflow_reroute(ctypes.byref(on), None, None, None, P, P, P, P, P, 1 << 30,
+                                    None) == 1     # x missing
+    assert lib.moe_overflow_reroute(ctypes.byref(on), P, None, None, P, P, P, P, None, 1 << 30,
+                                    None) == 3     # no workspace
