@@ -113,13 +113,20 @@ def touched_experts(counts, C):
     return sum(1 for c in kept if c > 0), sum(kept)
 
 
+def weight_bytes_per_element(cfg):
+    """HBM bytes per expert weight: 2 for bf16; bits/8 plus the fp16 scale and uint8 zero-point
+    of each 128-weight group for quantized experts."""
+    bits = getattr(cfg, "weight_bits", 0)
+    return 2.0 if not bits else bits / 8.0 + 3.0 / 128.0
+
+
 def layer_roofline(cfg, n_touched, n_kept, t_layer_s, peaks):
     P_tc = peaks["bf16_tflops"] * 1e12
     P_hbm = peaks["hbm_gbs"] * 1e9
     d, f, E, T, k, S = cfg.d, cfg.f, cfg.E, cfg.T, cfg.k, cfg.S
     F = 6.0 * T * k * d * f
     F_alg = 6.0 * n_kept * d * f + 6.0 * T * S * d * f + 2.0 * T * d * E
-    B = (n_touched + S) * 3.0 * d * f * 2 + d * E * 2 + 2.0 * T * d * 2
+    B = (n_touched + S) * 3.0 * d * f * weight_bytes_per_element(cfg) + d * E * 2 + 2.0 * T * d * 2
     t_roof = max(F / P_tc, B / P_hbm)
     t_alg = max(F_alg / P_tc, B / P_hbm)
     return {"bound": "tensor" if F / P_tc >= B / P_hbm else "hbm",
@@ -133,10 +140,11 @@ def kernel_work(cfg, phase, n_touched, n_kept):
     d, f, E, T, k, S = cfg.d, cfg.f, cfg.E, cfg.T, cfg.k, cfg.S
     rows = n_kept + S * T
     ne = n_touched + S
+    wb = weight_bytes_per_element(cfg)
     if phase == "gate_up_gemm":
-        return 4.0 * rows * d * f, ne * 2.0 * d * f * 2 + rows * d * 2.0 + rows * f * 2.0
+        return 4.0 * rows * d * f, ne * 2.0 * d * f * wb + rows * d * 2.0 + rows * f * 2.0
     if phase == "down_gemm":
-        return 2.0 * rows * f * d, ne * 1.0 * f * d * 2 + rows * f * 2.0 + rows * d * 2.0
+        return 2.0 * rows * f * d, ne * 1.0 * f * d * wb + rows * f * 2.0 + rows * d * 2.0
     if phase == "router":
         return 2.0 * T * d * E, T * d * 2.0 + d * E * 2.0 + T * k * 8.0
     if phase == "combine":
@@ -178,16 +186,22 @@ def oracle_sample_run(cfg, x_bits, Wg_bits, bias, u, get_expert, get_shared, n_t
 
 
 class WidenedExperts:
-    """bf16 expert weights (host numpy) widened to float64 on first use and kept."""
+    """bf16 expert weights (host numpy) widened to float64 on first use and kept; with bits > 0
+    the oracle's own quantize-dequantize of them (model load, outside any timing)."""
 
-    def __init__(self, Wg, Wu, Wd):
+    def __init__(self, Wg, Wu, Wd, bits=0):
         self.src = (Wg, Wu, Wd)
+        self.bits = bits
         self.cache = {}
 
     def __call__(self, e):
         import oracle as O
         if e not in self.cache:
-            self.cache[e] = tuple(O.bf16_bits_to_f64(w[e]) for w in self.src)
+            ws = tuple(O.bf16_bits_to_f64(w[e]) for w in self.src)
+            if self.bits:
+                ws = tuple(O.dequantize_groupwise(*O.quantize_groupwise(w, self.bits))
+                           for w in ws)
+            self.cache[e] = ws
         return self.cache[e]
 
 
@@ -207,14 +221,14 @@ def routing_inputs_np(inp):
     return x_bits, Wg_bits, bias, u
 
 
-def host_weights_np(inp):
+def host_weights_np(inp, bits=0):
     import workloads as W
     ex = WidenedExperts(W.bf16_bits(inp["W_gate"]), W.bf16_bits(inp["W_up"]),
-                        W.bf16_bits(inp["W_down"]))
+                        W.bf16_bits(inp["W_down"]), bits)
     sh = None
     if inp.get("Ws_gate") is not None:
         sh = WidenedExperts(W.bf16_bits(inp["Ws_gate"]), W.bf16_bits(inp["Ws_up"]),
-                            W.bf16_bits(inp["Ws_down"]))
+                            W.bf16_bits(inp["Ws_down"]), bits)
     return ex, sh
 
 
@@ -222,7 +236,7 @@ def cpu_baseline(cfg, inp, target_s=12.0):
     """The oracle as it stands, timed on a bounded sample: the first n tokens taken as one
     batch (n = T when a whole batch fits the time budget, then repeated while under it)."""
     x_bits, Wg_bits, bias, u = routing_inputs_np(inp)
-    ex, sh = host_weights_np(inp)
+    ex, sh = host_weights_np(inp, cfg.weight_bits)
     n0 = min(32, cfg.T)
     oracle_sample_run(cfg, x_bits, Wg_bits, bias, u, ex, sh, n0)       # widen + warm
     t0 = oracle_sample_run(cfg, x_bits, Wg_bits, bias, u, ex, sh, n0)
@@ -249,7 +263,7 @@ def run_reference(args, cfg):
     import workloads as W
     inp = W.make_inputs(cfg, weights_device="cpu")
     x_bits, Wg_bits, bias, u = routing_inputs_np(inp)
-    ex, sh = host_weights_np(inp)
+    ex, sh = host_weights_np(inp, cfg.weight_bits)
     budget = 150.0
     n0 = min(8, cfg.T)
     oracle_sample_run(cfg, x_bits, Wg_bits, bias, u, ex, sh, n0)          # widen + warm
@@ -285,7 +299,7 @@ def config_dict(cfg):
             "n_shared": cfg.S, "top_k": cfg.k, "d_ff": cfg.f, "mode": cfg.mode, "tau": cfg.tau,
             "capacity_factor": cfg.capacity_factor, "seed": cfg.seed,
             "n_groups": cfg.n_groups, "topk_groups": cfg.topk_groups,
-            "overflow_reroute": cfg.reroute,
+            "overflow_reroute": cfg.reroute, "weight_bits": cfg.weight_bits,
             "l2": "flushed between timed steps (256 MB write)", "parallelism": "replicas"}
 
 
@@ -326,17 +340,27 @@ def main():
     inp = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp_host.items()}
     mc = M.MoeConfig.from_layer(cfg)
     ws = M.alloc_workspace(mc, dev)
-    # one-time weight preparation (outside the timed layer): fp16 re-encoding of W_down
+    # one-time weight preparation (outside the timed layer): the fp16 re-encoding of W_down, or
+    # the group-wise quantization of every expert matrix
     pk0, pk1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     pk0.record()
-    Wd16 = M.packed_f16(inp["W_down"])
-    Wsd16 = M.packed_f16(inp["Ws_down"]) if inp.get("Ws_down") is not None else None
+    if cfg.weight_bits:
+        names = ("W_gate", "W_up", "W_down", "Ws_gate", "Ws_up", "Ws_down")
+        qmats = {n: (M.quantize_weights(inp[n], cfg.weight_bits) if inp.get(n) is not None
+                     else None) for n in names}
+        qstruct = M.make_qweights(*[qmats[n] for n in names])
+    else:
+        Wd16 = M.packed_f16(inp["W_down"])
+        Wsd16 = M.packed_f16(inp["Ws_down"]) if inp.get("Ws_down") is not None else None
     pk1.record()
     torch.cuda.synchronize()
     pack_ms = pk0.elapsed_time(pk1)
-    weights = M.make_weights(inp["W_g"], inp["bias"], inp["W_gate"], inp["W_up"], inp["W_down"],
-                             inp.get("Ws_gate"), inp.get("Ws_up"), inp.get("Ws_down"), Wd16,
-                             Wsd16)
+    if cfg.weight_bits:
+        weights = M.make_weights(inp["W_g"], inp["bias"], None, None, None, quant=qstruct)
+    else:
+        weights = M.make_weights(inp["W_g"], inp["bias"], inp["W_gate"], inp["W_up"],
+                                 inp["W_down"], inp.get("Ws_gate"), inp.get("Ws_up"),
+                                 inp.get("Ws_down"), Wd16, Wsd16)
     T, k, E, d = cfg.T, cfg.k, cfg.E, cfg.d
     out = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
     counts = torch.empty(E, dtype=torch.int32, device=dev)
@@ -442,7 +466,9 @@ def main():
         return
     line = {"metric": METRIC, "value": replica_throughput(world, T, ms), "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": (f"int{cfg.weight_bits} weights x fp16 activations, fp32 accumulate"
+                      if cfg.weight_bits else "bf16"),
             "data": "synthetic (seeded inputs, random-init weights)",
             "config": config_dict(cfg),
             "roofline": roof,

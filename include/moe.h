@@ -105,7 +105,39 @@ typedef struct {
    * and a re-routed token's gates become the softmax over its final experts. 0: Level 1 only.
    * Needs a capacity limit to have an effect; not supported together with n_groups > 0. */
   int32_t overflow_reroute;
+  /* Expert weight format: 0 = bf16 (moe_weights.W_gate/W_up/W_down and the shared ones); 4 or
+   * 8 = weight-only group-wise quantized experts (moe_weights.quant, written by
+   * moe_quantize_weights), "大模型MoE稀疏激活原理与工程实践" §4.2 量化与混合精度 (expert weights to
+   * INT4, one scale and zero-point per 128 weights; the router stays in higher precision).
+   * Quantized experts need d and d_ff multiples of 128. Activations stay bf16/fp16 and every
+   * product accumulates in fp32; the path streams each touched expert's codes once and is
+   * built for decode-sized batches (a few rows per expert), where the layer is bound by weight
+   * bytes. */
+  int32_t weight_bits;
 } moe_config;
+
+/* One group-wise quantized weight matrix set: n_mat matrices of K x N (K = input dimension).
+ * For every matrix m, group g (input rows [128 g, 128 g + 128)) and output column n:
+ *   scale[(m * K/128 + g) * N + n]  fp16, zero[(m * K/128 + g) * N + n]  uint8,
+ *   code q in [0, 2^bits - 1], weight = (q - zero) * scale.
+ * Codes are stored in the order the tensor-core fragments consume them: 16-column tiles
+ * nt = n / 16, and inside a tile 16-row steps st = k / 16 for 32 lanes. With r = n % 16,
+ * kk = k % 16: lane = (r % 8) * 4 + (kk % 8) / 2 and the element's slot in the lane's step is
+ *   j = (kk % 2) + 2 * (r / 8) + 4 * (kk / 8)           (j = 0..7).
+ *   8-bit: byte ((m * N/16 + nt) * K/32 + st / 2) * 512 + lane * 16 + (st % 2) * 8 + j;
+ *   4-bit: 32-bit word at byte ((m * N/16 + nt) * K/64 + st / 4) * 512 + lane * 16 + (st % 4) * 4,
+ *          nibble at bit 16 * (j % 2) + 4 * (j / 2).
+ * Total code bytes: n_mat * K * N * bits / 8. */
+typedef struct {
+  const uint8_t* q;
+  const uint16_t* scale;
+  const uint8_t* zero;
+} moe_qmatrix;
+
+typedef struct {
+  moe_qmatrix gate, up, down;          /* routed experts: [E, d, d_ff], [E, d, d_ff], [E, d_ff, d] */
+  moe_qmatrix sh_gate, sh_up, sh_down; /* shared experts (n_shared > 0): [S, ...] likewise */
+} moe_qweights;
 
 typedef struct {
   const uint16_t* W_g;        /* [d, E] bf16 */
@@ -123,6 +155,9 @@ typedef struct {
   const uint16_t* W_down_f16;   /* [E, d_ff, d] fp16 or NULL */
   const uint16_t* Wsh_down_f16; /* [S, d_ff, d] fp16 or NULL (required when W_down_f16 is set
                                  * and n_shared > 0) */
+  /* Quantized experts, used instead of the bf16 ones when moe_config.weight_bits is 4 or 8
+   * (the bf16 expert pointers may then be NULL). */
+  const moe_qweights* quant;
 } moe_weights;
 
 /* Optional copies of the routing results written by moe_layer_forward (any member may be
@@ -234,6 +269,26 @@ moe_status moe_combine(const moe_config* cfg, const uint16_t* y_slot, const int3
  * (absolute error <= 2^-25). n elements; src and dst device pointers, 16-byte aligned. */
 moe_status moe_pack_f16(const uint16_t* src_bf16, uint16_t* dst_f16, size_t n,
                         moe_stream_t stream);
+
+/* One-time weight preparation: group-wise quantization of n_mat bf16 matrices W [n_mat, K, N]
+ * (row-major, K = input dimension, K % 128 == 0, N % 32 == 0) to bits = 4 or 8, in the layout
+ * of moe_qmatrix. For each group of 128 weights w along K of one column: s = fp16((max - min) /
+ * (2^bits - 1)) (a zero or non-finite s becomes fp16(max |w|), or 1 for an all-zero group),
+ * z = clamp(rint(-min / s), 0, 2^bits - 1), q = clamp(rint(w / s) + z, 0, 2^bits - 1); every
+ * division in float64, rint to nearest even. q_out needs n_mat*K*N*bits/8 bytes, scale_out and
+ * zero_out n_mat*K/128*N entries each. Asynchronous on stream. */
+moe_status moe_quantize_weights(int32_t bits, int32_t n_mat, int32_t K, int32_t N,
+                                const uint16_t* W, uint8_t* q_out, uint16_t* scale_out,
+                                uint8_t* zero_out, moe_stream_t stream);
+
+/* Steps 7-9 with quantized experts (cfg->weight_bits = 4 or 8): the same contract as
+ * moe_grouped_ffn (x, perm_slot, offsets, topk_w, fp16 y_slot rows [T*k + S*T, d]) with the
+ * expert weights taken from qw. */
+moe_status moe_grouped_ffn_quantized(const moe_config* cfg, const uint16_t* x,
+                                     const int32_t* perm_slot, const int32_t* offsets,
+                                     const float* topk_w, const moe_qweights* qw,
+                                     uint16_t* y_slot, void* ws, size_t ws_bytes,
+                                     moe_stream_t stream);
 
 /* Steps 1-10 on device buffers: route -> permute -> grouped FFN -> combine, all enqueued on
  * stream with no host synchronisation. gumbel_u is required for GUMBEL. route_out may be NULL.

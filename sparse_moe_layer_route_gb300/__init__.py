@@ -20,7 +20,7 @@ DEVFAULT_BAD_EXPERT_INDEX, DEVFAULT_PIPELINE_TIMEOUT, DEVFAULT_BAD_TILE = 0x1, 0
 
 EXPORTS = ("moe_workspace_size", "moe_workspace_init", "moe_route", "moe_permute",
            "moe_permute_noalloc", "moe_overflow_reroute",
-           "moe_grouped_ffn", "moe_combine", "moe_layer_forward", "moe_layer_forward_profiled",
+           "moe_grouped_ffn", "moe_grouped_ffn_quantized", "moe_quantize_weights", "moe_combine", "moe_layer_forward", "moe_layer_forward_profiled",
            "moe_layer_forward_host", "moe_pack_f16", "moe_bias_update", "moe_device_status",
            "moe_status_string")
 
@@ -37,29 +37,39 @@ class MoeConfig(ctypes.Structure):
                 ("n_shared", ctypes.c_int32), ("mode", ctypes.c_int32), ("tau", ctypes.c_float),
                 ("capacity_factor", ctypes.c_float), ("capacity_override", ctypes.c_int32),
                 ("n_groups", ctypes.c_int32), ("topk_groups", ctypes.c_int32),
-                ("overflow_reroute", ctypes.c_int32)]
+                ("overflow_reroute", ctypes.c_int32), ("weight_bits", ctypes.c_int32)]
 
     @classmethod
     def make(cls, T, d, E, top_k, d_ff, n_shared=0, mode=ROUTE_PLAIN, tau=1.0,
              capacity_factor=0.0, capacity_override=0, n_groups=0, topk_groups=0,
-             overflow_reroute=0):
+             overflow_reroute=0, weight_bits=0):
         return cls(T, d, E, top_k, d_ff, n_shared, mode, tau, capacity_factor, capacity_override,
-                   n_groups, topk_groups, int(bool(overflow_reroute)))
+                   n_groups, topk_groups, int(bool(overflow_reroute)), weight_bits)
 
     @classmethod
     def from_layer(cls, c):
         """From any object with T, d, E, k, f, S, mode, tau, capacity_factor (and optionally
-        n_groups, topk_groups, reroute) attributes."""
+        n_groups, topk_groups, reroute, weight_bits) attributes."""
         return cls.make(c.T, c.d, c.E, c.k, c.f, c.S, c.mode, c.tau, c.capacity_factor,
                         n_groups=getattr(c, "n_groups", 0),
                         topk_groups=getattr(c, "topk_groups", 0),
-                        overflow_reroute=getattr(c, "reroute", False))
+                        overflow_reroute=getattr(c, "reroute", False),
+                        weight_bits=getattr(c, "weight_bits", 0))
+
+
+class MoeQMatrix(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("scale", ctypes.c_void_p), ("zero", ctypes.c_void_p)]
+
+
+class MoeQWeights(ctypes.Structure):
+    _fields_ = [(n, MoeQMatrix) for n in ("gate", "up", "down", "sh_gate", "sh_up", "sh_down")]
 
 
 class MoeWeights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("W_g", "expert_bias", "W_gate", "W_up", "W_down", "Wsh_gate", "Wsh_up",
-                 "Wsh_down", "W_down_f16", "Wsh_down_f16")]
+                 "Wsh_down", "W_down_f16", "Wsh_down_f16")] + \
+        [("quant", ctypes.POINTER(MoeQWeights))]
 
 
 class MoeRouteOut(ctypes.Structure):
@@ -86,6 +96,10 @@ def lib():
         L.moe_permute.argtypes = [cfgp, P, P, P, P, P, P, S, P]
         L.moe_permute_noalloc.argtypes = [cfgp, P, P, P, P, P, P, P]
         L.moe_overflow_reroute.argtypes = [cfgp, P, P, P, P, P, P, P, P, S, P]
+        i32 = ctypes.c_int32
+        L.moe_quantize_weights.argtypes = [i32, i32, i32, i32, P, P, P, P, P]
+        L.moe_grouped_ffn_quantized.argtypes = [cfgp, P, P, P, P, ctypes.POINTER(MoeQWeights),
+                                                P, P, S, P]
         L.moe_grouped_ffn.argtypes = [cfgp, P, P, P, P, P, P, P, P, P, P, P, P, P, P, S, P]
         L.moe_combine.argtypes = [cfgp, P, P, P, P, S, P]
         L.moe_layer_forward.argtypes = [cfgp, ctypes.POINTER(MoeWeights), P, P, P,
@@ -192,6 +206,41 @@ def grouped_ffn(cfg, x, perm_slot, offsets, topk_w, W_gate, W_up, W_down, Wsh_ga
                                  _ptr(ws), ws.numel(), _stream(stream)), "moe_grouped_ffn")
 
 
+QUANT_GROUP = 128
+
+
+def quantize_weights(W, bits, stream=None):
+    """Group-wise quantization of bf16 weights W [n, K, N] (or [K, N]) on W's device; returns
+    a dict with q (uint8, fragment order), scale (fp16 [n, K/128, N]) and zero (uint8, same)."""
+    import torch
+    shp = tuple(W.shape)
+    n_mat = 1 if len(shp) == 2 else shp[0]
+    K, N = shp[-2], shp[-1]
+    dev = W.device
+    q = torch.empty(n_mat * K * N * bits // 8, dtype=torch.uint8, device=dev)
+    sc = torch.empty((n_mat, K // QUANT_GROUP, N), dtype=torch.float16, device=dev)
+    z = torch.empty((n_mat, K // QUANT_GROUP, N), dtype=torch.uint8, device=dev)
+    _check(lib().moe_quantize_weights(bits, n_mat, K, N, _ptr(W), _ptr(q), _ptr(sc), _ptr(z),
+                                      _stream(stream)), "moe_quantize_weights")
+    return {"q": q, "scale": sc, "zero": z, "bits": bits, "shape": (n_mat, K, N)}
+
+
+def make_qweights(gate, up, down, sh_gate=None, sh_up=None, sh_down=None) -> MoeQWeights:
+    """From quantize_weights() results (keep those tensors alive while the struct is used)."""
+    def m(d):
+        return MoeQMatrix(None, None, None) if d is None else \
+            MoeQMatrix(_ptr(d["q"]), _ptr(d["scale"]), _ptr(d["zero"]))
+    return MoeQWeights(m(gate), m(up), m(down), m(sh_gate), m(sh_up), m(sh_down))
+
+
+def grouped_ffn_quantized(cfg, x, perm_slot, offsets, topk_w, qweights: MoeQWeights, y_slot,
+                          ws, stream=None):
+    _check(lib().moe_grouped_ffn_quantized(ctypes.byref(cfg), _ptr(x), _ptr(perm_slot),
+                                           _ptr(offsets), _ptr(topk_w), ctypes.byref(qweights),
+                                           _ptr(y_slot), _ptr(ws), ws.numel(), _stream(stream)),
+           "moe_grouped_ffn_quantized")
+
+
 def pack_f16(src_bf16, dst_f16, stream=None):
     """dst (int16/float16 tensor) = fp16 re-encoding of the bf16 tensor src (same shape)."""
     assert src_bf16.numel() == dst_f16.numel()
@@ -213,9 +262,14 @@ def combine(cfg, y_slot, slot_pos, out, ws, stream=None):
 
 
 def make_weights(W_g, expert_bias, W_gate, W_up, W_down, Wsh_gate=None, Wsh_up=None,
-                 Wsh_down=None, W_down_f16=None, Wsh_down_f16=None) -> MoeWeights:
-    return MoeWeights(*[_ptr(t) for t in (W_g, expert_bias, W_gate, W_up, W_down, Wsh_gate,
-                                           Wsh_up, Wsh_down, W_down_f16, Wsh_down_f16)])
+                 Wsh_down=None, W_down_f16=None, Wsh_down_f16=None,
+                 quant: MoeQWeights | None = None) -> MoeWeights:
+    w = MoeWeights(*[_ptr(t) for t in (W_g, expert_bias, W_gate, W_up, W_down, Wsh_gate,
+                                        Wsh_up, Wsh_down, W_down_f16, Wsh_down_f16)])
+    if quant is not None:
+        w.quant = ctypes.pointer(quant)
+        w._quant_ref = quant          # keep the struct alive with the weights
+    return w
 
 
 def make_route_out(topk_idx=None, topk_w=None, counts=None, offsets=None, perm_slot=None,

@@ -11,6 +11,7 @@
 namespace moe {
 
 constexpr int kTileM = 128;        // rows per grouped-GEMM tile (one UMMA M=128 accumulator)
+constexpr int kQTileM = 8;         // rows per tile of the quantized expert path (MMA N = 8)
 constexpr int kPermuteBlock = 256; // slots per dispatch block
 
 struct Shape {
@@ -22,7 +23,8 @@ struct Shape {
   long long TK;   // T * k
   long long rows; // rows of the expert-ordered buffers: T * k + S * T
   int n_pblk;     // dispatch blocks = ceil(T*k / kPermuteBlock)
-  int max_tiles;  // upper bound on grouped-GEMM row tiles
+  int tile_m;     // rows per row tile: kTileM (bf16 GEMM) or kQTileM (quantized experts)
+  int max_tiles;  // upper bound on row tiles
 };
 
 // One grouped-GEMM row tile: rows [row0, row0 + rows) of the expert-ordered buffers belong to
@@ -45,7 +47,8 @@ struct Meta {
   int refine_count;   // near-tie tokens listed by the router (reset by the refine kernel)
   int refine_done;    // refine CTAs finished (reset by the last one)
   int reroute_rounds; // proposal rounds of the last overflow re-route (diagnostic)
-  int pad[59];
+  int work[2];        // next work unit of the quantized gate/up and down passes
+  int pad[57];
 };
 
 // Offsets of every buffer carved from the caller's workspace (bytes, 256-aligned).
@@ -143,6 +146,24 @@ struct FfnPtrs {
 // ev_mid (optional): recorded on st between the gate/up and the down GEMM.
 cudaError_t launch_grouped_ffn(const Shape& s, const FfnPtrs& p, cudaStream_t st,
                                cudaEvent_t ev_mid = nullptr);
+
+// Weight-only quantized experts (quant_ffn.cu).
+cudaError_t launch_quantize(int bits, int n_mat, int K, int N, const uint16_t* W, uint8_t* q,
+                            uint16_t* scale, uint8_t* zero, cudaStream_t st);
+struct QFfnPtrs {
+  const uint16_t* x;          // [T, d] bf16
+  const uint16_t* xp;         // gathered rows [T*k, d] bf16
+  uint16_t* h;                // H [rows, f] fp16
+  uint16_t* y;                // Y [rows, d] fp16, slot order
+  const int32_t* perm_slot;   // [T*k]
+  const float* topk_w;        // [T*k] or nullptr
+  const TileEntry* tiles;     // kQTileM-row tiles (launch_tiles_and_gather)
+  Meta* meta;
+  const moe_qweights* qw;
+};
+// ev_mid (optional): recorded on st between the gate/up and the down pass.
+cudaError_t launch_quant_ffn(const Shape& s, int bits, const QFfnPtrs& p, cudaStream_t st,
+                             cudaEvent_t ev_mid = nullptr);
 
 cudaError_t launch_combine(const Shape& s, const uint16_t* y, const int32_t* slot_pos,
                            uint16_t* out, cudaStream_t st);

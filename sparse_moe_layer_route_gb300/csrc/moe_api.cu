@@ -60,8 +60,9 @@ Shape make_shape(const moe_config& c) {
   s.C = (int)C;
   s.reroute = c.overflow_reroute != 0 && s.C != INT_MAX;
   s.n_pblk = (int)((s.TK + kPermuteBlock - 1) / kPermuteBlock);
-  s.max_tiles = (int)((s.TK + kTileM - 1) / kTileM + s.E +
-                      (long long)s.S * ((s.T + kTileM - 1) / kTileM));
+  s.tile_m = c.weight_bits != 0 ? kQTileM : kTileM;
+  s.max_tiles = (int)((s.TK + s.tile_m - 1) / s.tile_m + s.E +
+                      (long long)s.S * ((s.T + s.tile_m - 1) / s.tile_m));
   return s;
 }
 
@@ -145,6 +146,8 @@ moe_status check_cfg(const moe_config* c) {
     if ((long long)c->top_k > (long long)c->topk_groups * (c->E / c->n_groups))
       return MOE_ERR_INVALID_ARG;
   }
+  if (c->weight_bits != 0 && c->weight_bits != 4 && c->weight_bits != 8) return MOE_ERR_INVALID_ARG;
+  if (c->weight_bits != 0 && (c->d % 128 != 0 || c->d_ff % 128 != 0)) return MOE_ERR_UNSUPPORTED;
   if (c->overflow_reroute != 0 && c->overflow_reroute != 1) return MOE_ERR_INVALID_ARG;
   if (c->overflow_reroute && c->n_groups > 0) return MOE_ERR_UNSUPPORTED;
   const long long rows = (long long)c->T * (c->top_k + c->n_shared);
@@ -268,18 +271,54 @@ moe_status ffn_impl(const Shape& s, const WsLayout& L, void* ws, const uint16_t*
   return cuda_status(launch_grouped_ffn(s, p, st, ev_gate_up));
 }
 
+bool qmat_ok(const moe_qmatrix& m) { return m.q && m.scale && m.zero; }
+
+bool qweights_ok(const moe_config* c, const moe_qweights* q) {
+  if (q == nullptr || !qmat_ok(q->gate) || !qmat_ok(q->up) || !qmat_ok(q->down)) return false;
+  if (c->n_shared > 0 && (!qmat_ok(q->sh_gate) || !qmat_ok(q->sh_up) || !qmat_ok(q->sh_down)))
+    return false;
+  return true;
+}
+
+moe_status qffn_impl(const Shape& s, int bits, const WsLayout& L, void* ws, const uint16_t* x,
+                     const int32_t* perm_slot, const int32_t* offsets, const float* topk_w,
+                     const moe_qweights* qw, uint16_t* y, cudaStream_t st,
+                     cudaEvent_t ev_gathered = nullptr, cudaEvent_t ev_gate_up = nullptr) {
+  cudaError_t e = launch_tiles_and_gather(s, x, perm_slot, offsets, at<uint16_t>(ws, L.xp),
+                                          at<TileEntry>(ws, L.tiles), at<Meta>(ws, L.meta), st);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (ev_gathered != nullptr && cudaEventRecord(ev_gathered, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  QFfnPtrs p;
+  p.x = x;
+  p.xp = at<uint16_t>(ws, L.xp);
+  p.h = at<uint16_t>(ws, L.h);
+  p.y = y;
+  p.perm_slot = perm_slot;
+  p.topk_w = topk_w;
+  p.tiles = at<TileEntry>(ws, L.tiles);
+  p.meta = at<Meta>(ws, L.meta);
+  p.qw = qw;
+  return cuda_status(launch_quant_ffn(s, bits, p, st, ev_gate_up));
+}
+
 moe_status layer_impl(const moe_config* cfg, const moe_weights* w, const uint16_t* x,
                       const float* gumbel_u, uint16_t* out, moe_route_out* ro, void* ws,
                       size_t ws_bytes, cudaStream_t st, cudaEvent_t const* ev) {
   moe_status r = check_cfg(cfg);
   if (r != MOE_OK) return r;
-  if (!w || !x || !out || !w->W_g || !w->W_gate || !w->W_up || !w->W_down)
-    return MOE_ERR_INVALID_ARG;
+  if (!w || !x || !out || !w->W_g) return MOE_ERR_INVALID_ARG;
+  const bool quant = cfg->weight_bits != 0;
+  if (quant) {
+    if (!qweights_ok(cfg, w->quant)) return MOE_ERR_INVALID_ARG;
+  } else {
+    if (!w->W_gate || !w->W_up || !w->W_down) return MOE_ERR_INVALID_ARG;
+    if (cfg->n_shared > 0 && (!w->Wsh_gate || !w->Wsh_up || !w->Wsh_down))
+      return MOE_ERR_INVALID_ARG;
+    if (w->W_down_f16 && cfg->n_shared > 0 && !w->Wsh_down_f16) return MOE_ERR_INVALID_ARG;
+  }
   if (cfg->mode == MOE_ROUTE_BIAS_SELECT && !w->expert_bias) return MOE_ERR_INVALID_ARG;
   if (cfg->mode == MOE_ROUTE_GUMBEL && !gumbel_u) return MOE_ERR_INVALID_ARG;
-  if (cfg->n_shared > 0 && (!w->Wsh_gate || !w->Wsh_up || !w->Wsh_down))
-    return MOE_ERR_INVALID_ARG;
-  if (w->W_down_f16 && cfg->n_shared > 0 && !w->Wsh_down_f16) return MOE_ERR_INVALID_ARG;
   if ((r = check_ws(cfg, ws, ws_bytes)) != MOE_OK) return r;
   const Shape s = make_shape(*cfg);
   const WsLayout L = ws_layout(s);
@@ -306,11 +345,14 @@ moe_status layer_impl(const moe_config* cfg, const moe_weights* w, const uint16_
   }
   if (!mark(2)) return MOE_ERR_CUDA;
   uint16_t* y = at<uint16_t>(ws, L.y);
-  if ((r = ffn_impl(s, L, ws, x, perm_slot, offsets, gw, w->W_gate, w->W_up, w->W_down,
-                    w->Wsh_gate, w->Wsh_up, w->Wsh_down, w->W_down_f16, w->Wsh_down_f16, y, st,
-                    ev ? ev[3] : nullptr,
-                    ev ? ev[4] : nullptr)) != MOE_OK)
-    return r;
+  if (quant)
+    r = qffn_impl(s, cfg->weight_bits, L, ws, x, perm_slot, offsets, gw, w->quant, y, st,
+                  ev ? ev[3] : nullptr, ev ? ev[4] : nullptr);
+  else
+    r = ffn_impl(s, L, ws, x, perm_slot, offsets, gw, w->W_gate, w->W_up, w->W_down,
+                 w->Wsh_gate, w->Wsh_up, w->Wsh_down, w->W_down_f16, w->Wsh_down_f16, y, st,
+                 ev ? ev[3] : nullptr, ev ? ev[4] : nullptr);
+  if (r != MOE_OK) return r;
   if (!mark(5)) return MOE_ERR_CUDA;
   if ((r = cuda_status(launch_combine(s, y, slot_pos, out, st))) != MOE_OK) return r;
   return mark(6) ? MOE_OK : MOE_ERR_CUDA;
@@ -383,6 +425,33 @@ moe_status moe_overflow_reroute(const moe_config* cfg, const uint16_t* x,
                       (cudaStream_t)stream);
 }
 
+moe_status moe_quantize_weights(int32_t bits, int32_t n_mat, int32_t K, int32_t N,
+                                const uint16_t* W, uint8_t* q_out, uint16_t* scale_out,
+                                uint8_t* zero_out, moe_stream_t stream) {
+  if (bits != 4 && bits != 8) return MOE_ERR_INVALID_ARG;
+  if (n_mat < 1 || K < 1 || N < 1 || !W || !q_out || !scale_out || !zero_out)
+    return MOE_ERR_INVALID_ARG;
+  if (K % 128 != 0 || N % 32 != 0) return MOE_ERR_UNSUPPORTED;
+  return cuda_status(launch_quantize(bits, n_mat, K, N, W, q_out, scale_out, zero_out,
+                                     (cudaStream_t)stream));
+}
+
+moe_status moe_grouped_ffn_quantized(const moe_config* cfg, const uint16_t* x,
+                                     const int32_t* perm_slot, const int32_t* offsets,
+                                     const float* topk_w, const moe_qweights* qw,
+                                     uint16_t* y_slot, void* ws, size_t ws_bytes,
+                                     moe_stream_t stream) {
+  moe_status r = check_cfg(cfg);
+  if (r != MOE_OK) return r;
+  if (cfg->weight_bits == 0) return MOE_ERR_INVALID_ARG;
+  if (!x || !perm_slot || !offsets || !y_slot || !qweights_ok(cfg, qw)) return MOE_ERR_INVALID_ARG;
+  if ((r = check_ws(cfg, ws, ws_bytes)) != MOE_OK) return r;
+  const Shape s = make_shape(*cfg);
+  const WsLayout L = ws_layout(s);
+  return qffn_impl(s, cfg->weight_bits, L, ws, x, perm_slot, offsets, topk_w, qw, y_slot,
+                   (cudaStream_t)stream);
+}
+
 moe_status moe_permute_noalloc(const moe_config* cfg, const int32_t* topk_idx, int32_t* counts,
                                int32_t* offsets, int32_t* perm_slot, int32_t* slot_pos,
                                int32_t* fault_bits, moe_stream_t stream) {
@@ -404,6 +473,7 @@ moe_status moe_grouped_ffn(const moe_config* cfg, const uint16_t* x, const int32
                            size_t ws_bytes, moe_stream_t stream) {
   moe_status r = check_cfg(cfg);
   if (r != MOE_OK) return r;
+  if (cfg->weight_bits != 0) return MOE_ERR_INVALID_ARG;  // see moe_grouped_ffn_quantized
   if (!x || !perm_slot || !offsets || !W_gate || !W_up || !W_down || !y_slot)
     return MOE_ERR_INVALID_ARG;
   if (cfg->n_shared > 0 && (!Wsh_gate || !Wsh_up || !Wsh_down)) return MOE_ERR_INVALID_ARG;

@@ -165,6 +165,7 @@ __global__ void __launch_bounds__(kThreads) scatter_kernel(
 // each shared expert's identity segment over all T tokens.
 __global__ void __launch_bounds__(kThreads) tiles_kernel(const int32_t* __restrict__ offsets,
                                                          int E, int S, int T, long long TK,
+                                                         int tile_m,
                                                          TileEntry* __restrict__ tiles,
                                                          Meta* meta) {
   __shared__ int warp_tot[kThreads / 32];
@@ -176,7 +177,7 @@ __global__ void __launch_bounds__(kThreads) tiles_kernel(const int32_t* __restri
     o0 = offsets[e];
     kept = offsets[e + 1] - o0;
   }
-  const int nt = (kept + kTileM - 1) / kTileM;
+  const int nt = (kept + tile_m - 1) / tile_m;
   int v = nt;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
@@ -194,21 +195,21 @@ __global__ void __launch_bounds__(kThreads) tiles_kernel(const int32_t* __restri
   for (int i = 0; i < nt; ++i) {
     TileEntry te;
     te.expert = e;
-    te.row0 = o0 + i * kTileM;
-    te.rows = min(kTileM, kept - i * kTileM);
+    te.row0 = o0 + i * tile_m;
+    te.rows = min(tile_m, kept - i * tile_m);
     te.arow0 = te.row0;
     te.g0 = start;
     te.gn = nt;
     tiles[start + i] = te;
   }
-  const int per_shared = (T + kTileM - 1) / kTileM;
+  const int per_shared = (T + tile_m - 1) / tile_m;
   for (int i = threadIdx.x; i < S * per_shared; i += kThreads) {
     const int s = i / per_shared, m = i % per_shared;
     TileEntry te;
     te.expert = E + s;
-    te.row0 = (int)(TK + (long long)s * T + (long long)m * kTileM);
-    te.rows = min(kTileM, T - m * kTileM);
-    te.arow0 = m * kTileM;
+    te.row0 = (int)(TK + (long long)s * T + (long long)m * tile_m);
+    te.rows = min(tile_m, T - m * tile_m);
+    te.arow0 = m * tile_m;
     te.g0 = total + s * per_shared;
     te.gn = per_shared;
     tiles[total + i] = te;
@@ -216,6 +217,8 @@ __global__ void __launch_bounds__(kThreads) tiles_kernel(const int32_t* __restri
   if (threadIdx.x == 0) {
     meta->n_tiles = total + S * per_shared;
     meta->n_kept = offsets[E];
+    meta->work[0] = 0;  // work counters of the quantized FFN passes
+    meta->work[1] = 0;
   }
 }
 
@@ -306,7 +309,7 @@ cudaError_t launch_tiles_and_gather(const Shape& s, const uint16_t* x, const int
                                     const int32_t* offsets, uint16_t* xp, TileEntry* tiles,
                                     Meta* meta, cudaStream_t st) {
   cudaError_t e = launch_k(tiles_kernel, dim3(1), dim3(kThreads), 0, st, offsets, s.E, s.S, s.T,
-                           s.TK, tiles, meta);
+                           s.TK, s.tile_m, tiles, meta);
   if (e != cudaSuccess) return e;
   const long long rows_per_blk = kThreads / 32;
   const long long grid = (s.TK + rows_per_blk - 1) / rows_per_blk;

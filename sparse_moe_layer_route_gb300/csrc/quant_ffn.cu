@@ -1,0 +1,382 @@
+// Weight-only group-wise quantized experts ("大模型MoE稀疏激活原理与工程实践", §4.2 量化与混合精度:
+// expert weights to INT4 with one scale and zero-point per 128 weights, the router kept in
+// higher precision).
+//
+// quantize_kernel     one thread per (matrix, group of 128 input rows, output column): min/max,
+//                     fp16 scale, zero-point and codes, all in float64; codes are written in the
+//                     fragment order of include/moe.h (moe_qmatrix).
+// qffn_kernel<B, M>   the expert FFN on the codes, one warp per (expert, 32 output columns):
+//                     M = 0 gate/up with the SwiGLU epilogue into H (fp16), M = 1 down with the
+//                     gate scale into the slot-ordered fp16 rows Y (the same buffers and layouts
+//                     as the bf16 grouped GEMM, so dispatch and combine are shared).
+//
+// Why this shape. At decode sizes an expert sees one or two rows, so the layer is bound by the
+// bytes of the weights it touches; the kernel streams each code once with 16-byte coalesced
+// loads (a warp reads 512 contiguous bytes per load) and the arithmetic per code has to stay
+// below the memory time. The codes become exact fp16 integers (q - z) in registers (a byte or
+// nibble placed into the mantissa of 1024.0, minus 1024 + z), feed mma.sync m16n8k16 as the A
+// operand straight from registers (weights as the M side, up to 8 tokens as N), and each 128-row
+// group's fp32 partial sums are multiplied by the group's scale in fp32, so every product and sum
+// is the one of the dequantized weights (q - z) * s. A tcgen05 MMA would need the dequantized
+// tile in shared memory first: 2 more bytes written and read per weight on top of the code, more
+// shared-memory traffic than the SM has at the HBM rate of 1-byte codes.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kGroup = 128;
+constexpr int kQThreads = 128;  // 4 warps per CTA, each taking work units on its own
+
+// ------------------------------------------------------------------------------ quantization
+template <int BITS>
+__global__ void __launch_bounds__(256) quantize_kernel(const uint16_t* __restrict__ W,
+                                                       uint8_t* __restrict__ q,
+                                                       uint16_t* __restrict__ scale,
+                                                       uint8_t* __restrict__ zero, int n_mat,
+                                                       int K, int N) {
+  const long long groups = (long long)n_mat * (K / kGroup);
+  const long long total = groups * N;
+  const double top = (double)((1 << BITS) - 1);
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int n = (int)(i % N);
+    const long long mg = i / N;  // matrix * K/128 + group
+    const int m = (int)(mg / (K / kGroup));
+    const int grp = (int)(mg % (K / kGroup));
+    const uint16_t* col = W + ((size_t)m * K + (size_t)grp * kGroup) * N + n;
+    double lo = INFINITY, hi = -INFINITY;
+    for (int r = 0; r < kGroup; ++r) {
+      const double w = (double)__uint_as_float((uint32_t)col[(size_t)r * N] << 16);
+      lo = fmin(lo, w);
+      hi = fmax(hi, w);
+    }
+    __half sh = __double2half((hi - lo) / top);
+    double s = (double)__half2float(sh);
+    if (!(s > 0.0) || isinf(s)) {  // no range (or under/overflow): fp16(max |w|), else 1
+      sh = __double2half(fmax(fabs(lo), fabs(hi)));
+      s = (double)__half2float(sh);
+      if (!(s > 0.0) || isinf(s)) {
+        sh = __float2half(1.0f);
+        s = 1.0;
+      }
+    }
+    const double z = fmin(fmax(rint(-lo / s), 0.0), top);
+    scale[mg * N + n] = __half_as_ushort(sh);
+    zero[mg * N + n] = (uint8_t)z;
+    // fragment-order position of (n, k): tile nt, lane, slot j in the step (see moe_qmatrix)
+    const int nt = n / 16, rr = n % 16;
+    for (int r = 0; r < kGroup; ++r) {
+      const double w = (double)__uint_as_float((uint32_t)col[(size_t)r * N] << 16);
+      const int code = (int)fmin(fmax(rint(w / s) + z, 0.0), top);
+      const int k = grp * kGroup + r;
+      const int st = k / 16, kk = k % 16;
+      const int lane = (rr % 8) * 4 + (kk % 8) / 2;
+      const int j = (kk % 2) + 2 * (rr / 8) + 4 * (kk / 8);
+      const size_t tile = (size_t)m * (N / 16) + nt;
+      if (BITS == 8) {
+        const size_t off = (tile * (K / 32) + st / 2) * 512 + lane * 16 + (st % 2) * 8 + j;
+        q[off] = (uint8_t)code;
+      } else {
+        const size_t off = (tile * (K / 64) + st / 4) * 512 + lane * 16 + (st % 4) * 4;
+        atomicOr(reinterpret_cast<unsigned int*>(q + off),
+                 (unsigned int)code << (16 * (j % 2) + 4 * (j / 2)));
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------ FFN
+struct QMat {
+  const uint8_t* q;
+  const uint16_t* s;
+  const uint8_t* z;
+};
+
+struct QArgs {
+  QMat routed[2], shared[2];  // M = 0: gate, up; M = 1: down (index 0)
+  const uint16_t* src;        // M = 0: gathered rows Xp [T*k, K] bf16; M = 1: H [rows, K] fp16
+  const uint16_t* x;          // M = 0: x [T, K] bf16 (shared experts' rows)
+  uint16_t* out;              // M = 0: H [rows, N] fp16; M = 1: Y [rows, N] fp16
+  const TileEntry* tiles;     // 8-row tiles of every expert's rows (device-written)
+  Meta* meta;                 // tile count and the work counters
+  const int32_t* perm_slot;   // M = 1
+  const float* topk_w;        // M = 1 (NULL: gate 1)
+  int E, K, N;
+};
+
+__device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, uint32_t b) {
+  const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&a),
+                            *reinterpret_cast<const __half2*>(&b));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+// A fragment (q - z as exact fp16) of one 16x16 step from its 8 codes.
+// 8-bit: lo = codes j0..j3, hi = codes j4..j7 (one byte each).
+__device__ __forceinline__ void a_frag8(uint32_t lo, uint32_t hi, uint32_t z0, uint32_t z1,
+                                        uint32_t (&a)[4]) {
+  a[0] = hsub2_u32(__byte_perm(lo, 0x64646464u, 0x4140), z0);  // (j0, j1) row g
+  a[1] = hsub2_u32(__byte_perm(lo, 0x64646464u, 0x4342), z1);  // (j2, j3) row g + 8
+  a[2] = hsub2_u32(__byte_perm(hi, 0x64646464u, 0x4140), z0);  // (j4, j5) row g
+  a[3] = hsub2_u32(__byte_perm(hi, 0x64646464u, 0x4342), z1);  // (j6, j7) row g + 8
+}
+
+// 4-bit: one word; slot j at bit 16 * (j % 2) + 4 * (j / 2).
+__device__ __forceinline__ void a_frag4(uint32_t w, uint32_t z0, uint32_t z1, uint32_t (&a)[4]) {
+  a[0] = hsub2_u32((w & 0x000F000Fu) | 0x64006400u, z0);
+  a[1] = hsub2_u32(((w >> 4) & 0x000F000Fu) | 0x64006400u, z1);
+  a[2] = hsub2_u32(((w >> 8) & 0x000F000Fu) | 0x64006400u, z0);
+  a[3] = hsub2_u32(((w >> 12) & 0x000F000Fu) | 0x64006400u, z1);
+}
+
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// bf16 pair -> fp16 pair (activations of the gate/up pass)
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
+  const __half2 h = __floats2half2_rn(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint16_t f16_sat(float v) {
+  return __half_as_ushort(__float2half_rn(fminf(fmaxf(v, -65504.f), 65504.f)));
+}
+
+// One 128-row group's operands, loaded ahead of their use: the codes (NL 16-byte loads per
+// matrix) and the B fragments of its eight 16-row steps.
+template <int NM, int NL>
+struct GroupRegs {
+  uint4 code[NM][NL];
+  uint32_t b[8][2];
+};
+
+template <int BITS, int MODE, int NM, int NL>
+__device__ __forceinline__ void load_group(GroupRegs<NM, NL>& r, const QMat* mats, size_t tile,
+                                           int grp, int KP, int lane, const uint32_t* brow,
+                                           bool tok_ok, int c) {
+#pragma unroll
+  for (int m = 0; m < NM; ++m)
+#pragma unroll
+    for (int l = 0; l < NL; ++l)
+      r.code[m][l] = __ldcs(reinterpret_cast<const uint4*>(
+                                mats[m].q + (tile * KP + (size_t)grp * NL + l) * 512) +
+                            lane);
+#pragma unroll
+  for (int st = 0; st < 8; ++st) {
+    const int k0 = (grp * 8 + st) * 16;
+    r.b[st][0] = tok_ok ? brow[(k0 + 2 * c) / 2] : 0u;
+    r.b[st][1] = tok_ok ? brow[(k0 + 2 * c + 8) / 2] : 0u;
+  }
+}
+
+template <int BITS, int MODE, int NM, int NL>
+__device__ __forceinline__ void compute_group(const GroupRegs<NM, NL>& r, const QMat* mats,
+                                              int ex_ix, int grp, int groups, int N, int n,
+                                              float (&acc)[NM][4]) {
+  float cg[NM][4];
+  uint32_t zz[NM][2];
+  float sc[NM][2];
+#pragma unroll
+  for (int m = 0; m < NM; ++m) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) cg[m][i] = 0.f;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const size_t ix = ((size_t)ex_ix * groups + grp) * N + n + 8 * h;
+      sc[m][h] = __half2float(__ushort_as_half(mats[m].s[ix]));
+      const uint32_t zh = 0x6400u | mats[m].z[ix];  // fp16 1024 + z
+      zz[m][h] = zh | (zh << 16);
+    }
+  }
+#pragma unroll
+  for (int st = 0; st < 8; ++st) {
+    uint32_t b0 = r.b[st][0], b1 = r.b[st][1];
+    if (MODE == 0) {
+      b0 = bf16x2_to_f16x2(b0);
+      b1 = bf16x2_to_f16x2(b1);
+    }
+#pragma unroll
+    for (int m = 0; m < NM; ++m) {
+      uint32_t af[4];
+      if (BITS == 8) {
+        const uint4 v = r.code[m][st / 2];
+        const uint32_t lo = (st & 1) ? v.z : v.x, hi = (st & 1) ? v.w : v.y;
+        a_frag8(lo, hi, zz[m][0], zz[m][1], af);
+      } else {
+        const uint4 v = r.code[m][st / 4];
+        const int q = st & 3;
+        a_frag4(q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w, zz[m][0], zz[m][1], af);
+      }
+      mma16816(cg[m], af, b0, b1);
+    }
+  }
+#pragma unroll
+  for (int m = 0; m < NM; ++m) {
+    acc[m][0] = fmaf(sc[m][0], cg[m][0], acc[m][0]);
+    acc[m][1] = fmaf(sc[m][0], cg[m][1], acc[m][1]);
+    acc[m][2] = fmaf(sc[m][1], cg[m][2], acc[m][2]);
+    acc[m][3] = fmaf(sc[m][1], cg[m][3], acc[m][3]);
+  }
+}
+
+// Work unit = (8-row tile, 16 output columns), taken from a device counter so that units of
+// every length balance across warps. Units with the same column strip run side by side (unit u
+// -> tile u % n_tiles, strip u / n_tiles), so the tiles of one expert share its codes in L2.
+template <int BITS, int MODE>
+__global__ void __launch_bounds__(kQThreads) qffn_kernel(const QArgs a) {
+  constexpr int NM = MODE == 0 ? 2 : 1;  // matrices per unit (gate and up, or down)
+  constexpr int NL = BITS == 8 ? 4 : 2;  // 16-byte code loads per lane per group and matrix
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2, c = lane & 3;
+  griddep_wait();
+  const int n_tiles = a.meta->n_tiles;
+  const int strips = a.N / 16;
+  const long long units = (long long)n_tiles * strips;
+  const int KP = a.K / (16 * (BITS == 8 ? 2 : 4));
+  const int groups = a.K / kGroup;
+  int* counter = &a.meta->work[MODE];
+  while (true) {
+    long long u = 0;
+    if (lane == 0) u = atomicAdd(counter, 1);
+    u = __shfl_sync(0xffffffffu, u, 0);
+    if (u >= units) break;
+    const TileEntry te = a.tiles[u % n_tiles];
+    const int strip = (int)(u / n_tiles);
+    const bool shared = te.expert >= a.E;
+    const int ex_ix = shared ? te.expert - a.E : te.expert;
+    const QMat* mats = shared ? a.shared : a.routed;
+    // this lane's B-fragment token: M = 0 reads Xp (routed) or x (shared) rows, M = 1 H rows
+    const int tok = g;
+    const bool tok_ok = tok < te.rows;
+    const uint16_t* srow;
+    if (MODE == 0)
+      srow = shared ? a.x + (size_t)(te.arow0 + (tok_ok ? tok : 0)) * a.K
+                    : a.src + (size_t)(te.row0 + (tok_ok ? tok : 0)) * a.K;
+    else
+      srow = a.src + (size_t)(te.row0 + (tok_ok ? tok : 0)) * a.K;
+    const uint32_t* brow = reinterpret_cast<const uint32_t*>(srow);
+    const size_t tile = (size_t)ex_ix * (a.N / 16) + strip;
+    const int n = strip * 16 + g;  // this lane's rows of the tile: n and n + 8
+    float acc[NM][4];
+#pragma unroll
+    for (int m = 0; m < NM; ++m)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[m][i] = 0.f;
+    // two groups in flight: the loads of group i + 1 are issued before group i is computed
+    GroupRegs<NM, NL> ra, rb;
+    load_group<BITS, MODE, NM, NL>(ra, mats, tile, 0, KP, lane, brow, tok_ok, c);
+    for (int grp = 0; grp < groups; grp += 2) {
+      if (grp + 1 < groups)
+        load_group<BITS, MODE, NM, NL>(rb, mats, tile, grp + 1, KP, lane, brow, tok_ok, c);
+      compute_group<BITS, MODE, NM, NL>(ra, mats, ex_ix, grp, groups, a.N, n, acc);
+      if (grp + 1 < groups) {
+        if (grp + 2 < groups)
+          load_group<BITS, MODE, NM, NL>(ra, mats, tile, grp + 2, KP, lane, brow, tok_ok, c);
+        compute_group<BITS, MODE, NM, NL>(rb, mats, ex_ix, grp + 1, groups, a.N, n, acc);
+      }
+    }
+    // epilogue: element i is (column n + 8 (i / 2), token 2 c + i % 2 of the tile)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int t = 2 * c + (i & 1);
+      if (t >= te.rows) continue;
+      long long orow = te.row0 + t;
+      float gate = 1.f;
+      if (MODE == 1 && !shared) {
+        const int slot = a.perm_slot[te.row0 + t];
+        orow = slot;
+        if (a.topk_w != nullptr) gate = a.topk_w[slot];
+      }
+      const int col = n + 8 * (i >> 1);
+      float v;
+      if (MODE == 0) {
+        const float gv = acc[0][i], uv = acc[NM - 1][i];
+        v = gv / (1.0f + __expf(-gv)) * uv;
+      } else {
+        v = gate * acc[0][i];
+      }
+      a.out[orow * a.N + col] = f16_sat(v);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_quantize(int bits, int n_mat, int K, int N, const uint16_t* W, uint8_t* q,
+                            uint16_t* scale, uint8_t* zero, cudaStream_t st) {
+  const size_t code_bytes = (size_t)n_mat * K * N * bits / 8;
+  if (bits == 4) {  // nibbles are OR-ed into zeroed words
+    const cudaError_t e = cudaMemsetAsync(q, 0, code_bytes, st);
+    if (e != cudaSuccess) return e;
+  }
+  const long long total = (long long)n_mat * (K / kGroup) * N;
+  const int grid = (int)std::min<long long>((total + 255) / 256, 8LL * num_sms());
+  if (bits == 8)
+    quantize_kernel<8><<<grid, 256, 0, st>>>(W, q, scale, zero, n_mat, K, N);
+  else
+    quantize_kernel<4><<<grid, 256, 0, st>>>(W, q, scale, zero, n_mat, K, N);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_ffn(const Shape& s, int bits, const QFfnPtrs& p, cudaStream_t st,
+                             cudaEvent_t ev_mid) {
+  QArgs a{};
+  a.E = s.E;
+  a.tiles = p.tiles;
+  a.meta = p.meta;
+  a.perm_slot = p.perm_slot;
+  a.topk_w = p.topk_w;
+  const int sms = num_sms();
+  // persistent: as many CTAs as fit (work units come from the counters in Meta)
+  auto grid_of = [&](void (*k)(const QArgs)) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kQThreads, 0) != cudaSuccess ||
+        per_sm < 1)
+      per_sm = 1;
+    return dim3(per_sm * sms);
+  };
+  // ---- gate/up: K = d, N = d_ff
+  a.routed[0] = {p.qw->gate.q, p.qw->gate.scale, p.qw->gate.zero};
+  a.routed[1] = {p.qw->up.q, p.qw->up.scale, p.qw->up.zero};
+  a.shared[0] = {p.qw->sh_gate.q, p.qw->sh_gate.scale, p.qw->sh_gate.zero};
+  a.shared[1] = {p.qw->sh_up.q, p.qw->sh_up.scale, p.qw->sh_up.zero};
+  a.src = p.xp;
+  a.x = p.x;
+  a.out = p.h;
+  a.K = s.d;
+  a.N = s.f;
+  cudaError_t err;
+  if (bits == 8)
+    err = launch_k(qffn_kernel<8, 0>, grid_of(qffn_kernel<8, 0>), dim3(kQThreads), 0, st, a);
+  else
+    err = launch_k(qffn_kernel<4, 0>, grid_of(qffn_kernel<4, 0>), dim3(kQThreads), 0, st, a);
+  if (err != cudaSuccess) return err;
+  if (ev_mid != nullptr && (err = cudaEventRecord(ev_mid, st)) != cudaSuccess) return err;
+  // ---- down: K = d_ff, N = d
+  a.routed[0] = {p.qw->down.q, p.qw->down.scale, p.qw->down.zero};
+  a.routed[1] = a.routed[0];
+  a.shared[0] = {p.qw->sh_down.q, p.qw->sh_down.scale, p.qw->sh_down.zero};
+  a.shared[1] = a.shared[0];
+  a.src = p.h;
+  a.x = nullptr;
+  a.out = p.y;
+  a.K = s.f;
+  a.N = s.d;
+  if (bits == 8)
+    return launch_k(qffn_kernel<8, 1>, grid_of(qffn_kernel<8, 1>), dim3(kQThreads), 0, st, a);
+  return launch_k(qffn_kernel<4, 1>, grid_of(qffn_kernel<4, 1>), dim3(kQThreads), 0, st, a);
+}
+
+}  // namespace moe

@@ -11,7 +11,8 @@ Contract (per token):
   * counts / offsets / perm_slot / slot_pos bit-exact against the oracle dispatch run on the
     GPU's indices;
   * layer output (bf16) against the oracle's float64 output conditioned on the GPU's indices:
-    max-abs <= 2e-2 and relative L2 <= 1e-2.
+    max-abs <= 2e-2 and relative L2 <= 1e-2 (with quantized experts, the oracle runs on its own
+    quantize-dequantize of the same bf16 weights).
   * with the Level-2 overflow re-route: the router's own indices (before the re-route) follow
     the rule above; the oracle's re-route walk, run on those indices, must give the GPU's final
     indices, unless the first token where they differ had an oracle re-route decision gap below
@@ -56,9 +57,22 @@ def pack_down(inp):
     return inp
 
 
+def quantize_inputs(inp, bits):
+    """GPU group-wise quantization of every expert matrix (one-time weight preparation)."""
+    key = f"q{bits}"
+    if key not in inp:
+        names = ("W_gate", "W_up", "W_down", "Ws_gate", "Ws_up", "Ws_down")
+        qs = {n: (M.quantize_weights(inp[n], bits) if inp.get(n) is not None else None)
+              for n in names}
+        inp[key] = qs
+        inp[key + "_struct"] = M.make_qweights(*[qs[n] for n in names])
+    return inp[key], inp[key + "_struct"]
+
+
 def run_layer(cfg, inp, capacity_override=0, stream=None, f16=True):
     """moe_layer_forward with every routing output requested; returns numpy arrays.
-    f16: use the fp16 down path (W_down re-encoded once), else the bf16 down path."""
+    f16: use the fp16 down path (W_down re-encoded once), else the bf16 down path.
+    With cfg.weight_bits the experts are quantized on the GPU first."""
     mc = M.MoeConfig.from_layer(cfg)
     mc.capacity_override = capacity_override
     T, k, E, d = cfg.T, cfg.k, cfg.E, cfg.d
@@ -72,12 +86,17 @@ def run_layer(cfg, inp, capacity_override=0, stream=None, f16=True):
     slot_pos = torch.full((T * k,), -7, **i32)
     out = torch.full((T, d), float("nan"), dtype=torch.bfloat16, device=dev)
     ws = M.alloc_workspace(mc, dev)
-    if f16:
-        pack_down(inp)
-    weights = M.make_weights(inp["W_g"], inp["bias"], inp["W_gate"], inp["W_up"], inp["W_down"],
-                             inp.get("Ws_gate"), inp.get("Ws_up"), inp.get("Ws_down"),
-                             inp.get("W_down_f16") if f16 else None,
-                             inp.get("Ws_down_f16") if f16 else None)
+    bits = getattr(cfg, "weight_bits", 0)
+    if bits:
+        _, qstruct = quantize_inputs(inp, bits)
+        weights = M.make_weights(inp["W_g"], inp["bias"], None, None, None, quant=qstruct)
+    else:
+        if f16:
+            pack_down(inp)
+        weights = M.make_weights(inp["W_g"], inp["bias"], inp["W_gate"], inp["W_up"],
+                                 inp["W_down"], inp.get("Ws_gate"), inp.get("Ws_up"),
+                                 inp.get("Ws_down"), inp.get("W_down_f16") if f16 else None,
+                                 inp.get("Ws_down_f16") if f16 else None)
     ro = M.make_route_out(idx, w, counts, offsets, perm_slot, slot_pos)
     primary = None
     if getattr(cfg, "reroute", False):
@@ -95,15 +114,23 @@ def run_layer(cfg, inp, capacity_override=0, stream=None, f16=True):
     return res
 
 
-def expert_getter(inp):
+def _oracle_weights(mats, bits):
+    """bf16 matrices widened, or (bits > 0) the oracle's own quantize-dequantize of them."""
+    ws = tuple(f64(m) for m in mats)
+    if bits:
+        ws = tuple(O.dequantize_groupwise(*O.quantize_groupwise(w, bits)) for w in ws)
+    return ws
+
+
+def expert_getter(inp, bits=0):
     def get(e):
-        return (f64(inp["W_gate"][e]), f64(inp["W_up"][e]), f64(inp["W_down"][e]))
+        return _oracle_weights((inp["W_gate"][e], inp["W_up"][e], inp["W_down"][e]), bits)
     return get
 
 
-def shared_getter(inp):
+def shared_getter(inp, bits=0):
     def get(s):
-        return (f64(inp["Ws_gate"][s]), f64(inp["Ws_up"][s]), f64(inp["Ws_down"][s]))
+        return _oracle_weights((inp["Ws_gate"][s], inp["Ws_up"][s], inp["Ws_down"][s]), bits)
     return get
 
 
@@ -145,8 +172,9 @@ def check_layer(cfg, inp, gpu, tokens=None, capacity_override=0, x64=None, r=Non
     p = O.permute(idx_g, E, C)
     for key in ("counts", "offsets", "perm_slot", "slot_pos"):
         assert np.array_equal(gpu[key], p[key]), f"{key} differs from the oracle dispatch"
-    out_ref, _ = O.layer_from_routing(x64, idx_g, w_cond, E, C, expert_getter(inp), cfg.S,
-                                      shared_getter(inp), tokens)
+    bits = getattr(cfg, "weight_bits", 0)
+    out_ref, _ = O.layer_from_routing(x64, idx_g, w_cond, E, C, expert_getter(inp, bits), cfg.S,
+                                      shared_getter(inp, bits), tokens)
     out_t = gpu["out_t"] if tokens is None else gpu["out_t"][torch.as_tensor(tokens)]
     out_g = f64(out_t)
     err = np.abs(out_g - out_ref)

@@ -51,6 +51,7 @@ def test_workspace_size_and_layout(lib):
     (dict(overflow_reroute=2), 1), (dict(overflow_reroute=1, n_groups=4, topk_groups=2), 2),
     (dict(n_groups=3), 2), (dict(n_groups=4, topk_groups=0), 1),
     (dict(n_groups=4, topk_groups=1, top_k=3), 1),
+    (dict(weight_bits=5), 1), (dict(weight_bits=8, d=192), 2), (dict(weight_bits=4), 0),
 ])
 def test_bad_configs_rejected(lib, kw, status):
     base = dict(T=64, d=128, E=8, top_k=2, d_ff=128, n_shared=0, mode=0, tau=1.0,
@@ -124,3 +125,19 @@ def test_reroute_workspace_and_validation(lib):
                                     None) == 1     # x missing
     assert lib.moe_overflow_reroute(ctypes.byref(on), P, None, None, P, P, P, P, None, 1 << 30,
                                     None) == 3     # no workspace
+
+
+def test_quantize_weights_validation(lib):
+    P = ctypes.c_void_p(0x1000)
+    assert lib.moe_quantize_weights(3, 1, 128, 32, P, P, P, P, None) == 1     # bits
+    assert lib.moe_quantize_weights(8, 0, 128, 32, P, P, P, P, None) == 1     # n_mat
+    assert lib.moe_quantize_weights(8, 1, 192, 32, P, P, P, P, None) == 2     # K % 128
+    assert lib.moe_quantize_weights(4, 1, 128, 48, P, P, P, P, None) == 2     # N % 32
+    assert lib.moe_quantize_weights(4, 1, 128, 32, None, P, P, P, None) == 1  # W missing
+    cfg = M.MoeConfig.make(64, 128, 8, 2, 128, weight_bits=8)
+    q = M.MoeQWeights()
+    assert lib.moe_grouped_ffn_quantized(ctypes.byref(cfg), P, P, P, None, ctypes.byref(q), P,
+                                         P, 1 << 30, None) == 1            # codes missing
+    cfg0 = M.MoeConfig.make(64, 128, 8, 2, 128)
+    assert lib.moe_grouped_ffn_quantized(ctypes.byref(cfg0), P, P, P, None, ctypes.byref(q), P,
+                                         P, 1 << 30, None) == 1            # weight_bits 0

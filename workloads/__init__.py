@@ -53,6 +53,7 @@ class LayerConfig:
     n_groups: int = 0          # group-limited routing (0: off)
     topk_groups: int = 0
     reroute: bool = False      # Level-2 overflow re-route (with a capacity limit)
+    weight_bits: int = 0       # 0: bf16 experts; 4 / 8: group-wise quantized experts
     description: str = ""
 
     def as_dict(self):
@@ -81,6 +82,14 @@ CONFIGS = {
         capacity_factor=1.25, seed=3, bias="zipf", zipf_s=1.1, reroute=True,
         description="the skewed prefill with Level-2 overflow re-route: dropped slots move to "
                     "the best expert with room"),
+    "decode_int8": LayerConfig(
+        "decode_int8", T=64, d=7168, E=128, k=2, f=2048, S=1, mode=PLAIN, seed=2, weight_bits=8,
+        description="the decode shape with 8-bit group-wise quantized experts (128 weights per "
+                    "group)"),
+    "decode_int4": LayerConfig(
+        "decode_int4", T=64, d=7168, E=128, k=2, f=2048, S=1, mode=PLAIN, seed=2, weight_bits=4,
+        description="the decode shape with 4-bit group-wise quantized experts (128 weights per "
+                    "group)"),
     "gumbel": LayerConfig(
         "gumbel", T=8192, d=4096, E=16, k=2, f=14336, S=0, mode=GUMBEL, tau=0.5, seed=4,
         description="Gumbel top-2: T=8192 d=4096 E=16 k=2 d_ff=14336, tau=0.5"),
@@ -89,12 +98,12 @@ CONFIGS = {
 
 def small_config(name="small", T=64, d=128, E=8, k=2, f=128, S=0, mode=PLAIN, tau=1.0,
                  capacity_factor=0.0, seed=0, bias="zero", bias_var=0.0, zipf_s=1.1,
-                 n_groups=0, topk_groups=0, reroute=False):
+                 n_groups=0, topk_groups=0, reroute=False, weight_bits=0):
     """A config for tests at sizes the oracle finishes in seconds."""
     return LayerConfig(name, T=T, d=d, E=E, k=k, f=f, S=S, mode=mode, tau=tau,
                        capacity_factor=capacity_factor, seed=seed, bias=bias,
                        bias_var=bias_var, zipf_s=zipf_s, n_groups=n_groups,
-                       topk_groups=topk_groups, reroute=reroute)
+                       topk_groups=topk_groups, reroute=reroute, weight_bits=weight_bits)
 
 
 def skew_scale() -> float:
