@@ -154,95 +154,139 @@ __device__ __forceinline__ uint16_t f16_sat(float v) {
   return __half_as_ushort(__float2half_rn(fminf(fmaxf(v, -65504.f), 65504.f)));
 }
 
-// One 128-row group's operands, loaded ahead of their use: the codes (NL 16-byte loads per
-// matrix) and the B fragments of its eight 16-row steps.
-template <int NM, int NL>
-struct GroupRegs {
-  uint4 code[NM][NL];
-  uint32_t b[8][2];
-};
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
-template <int BITS, int MODE, int NM, int NL>
-__device__ __forceinline__ void load_group(GroupRegs<NM, NL>& r, const QMat* mats, size_t tile,
-                                           int grp, int KP, int lane, const uint32_t* brow,
-                                           bool tok_ok, int c) {
+constexpr int kStages = 3;  // 128-row groups of codes in flight per warp (shared-memory ring)
+
+// Codes of one 128-row group of one unit into ring stage `stage`: NM matrices x TL 16-column
+// tiles x NL 512-byte blocks, each lane copying its own 16 bytes of every block (and later
+// reading only those).
+template <int NM, int TL, int NL>
+__device__ __forceinline__ void issue_group(uint32_t ring, int stage, const QMat* mats,
+                                            size_t tile0, int grp, int KP, int lane) {
 #pragma unroll
   for (int m = 0; m < NM; ++m)
 #pragma unroll
-    for (int l = 0; l < NL; ++l)
-      r.code[m][l] = __ldcs(reinterpret_cast<const uint4*>(
-                                mats[m].q + (tile * KP + (size_t)grp * NL + l) * 512) +
-                            lane);
+    for (int t = 0; t < TL; ++t)
 #pragma unroll
-  for (int st = 0; st < 8; ++st) {
-    const int k0 = (grp * 8 + st) * 16;
-    r.b[st][0] = tok_ok ? brow[(k0 + 2 * c) / 2] : 0u;
-    r.b[st][1] = tok_ok ? brow[(k0 + 2 * c + 8) / 2] : 0u;
-  }
+      for (int l = 0; l < NL; ++l)
+        cp_async16(ring + (uint32_t)(((((stage * NM + m) * TL + t) * NL + l) * 32 + lane) * 16),
+                   mats[m].q + ((tile0 + t) * KP + (size_t)grp * NL + l) * 512 + lane * 16);
 }
 
-template <int BITS, int MODE, int NM, int NL>
-__device__ __forceinline__ void compute_group(const GroupRegs<NM, NL>& r, const QMat* mats,
-                                              int ex_ix, int grp, int groups, int N, int n,
-                                              float (&acc)[NM][4]) {
-  float cg[NM][4];
-  uint32_t zz[NM][2];
-  float sc[NM][2];
+// Scale (fp32) and zero-point (fp16 1024 + z, doubled) of this lane's two rows n, n + 8 of
+// every tile in one group, for every matrix of the unit.
+template <int NM, int TL>
+struct GroupQ {
+  float sc[NM][TL][2];
+  uint32_t zz[NM][TL][2];
+};
+
+template <int NM, int TL>
+__device__ __forceinline__ void load_group_q(GroupQ<NM, TL>& q, const QMat* mats, int ex_ix,
+                                             int grp, int groups, int N, int n, bool ok) {
 #pragma unroll
-  for (int m = 0; m < NM; ++m) {
+  for (int m = 0; m < NM; ++m)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) cg[m][i] = 0.f;
+    for (int t = 0; t < TL; ++t)
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const size_t ix = ((size_t)ex_ix * groups + grp) * N + n + 8 * h;
-      sc[m][h] = __half2float(__ushort_as_half(mats[m].s[ix]));
-      const uint32_t zh = 0x6400u | mats[m].z[ix];  // fp16 1024 + z
-      zz[m][h] = zh | (zh << 16);
-    }
-  }
+      for (int h = 0; h < 2; ++h) {
+        const size_t ix = ((size_t)ex_ix * groups + (ok ? grp : 0)) * N + n + 16 * t + 8 * h;
+        q.sc[m][t][h] = __half2float(__ushort_as_half(mats[m].s[ix]));
+        const uint32_t zh = 0x6400u | mats[m].z[ix];
+        q.zz[m][t][h] = zh | (zh << 16);
+      }
+}
+
+template <int BITS, int MODE, int NM, int TL, int NL>
+__device__ __forceinline__ void compute_group(const uint4 (&code)[NM][TL][NL],
+                                              const uint32_t (&bq)[8][2],
+                                              const GroupQ<NM, TL>& q,
+                                              float (&acc)[NM][TL][4]) {
+  float cg[NM][TL][4];
+#pragma unroll
+  for (int m = 0; m < NM; ++m)
+#pragma unroll
+    for (int t = 0; t < TL; ++t)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) cg[m][t][i] = 0.f;
 #pragma unroll
   for (int st = 0; st < 8; ++st) {
-    uint32_t b0 = r.b[st][0], b1 = r.b[st][1];
+    uint32_t b0 = bq[st][0], b1 = bq[st][1];
     if (MODE == 0) {
       b0 = bf16x2_to_f16x2(b0);
       b1 = bf16x2_to_f16x2(b1);
     }
 #pragma unroll
-    for (int m = 0; m < NM; ++m) {
-      uint32_t af[4];
-      if (BITS == 8) {
-        const uint4 v = r.code[m][st / 2];
-        const uint32_t lo = (st & 1) ? v.z : v.x, hi = (st & 1) ? v.w : v.y;
-        a_frag8(lo, hi, zz[m][0], zz[m][1], af);
-      } else {
-        const uint4 v = r.code[m][st / 4];
-        const int q = st & 3;
-        a_frag4(q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w, zz[m][0], zz[m][1], af);
+    for (int m = 0; m < NM; ++m)
+#pragma unroll
+      for (int t = 0; t < TL; ++t) {
+        uint32_t af[4];
+        if (BITS == 8) {
+          const uint4 v = code[m][t][st / 2];
+          const uint32_t lo = (st & 1) ? v.z : v.x, hi = (st & 1) ? v.w : v.y;
+          a_frag8(lo, hi, q.zz[m][t][0], q.zz[m][t][1], af);
+        } else {
+          const uint4 v = code[m][t][st / 4];
+          const int qq = st & 3;
+          a_frag4(qq == 0 ? v.x : qq == 1 ? v.y : qq == 2 ? v.z : v.w, q.zz[m][t][0],
+                  q.zz[m][t][1], af);
+        }
+        mma16816(cg[m][t], af, b0, b1);
       }
-      mma16816(cg[m], af, b0, b1);
-    }
   }
 #pragma unroll
-  for (int m = 0; m < NM; ++m) {
-    acc[m][0] = fmaf(sc[m][0], cg[m][0], acc[m][0]);
-    acc[m][1] = fmaf(sc[m][0], cg[m][1], acc[m][1]);
-    acc[m][2] = fmaf(sc[m][1], cg[m][2], acc[m][2]);
-    acc[m][3] = fmaf(sc[m][1], cg[m][3], acc[m][3]);
-  }
+  for (int m = 0; m < NM; ++m)
+#pragma unroll
+    for (int t = 0; t < TL; ++t) {
+      acc[m][t][0] = fmaf(q.sc[m][t][0], cg[m][t][0], acc[m][t][0]);
+      acc[m][t][1] = fmaf(q.sc[m][t][0], cg[m][t][1], acc[m][t][1]);
+      acc[m][t][2] = fmaf(q.sc[m][t][1], cg[m][t][2], acc[m][t][2]);
+      acc[m][t][3] = fmaf(q.sc[m][t][1], cg[m][t][3], acc[m][t][3]);
+    }
 }
 
-// Work unit = (8-row tile, 16 output columns), taken from a device counter so that units of
+// 16-column tiles per work unit: 4-bit groups carry half the bytes of 8-bit ones, so a 4-bit
+// unit takes two tiles to give each group the same code bytes and twice the MMAs per activation.
+template <int BITS>
+__host__ __device__ constexpr int tiles_per_unit() {
+  return BITS == 8 ? 1 : 2;
+}
+
+template <int NM, int TL, int NL>
+__host__ __device__ constexpr int ring_bytes_per_warp() {
+  return kStages * NM * TL * NL * 512;
+}
+
+// Work unit = (8-row tile, 16 * TL output columns), taken from a device counter so that units of
 // every length balance across warps. Units with the same column strip run side by side (unit u
 // -> tile u % n_tiles, strip u / n_tiles), so the tiles of one expert share its codes in L2.
+// Each warp keeps kStages groups of codes in flight through its shared-memory ring (cp.async,
+// 16 bytes per lane per block); the activations of the next group are loaded into registers
+// while the current one is computed.
 template <int BITS, int MODE>
 __global__ void __launch_bounds__(kQThreads) qffn_kernel(const QArgs a) {
   constexpr int NM = MODE == 0 ? 2 : 1;  // matrices per unit (gate and up, or down)
-  constexpr int NL = BITS == 8 ? 4 : 2;  // 16-byte code loads per lane per group and matrix
-  const int lane = threadIdx.x & 31;
+  constexpr int NL = BITS == 8 ? 4 : 2;  // 512-byte code blocks per group, matrix and tile
+  constexpr int TL = tiles_per_unit<BITS>();
+  constexpr int RB = ring_bytes_per_warp<NM, TL, NL>();
+  extern __shared__ __align__(16) uint8_t qsmem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
+  const uint32_t ring = (uint32_t)__cvta_generic_to_shared(qsmem) + (uint32_t)(warp * RB);
+  const uint4* ring4 = reinterpret_cast<const uint4*>(qsmem + warp * RB);
   griddep_wait();
   const int n_tiles = a.meta->n_tiles;
-  const int strips = a.N / 16;
+  const int strips = a.N / (16 * TL);
   const long long units = (long long)n_tiles * strips;
   const int KP = a.K / (16 * (BITS == 8 ? 2 : 4));
   const int groups = a.K / kGroup;
@@ -257,6 +301,13 @@ __global__ void __launch_bounds__(kQThreads) qffn_kernel(const QArgs a) {
     const bool shared = te.expert >= a.E;
     const int ex_ix = shared ? te.expert - a.E : te.expert;
     const QMat* mats = shared ? a.shared : a.routed;
+    const size_t tile0 = (size_t)ex_ix * (a.N / 16) + (size_t)strip * TL;
+    // start the ring: groups 0 .. kStages - 2
+#pragma unroll
+    for (int s = 0; s < kStages - 1; ++s) {
+      if (s < groups) issue_group<NM, TL, NL>(ring, s, mats, tile0, s, KP, lane);
+      cp_async_commit();
+    }
     // this lane's B-fragment token: M = 0 reads Xp (routed) or x (shared) rows, M = 1 H rows
     const int tok = g;
     const bool tok_ok = tok < te.rows;
@@ -267,27 +318,58 @@ __global__ void __launch_bounds__(kQThreads) qffn_kernel(const QArgs a) {
     else
       srow = a.src + (size_t)(te.row0 + (tok_ok ? tok : 0)) * a.K;
     const uint32_t* brow = reinterpret_cast<const uint32_t*>(srow);
-    const size_t tile = (size_t)ex_ix * (a.N / 16) + strip;
-    const int n = strip * 16 + g;  // this lane's rows of the tile: n and n + 8
-    float acc[NM][4];
+    const int n = strip * 16 * TL + g;  // this lane's rows of tile t: n + 16 t and n + 16 t + 8
+    float acc[NM][TL][4];
 #pragma unroll
     for (int m = 0; m < NM; ++m)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) acc[m][i] = 0.f;
-    // two groups in flight: the loads of group i + 1 are issued before group i is computed
-    GroupRegs<NM, NL> ra, rb;
-    load_group<BITS, MODE, NM, NL>(ra, mats, tile, 0, KP, lane, brow, tok_ok, c);
-    for (int grp = 0; grp < groups; grp += 2) {
-      if (grp + 1 < groups)
-        load_group<BITS, MODE, NM, NL>(rb, mats, tile, grp + 1, KP, lane, brow, tok_ok, c);
-      compute_group<BITS, MODE, NM, NL>(ra, mats, ex_ix, grp, groups, a.N, n, acc);
-      if (grp + 1 < groups) {
-        if (grp + 2 < groups)
-          load_group<BITS, MODE, NM, NL>(ra, mats, tile, grp + 2, KP, lane, brow, tok_ok, c);
-        compute_group<BITS, MODE, NM, NL>(rb, mats, ex_ix, grp + 1, groups, a.N, n, acc);
-      }
+      for (int t = 0; t < TL; ++t)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[m][t][i] = 0.f;
+    uint32_t bq[8][2];
+#pragma unroll
+    for (int st = 0; st < 8; ++st) {
+      bq[st][0] = tok_ok ? brow[(st * 16 + 2 * c) / 2] : 0u;
+      bq[st][1] = tok_ok ? brow[(st * 16 + 2 * c + 8) / 2] : 0u;
     }
-    // epilogue: element i is (column n + 8 (i / 2), token 2 c + i % 2 of the tile)
+    GroupQ<NM, TL> gq;
+    load_group_q<NM, TL>(gq, mats, ex_ix, 0, groups, a.N, n, true);
+    for (int grp = 0; grp < groups; ++grp) {
+      const int ahead = grp + kStages - 1;
+      if (ahead < groups)
+        issue_group<NM, TL, NL>(ring, ahead % kStages, mats, tile0, ahead, KP, lane);
+      cp_async_commit();
+      cp_async_wait<kStages - 1>();  // this lane's copies of group grp have landed
+      uint4 code[NM][TL][NL];
+      const int stage = grp % kStages;
+#pragma unroll
+      for (int m = 0; m < NM; ++m)
+#pragma unroll
+        for (int t = 0; t < TL; ++t)
+#pragma unroll
+          for (int l = 0; l < NL; ++l)
+            code[m][t][l] = ring4[(((stage * NM + m) * TL + t) * NL + l) * 32 + lane];
+      // the next group's activations, scales and zero-points, loaded during this group's MMAs
+      uint32_t bn[8][2];
+#pragma unroll
+      for (int st = 0; st < 8; ++st) {
+        const int k0 = ((grp + 1) * 8 + st) * 16;
+        const bool ok = tok_ok && grp + 1 < groups;
+        bn[st][0] = ok ? brow[(k0 + 2 * c) / 2] : 0u;
+        bn[st][1] = ok ? brow[(k0 + 2 * c + 8) / 2] : 0u;
+      }
+      GroupQ<NM, TL> gn;
+      load_group_q<NM, TL>(gn, mats, ex_ix, grp + 1, groups, a.N, n, grp + 1 < groups);
+      compute_group<BITS, MODE, NM, TL, NL>(code, bq, gq, acc);
+#pragma unroll
+      for (int st = 0; st < 8; ++st) {
+        bq[st][0] = bn[st][0];
+        bq[st][1] = bn[st][1];
+      }
+      gq = gn;
+    }
+    cp_async_wait<0>();
+    // epilogue: element i of tile t is (column n + 16 t + 8 (i / 2), token 2 c + i % 2)
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int t = 2 * c + (i & 1);
@@ -299,15 +381,18 @@ __global__ void __launch_bounds__(kQThreads) qffn_kernel(const QArgs a) {
         orow = slot;
         if (a.topk_w != nullptr) gate = a.topk_w[slot];
       }
-      const int col = n + 8 * (i >> 1);
-      float v;
-      if (MODE == 0) {
-        const float gv = acc[0][i], uv = acc[NM - 1][i];
-        v = gv / (1.0f + __expf(-gv)) * uv;
-      } else {
-        v = gate * acc[0][i];
+#pragma unroll
+      for (int t = 0; t < TL; ++t) {
+        const int col = n + 16 * t + 8 * (i >> 1);
+        float v;
+        if (MODE == 0) {
+          const float gv = acc[0][t][i], uv = acc[NM - 1][t][i];
+          v = gv / (1.0f + __expf(-gv)) * uv;
+        } else {
+          v = gate * acc[0][t][i];
+        }
+        a.out[orow * a.N + col] = f16_sat(v);
       }
-      a.out[orow * a.N + col] = f16_sat(v);
     }
   }
 }
@@ -340,9 +425,19 @@ cudaError_t launch_quant_ffn(const Shape& s, int bits, const QFfnPtrs& p, cudaSt
   a.topk_w = p.topk_w;
   const int sms = num_sms();
   // persistent: as many CTAs as fit (work units come from the counters in Meta)
-  auto grid_of = [&](void (*k)(const QArgs)) {
+  auto smem_of = [&](int mode) {
+    const int rb = bits == 8 ? (mode == 0 ? ring_bytes_per_warp<2, tiles_per_unit<8>(), 4>()
+                                          : ring_bytes_per_warp<1, tiles_per_unit<8>(), 4>())
+                             : (mode == 0 ? ring_bytes_per_warp<2, tiles_per_unit<4>(), 2>()
+                                          : ring_bytes_per_warp<1, tiles_per_unit<4>(), 2>());
+    return (size_t)(kQThreads / 32) * rb;
+  };
+  auto grid_of = [&](void (*k)(const QArgs), size_t smem) {
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kQThreads, 0) != cudaSuccess ||
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kQThreads, smem) !=
+            cudaSuccess ||
         per_sm < 1)
       per_sm = 1;
     return dim3(per_sm * sms);
@@ -358,10 +453,13 @@ cudaError_t launch_quant_ffn(const Shape& s, int bits, const QFfnPtrs& p, cudaSt
   a.K = s.d;
   a.N = s.f;
   cudaError_t err;
+  const size_t sm0 = smem_of(0), sm1 = smem_of(1);
   if (bits == 8)
-    err = launch_k(qffn_kernel<8, 0>, grid_of(qffn_kernel<8, 0>), dim3(kQThreads), 0, st, a);
+    err = launch_k(qffn_kernel<8, 0>, grid_of(qffn_kernel<8, 0>, sm0), dim3(kQThreads), sm0, st,
+                   a);
   else
-    err = launch_k(qffn_kernel<4, 0>, grid_of(qffn_kernel<4, 0>), dim3(kQThreads), 0, st, a);
+    err = launch_k(qffn_kernel<4, 0>, grid_of(qffn_kernel<4, 0>, sm0), dim3(kQThreads), sm0, st,
+                   a);
   if (err != cudaSuccess) return err;
   if (ev_mid != nullptr && (err = cudaEventRecord(ev_mid, st)) != cudaSuccess) return err;
   // ---- down: K = d_ff, N = d
@@ -375,8 +473,10 @@ cudaError_t launch_quant_ffn(const Shape& s, int bits, const QFfnPtrs& p, cudaSt
   a.K = s.f;
   a.N = s.d;
   if (bits == 8)
-    return launch_k(qffn_kernel<8, 1>, grid_of(qffn_kernel<8, 1>), dim3(kQThreads), 0, st, a);
-  return launch_k(qffn_kernel<4, 1>, grid_of(qffn_kernel<4, 1>), dim3(kQThreads), 0, st, a);
+    return launch_k(qffn_kernel<8, 1>, grid_of(qffn_kernel<8, 1>, sm1), dim3(kQThreads), sm1, st,
+                    a);
+  return launch_k(qffn_kernel<4, 1>, grid_of(qffn_kernel<4, 1>, sm1), dim3(kQThreads), sm1, st,
+                  a);
 }
 
 }  // namespace moe
