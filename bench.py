@@ -41,9 +41,10 @@ NCU_TRAFFIC = {("fine_grained", "gate_up_gemm"): (878.894336e6 + 67.953920e6),
 # router, histogram, scan, scatter, tile list, gather, gate/up, down, combine (+ router weight
 # padding when E is not a multiple of 64)
 def launches_per_step(cfg):
-    """Kernels of one layer call: router (weight prep, GEMM, selection, near-tie pass), dispatch
-    (histogram, scan, scatter), tile list, gather, the two grouped GEMMs and the combine; the
-    overflow re-route adds its three kernels and a second dispatch."""
+    """Kernels of one layer call: router (weight prep, GEMM, selection, exact near-tie pass),
+    dispatch (histogram, scan, scatter), tile list, gather, the two grouped GEMMs (or the
+    two quantized FFN passes) and the combine; the overflow re-route adds its three kernels and a
+    second dispatch."""
     n = 12
     if getattr(cfg, "reroute", False) and cfg.capacity_factor > 0:
         n += 3 + 3

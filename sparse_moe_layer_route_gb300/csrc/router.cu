@@ -8,14 +8,14 @@
 // (logits - log(-log u)) / tau from "GPT-4 Has 1.8 Trillion Parameters. It Uses 2% of Them Per
 // Token", §3.1 门控网络.
 //
-// Three kernels (plus the per-call weight preparation):
+// Two kernels (plus the per-call weight preparation):
 //  * router_gemm_kernel: CTA (row tile of 128 tokens, K slice). Warp 0 streams x tiles [128 x 64]
 //    (K-major) and W_g chunks [64 x 64] (expert-major, i.e. N-major) with TMA; warp 1 issues
 //    tcgen05.mma (M=128, N=E rounded up to 64, K=16) into TMEM; warps 4-7 write the fp32 partial
 //    logits of the slice. Splitting K fills the GPU when T is small (one row tile at decode).
-//  * select_kernel: per token, the K-slice partials summed in slice order, selection scores,
-//    top-(k+1) by k+1 branch-free argmax passes over scores staged in shared memory (two threads
-//    per token, four independent chains each), softmax gates, and the near-tie test.
+//  * select_kernel: 32 tokens per CTA, 8 threads per token. The K-slice partials summed in slice
+//    order, selection scores, top-(k+1) by k+1 argmax passes (each thread over its eighth of the
+//    experts, then a 3-step shuffle reduction), softmax gates and the near-tie test.
 //  * refine_kernel: the exact re-decision of the near-tie tokens (below).
 //
 // Exactness. The tensor core's fp32 accumulation differs from an exactly rounded dot product by
@@ -24,10 +24,12 @@
 // conservative band (router_band: 2.5e-4 x sqrt(d / 7168) x max(1, |largest logit of the row|),
 // about 6x the largest measured error) is flagged together with its candidate experts: every
 // expert whose tensor-core score lies within the band of the k-th score (only those can be in
-// the exact top-k). refine_kernel recomputes the candidates' logits as plain fp32 dot products
-// (error ~1e-7) and re-decides the token's top-k and gates. Tokens outside the band cannot change
-// their selection or order under the tensor-core error. Flagged tokens are appended to a list
-// (order irrelevant: each token is re-decided on its own), spread over all refine CTAs.
+// the exact top-k), or all experts when there are more than 16 of them or the group decision of
+// group-limited routing is itself that close. refine_kernel recomputes the candidates' logits as
+// plain fp32 dot products (error ~1e-7) and re-decides the token's top-k and gates. Tokens outside
+// the band cannot change their selection or order under the tensor-core error. Flagged tokens are
+// appended to a list (order irrelevant: each token is re-decided on its own) and spread over all
+// refine CTAs, a whole CTA per token, which keeps the pass short however the flags cluster.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <climits>
@@ -209,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 struct SelectArgs {
-  const float* part;
+  const float* part;   // [splits, T, EP]
   const float* bias;
   const float* u;
   int32_t* topk_idx;
@@ -225,36 +227,66 @@ struct SelectArgs {
   float tau;
 };
 
-// Two threads per token (scores [128][EP + 4] staged in dynamic shared memory: rows stay 16-byte
-// aligned and 128-bit reads of consecutive rows hit distinct banks). The pass loop is kept rolled
-// (its picks live in shared memory) so the kernel's code stays small.
-__global__ void __launch_bounds__(kThreads) select_kernel(const SelectArgs a) {
+constexpr int kSelRows = 32;              // tokens per selection CTA
+constexpr int kSelP = 8;                  // threads per token
+constexpr int kSelThreads = kSelRows * kSelP;
+
+// Group-limited routing: group scores (largest member score), the Gk best groups (ties to the
+// lower group) as a bit mask, and the gap between the Gk-th and the next group score.
+__device__ __forceinline__ unsigned long long pick_groups(const float* gm, int G, int Gk,
+                                                          float* gap) {
+  unsigned long long sel = 0ull;
+  float ps_g = INFINITY, kth = INFINITY, next = -INFINITY;
+  int pg = -1;
+  const int passes = Gk < G ? Gk + 1 : Gk;
+  for (int j = 0; j < passes; ++j) {
+    float bs = -INFINITY;
+    int bg = INT_MAX;
+    for (int gi = 0; gi < G; ++gi) {
+      const float v = gm[gi];
+      const bool after = v < ps_g || (v == ps_g && gi > pg);
+      if (after && beats(v, gi, bs, bg)) {
+        bs = v;
+        bg = gi;
+      }
+    }
+    if (j < Gk) {
+      sel |= 1ull << bg;
+      kth = bs;
+    } else {
+      next = bs;
+    }
+    ps_g = bs;
+    pg = bg;
+  }
+  *gap = Gk < G ? kth - next : INFINITY;
+  return sel;
+}
+
+__global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a) {
   extern __shared__ __align__(16) float ssm[];
-  const int LD = a.EP + 4;
-  float* scores = ssm;                                      // [128][LD]
-  float* maxl = scores + kBM * LD;                          // [128]
-  float* sel_s = maxl + kBM;                                // [2 parity][2 halves][128]
-  int* sel_e = reinterpret_cast<int*>(sel_s + 4 * kBM);     // [2][2][128]
-  float* pick_s = reinterpret_cast<float*>(sel_e + 4 * kBM);  // [kList][128]
-  int* pick_e = reinterpret_cast<int*>(pick_s + kList * kBM);  // [kList][128]
-  float* gmax = reinterpret_cast<float*>(pick_e + kList * kBM);  // [128][G] group scores
-  unsigned long long* gsel = reinterpret_cast<unsigned long long*>(gmax + kBM * a.G);  // [128]
-  float* gmarg = reinterpret_cast<float*>(gsel + kBM);          // [128] group-decision gap
+  const int LD = a.EP + 4;  // rows stay 16-byte aligned; 128-bit reads of consecutive rows
+                            // hit distinct banks
+  float* scores = ssm;                                        // [32][LD]
+  float* maxl = scores + kSelRows * LD;                       // [32]
+  float* gmax = maxl + kSelRows;                              // [32][G]
+  unsigned long long* gsel =
+      reinterpret_cast<unsigned long long*>(gmax + kSelRows * (a.G > 0 ? a.G : 0));  // [32]
+  float* gmarg = reinterpret_cast<float*>(gsel + kSelRows);   // [32]
   griddep_wait();
   const bool gumbel = a.mode == MOE_ROUTE_GUMBEL;
-  const int t0 = blockIdx.x * kBM;
-  // phase 1: all threads read the block's partial-logit tiles with coalesced 16-byte loads
-  // (every K slice of four groups in flight together), add the slices in slice order, and turn
-  // each logit into its selection score
+  const int t0 = blockIdx.x * kSelRows;
+  const int rows = min(kSelRows, a.T - t0);
+  // phase 1: the block's partial-logit tiles with coalesced 16-byte loads (every K slice of four
+  // groups in flight together), summed in slice order and turned into selection scores
   int* maxl_bits = reinterpret_cast<int*>(maxl);  // |logit| >= 0: int order = float order
-  if (threadIdx.x < kBM) maxl_bits[threadIdx.x] = 0;
+  if (threadIdx.x < kSelRows) maxl_bits[threadIdx.x] = 0;
   __syncthreads();
   {
     const int ep4 = a.EP / 4;
     const float4* __restrict__ P = reinterpret_cast<const float4*>(a.part);
-    const int rows = min(kBM, a.T - t0);
 #pragma unroll 4
-    for (int i = threadIdx.x; i < rows * ep4; i += kThreads) {
+    for (int i = threadIdx.x; i < rows * ep4; i += kSelThreads) {
       const int rr = i / ep4, c = (i - rr * ep4) * 4;
       const int tt = t0 + rr;
       float4 v[8];
@@ -290,168 +322,143 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const SelectArgs a) {
   __syncthreads();
   if (a.sfull != nullptr) {
     // the overflow re-route ranks every expert of a token: keep the scores and the row scale
-    const int rows = min(kBM, a.T - t0);
-    for (int i = threadIdx.x; i < rows * a.E; i += kThreads) {
+    for (int i = threadIdx.x; i < rows * a.E; i += kSelThreads) {
       const int rr = i / a.E, e = i - rr * a.E;
       a.sfull[(size_t)(t0 + rr) * a.E + e] = scores[rr * LD + e];
     }
     if (threadIdx.x < rows) a.maxl_out[t0 + threadIdx.x] = maxl[threadIdx.x];
   }
-  const int r = threadIdx.x & (kBM - 1), h = threadIdx.x >> 7;
+  const int r = threadIdx.x / kSelP, h = threadIdx.x % kSelP;
   const int t = t0 + r;
-  const bool row_ok = t < a.T;
+  const bool row_ok = r < rows;
   float* srow = scores + r * LD;
-  const int half = ((a.E + 1) / 2 + 3) & ~3;  // multiple of 4: float4 reads
-  const int e_lo = h * half, e_hi = min(a.E, e_lo + half);
+  const int chunk = ((a.E + kSelP - 1) / kSelP + 3) & ~3;  // multiple of 4: float4 reads
+  const int e_lo = h * chunk, e_hi = min(a.E, e_lo + chunk);
   if (a.G > 0) {
-    // group-limited routing: group score = largest score of its experts; keep the Gk best
-    // groups (ties to the lower group), the other experts' scores become -inf
+    // group-limited routing: experts outside the kept groups get -inf
     const int gsz = a.E / a.G;
     if (row_ok)
-      for (int gi = h; gi < a.G; gi += 2) {
+      for (int gi = h; gi < a.G; gi += kSelP) {
         float m = -INFINITY;
         for (int e = gi * gsz; e < (gi + 1) * gsz; ++e) m = fmaxf(m, srow[e]);
         gmax[r * a.G + gi] = m;
       }
     __syncthreads();
-    if (row_ok && h == 0) {
-      unsigned long long sel = 0ull;
-      float ps_g = INFINITY, kth = INFINITY, next = -INFINITY;
-      int pg = -1;
-      const int passes = a.Gk < a.G ? a.Gk + 1 : a.Gk;
-      for (int j = 0; j < passes; ++j) {
-        float bs = -INFINITY;
-        int bg = INT_MAX;
-        for (int gi = 0; gi < a.G; ++gi) {
-          const float v = gmax[r * a.G + gi];
-          const bool after = v < ps_g || (v == ps_g && gi > pg);
-          if (after && beats(v, gi, bs, bg)) {
-            bs = v;
-            bg = gi;
-          }
-        }
-        if (j < a.Gk) {
-          sel |= 1ull << bg;
-          kth = bs;
-        } else {
-          next = bs;
-        }
-        ps_g = bs;
-        pg = bg;
-      }
-      gsel[r] = sel;
-      gmarg[r] = a.Gk < a.G ? kth - next : INFINITY;
-    }
+    if (row_ok && h == 0) gsel[r] = pick_groups(gmax + r * a.G, a.G, a.Gk, &gmarg[r]);
     __syncthreads();
     if (row_ok) {
       const unsigned long long sel = gsel[r];
       for (int e = e_lo; e < e_hi; ++e)
         if (!((sel >> (e / gsz)) & 1ull)) srow[e] = -INFINITY;
     }
-    __syncthreads();
+    __syncwarp();
   }
   const int k = a.k;
   const int nl = k < a.E ? k + 1 : k;  // top-(k+1), or all E when k == E
-  // pass j: the best expert strictly after pick j-1 in (score desc, index asc) order
+  // pass j: the best expert strictly after pick j-1 in (score desc, index asc) order; each of
+  // the token's 8 threads scans its experts, then a shuffle reduction over the 8 lanes
+  float pick_s[kList];
+  int pick_e[kList];
   float ps = INFINITY;
   int pe = -1;
+#pragma unroll
+  for (int j = 0; j < kList; ++j) {
+    if (j < nl) {
+      float bs[2] = {-INFINITY, -INFINITY};
+      int be[2] = {INT_MAX, INT_MAX};
+      if (row_ok) {
+        const float4* s4 = reinterpret_cast<const float4*>(srow);
 #pragma unroll 1
-  for (int j = 0; j < nl; ++j) {
-    float bs[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-    int be[4] = {INT_MAX, INT_MAX, INT_MAX, INT_MAX};
-    if (row_ok) {
-      // 16 scores per step: four 128-bit reads issued together, one chain per read
-      const float4* s4 = reinterpret_cast<const float4*>(srow);
-#pragma unroll 1
-      for (int e = e_lo; e < e_hi; e += 16) {
-        float4 v[4];
+        for (int e = e_lo; e < e_hi; e += 8) {
+          // may read up to 7 floats past this thread's range (still inside the row's padded
+          // storage or the next row); those lanes fail the ee < e_hi test below
+          const float4 v0 = s4[e >> 2], v1 = s4[(e >> 2) + 1];
+          const float vv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
-        // may read up to 12 floats past this row (the next row, or for the last row the arrays
-        // that follow it in shared memory); those lanes fail the ee < e_hi test below
-        for (int c = 0; c < 4; ++c) v[c] = s4[(e >> 2) + c];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const float vv[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int ee = e + 4 * c + q;
+          for (int q = 0; q < 8; ++q) {
+            const int ee = e + q;
             const float sc = vv[q];
             const bool after = sc < ps || (sc == ps && ee > pe);
-            if (ee < e_hi && after && beats(sc, ee, bs[c], be[c])) {
-              bs[c] = sc;
-              be[c] = ee;
+            if (ee < e_hi && after && beats(sc, ee, bs[q & 1], be[q & 1])) {
+              bs[q & 1] = sc;
+              be[q & 1] = ee;
             }
           }
         }
       }
-    }
+      if (beats(bs[1], be[1], bs[0], be[0])) {
+        bs[0] = bs[1];
+        be[0] = be[1];
+      }
 #pragma unroll
-    for (int c = 1; c < 4; ++c)
-      if (beats(bs[c], be[c], bs[0], be[0])) {
-        bs[0] = bs[c];
-        be[0] = be[c];
+      for (int off = kSelP / 2; off > 0; off >>= 1) {
+        const float os = __shfl_xor_sync(0xffffffffu, bs[0], off);
+        const int oe = __shfl_xor_sync(0xffffffffu, be[0], off);
+        if (beats(os, oe, bs[0], be[0])) {
+          bs[0] = os;
+          be[0] = oe;
+        }
       }
-    sel_s[((j & 1) * 2 + h) * kBM + r] = bs[0];
-    sel_e[((j & 1) * 2 + h) * kBM + r] = be[0];
-    __syncthreads();
-    const float os = sel_s[((j & 1) * 2 + (h ^ 1)) * kBM + r];
-    const int oe = sel_e[((j & 1) * 2 + (h ^ 1)) * kBM + r];
-    if (beats(os, oe, bs[0], be[0])) {
-      bs[0] = os;
-      be[0] = oe;
+      pick_s[j] = bs[0];
+      pick_e[j] = be[0];
+      ps = bs[0];
+      pe = be[0];
     }
-    if (h == 0) {
-      pick_s[j * kBM + r] = bs[0];
-      pick_e[j * kBM + r] = be[0];
-    }
-    ps = bs[0];
-    pe = be[0];
   }
-  if (!row_ok || h != 0) return;  // after the last barrier
-  // near-tie test (scores in their own units: GUMBEL scores carry 1/tau)
-  float min_gap = INFINITY;
-  for (int j = 1; j < nl; ++j)
-    min_gap = fminf(min_gap, pick_s[(j - 1) * kBM + r] - pick_s[j * kBM + r]);
-  const float sk = pick_s[(k - 1) * kBM + r];
-  float band = router_band(a.d, maxl[r]);
-  if (gumbel) band /= a.tau;
-  int nc = 0;
-  if (a.G > 0 && gmarg[r] < band) {
-    nc = -1;  // the group decision itself is uncertain: recompute every expert exactly
-    a.rlist[atomicAdd(a.rcount, 1)] = t;
-  } else if (min_gap < band) {
-    // candidates: every expert scoring within the band of the k-th score
-    for (int e = 0; e < a.E; ++e) {
-      if (srow[e] >= sk - band) {
-        if (nc < kMaxCand) a.cand[(size_t)t * kMaxCand + nc] = e;
-        ++nc;
+  if (row_ok && h == 0) {
+    // near-tie test (scores in their own units: GUMBEL scores carry 1/tau)
+    float min_gap = INFINITY;
+#pragma unroll
+    for (int j = 1; j < kList; ++j)
+      if (j < nl) min_gap = fminf(min_gap, pick_s[j - 1] - pick_s[j]);
+    float sk = pick_s[0];
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j)
+      if (j == k - 1) sk = pick_s[j];
+    float band = router_band(a.d, maxl[r]);
+    if (gumbel) band /= a.tau;
+    int nc = 0;
+    if (a.G > 0 && gmarg[r] < band) {
+      nc = -1;  // the group decision itself is uncertain: recompute every expert exactly
+      a.rlist[atomicAdd(a.rcount, 1)] = t;
+    } else if (min_gap < band) {
+      // candidates: every expert scoring within the band of the k-th score
+      for (int e = 0; e < a.E; ++e) {
+        if (srow[e] >= sk - band) {
+          if (nc < kMaxCand) a.cand[(size_t)t * kMaxCand + nc] = e;
+          ++nc;
+        }
       }
+      nc = nc <= kMaxCand ? nc : -1;
+      a.rlist[atomicAdd(a.rcount, 1)] = t;
     }
-    nc = nc <= kMaxCand ? nc : -1;
-    a.rlist[atomicAdd(a.rcount, 1)] = t;
-  }
-  a.ncand[t] = nc;
-  // gates: softmax over the selected logits (PLAIN: the score; BIAS_SELECT: score - bias,
-  // within one rounding of the logit) or over the selected scores (GUMBEL)
-  float mx = -INFINITY;
-  for (int j = 0; j < k; ++j) {
-    const float s = pick_s[j * kBM + r];
-    const float av = a.mode == MOE_ROUTE_BIAS_SELECT ? s - a.bias[pick_e[j * kBM + r]] : s;
-    mx = fmaxf(mx, av);
-  }
-  float sum = 0.f;
-  for (int j = 0; j < k; ++j) {
-    const float s = pick_s[j * kBM + r];
-    const float av = a.mode == MOE_ROUTE_BIAS_SELECT ? s - a.bias[pick_e[j * kBM + r]] : s;
-    sum += expf(av - mx);
-  }
-  const float inv = 1.0f / sum;
-  for (int j = 0; j < k; ++j) {
-    const float s = pick_s[j * kBM + r];
-    const int e = pick_e[j * kBM + r];
-    const float av = a.mode == MOE_ROUTE_BIAS_SELECT ? s - a.bias[e] : s;
-    a.topk_idx[(size_t)t * k + j] = e;
-    a.topk_w[(size_t)t * k + j] = expf(av - mx) * inv;
+    a.ncand[t] = nc;
+    {
+      // gates: softmax over the selected logits (PLAIN: the score; BIAS_SELECT: score - bias,
+      // within one rounding of the logit) or over the selected scores (GUMBEL)
+      float av[kMaxK];
+      float mx = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j)
+        if (j < k) {
+          av[j] = a.mode == MOE_ROUTE_BIAS_SELECT ? pick_s[j] - a.bias[pick_e[j]] : pick_s[j];
+          mx = fmaxf(mx, av[j]);
+        }
+      float sum = 0.f;
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j)
+        if (j < k) {
+          av[j] = expf(av[j] - mx);
+          sum += av[j];
+        }
+      const float inv = 1.0f / sum;
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j)
+        if (j < k) {
+          a.topk_idx[(size_t)t * k + j] = pick_e[j];
+          a.topk_w[(size_t)t * k + j] = av[j] * inv;
+        }
+    }
   }
 }
 
@@ -680,6 +687,8 @@ cudaError_t launch_router(const Shape& s, const uint16_t* x, const uint16_t* W_g
   a.cand = rs.cand;
   a.rlist = rs.rlist;
   a.rcount = rs.rcount;
+  a.sfull = rs.sfull;
+  a.maxl_out = rs.maxl;
   a.T = s.T;
   a.E = s.E;
   a.EP = EP;
@@ -689,16 +698,15 @@ cudaError_t launch_router(const Shape& s, const uint16_t* x, const uint16_t* W_g
   a.splits = splits;
   a.G = s.G;
   a.Gk = s.Gk;
-  a.sfull = rs.sfull;
-  a.maxl_out = rs.maxl;
   a.tau = s.tau;
-  // group-limited routing adds the group scores, the kept-group masks and the group gaps
-  const size_t smem = sizeof(float) * ((size_t)kBM * (EP + 4) + kBM + 8 * kBM + 2 * kList * kBM +
-                                       (s.G > 0 ? (size_t)kBM * (s.G + 3) : 0));
+  const size_t smem =
+      sizeof(float) * ((size_t)kSelRows * (EP + 4) + kSelRows + (size_t)kSelRows * s.G +
+                       2 * kSelRows + kSelRows);
   err = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);
   if (err != cudaSuccess) return err;
-  err = launch_k(select_kernel, dim3(n_mt), dim3(kThreads), smem, st, a);
+  err = launch_k(select_kernel, dim3((s.T + kSelRows - 1) / kSelRows), dim3(kSelThreads), smem,
+                 st, a);
   if (err != cudaSuccess) return err;
   const int rgrid = 2 * num_sms();
   return launch_k(refine_kernel, dim3(rgrid), dim3(kThreads), 0, st, x, (const uint16_t*)rs.wg_t,
