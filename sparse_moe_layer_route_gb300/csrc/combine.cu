@@ -18,8 +18,7 @@ namespace {
 constexpr int kThreads = 256;
 
 // acc += 8 fp16 values (exact widening to fp32)
-__device__ __forceinline__ void add8(float (&acc)[8], const uint16_t* p) {
-  const uint4 v = *reinterpret_cast<const uint4*>(p);
+__device__ __forceinline__ void add8(float (&acc)[8], const uint4 v) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -30,9 +29,11 @@ __device__ __forceinline__ void add8(float (&acc)[8], const uint16_t* p) {
   }
 }
 
-// Grid (column blocks, tokens): thread = one 8-column group of one token. The token's slot
-// flags are the same for the whole block (broadcast loads); every row's 16-byte load of the
-// group is issued before the sum.
+// Grid (column blocks, tokens): thread = one 8-column group of one token. Without a capacity
+// limit every slot is kept, so every row's 16-byte load is issued at once; with one, a row is
+// loaded only when its slot was kept (dropped slots' rows are never written), the flags first.
+// Then the fixed-order sum.
+template <bool MAY_DROP, int KR, int SR>  // KR >= top_k, SR >= n_shared: the row registers
 __global__ void __launch_bounds__(kThreads) combine_kernel(const uint16_t* __restrict__ y,
                                                            const int32_t* __restrict__ slot_pos,
                                                            uint16_t* __restrict__ out, int T,
@@ -42,14 +43,26 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const uint16_t* __res
   const int g = blockIdx.x * kThreads + threadIdx.x;
   if (g >= d / 8) return;
   const long long TK = (long long)T * k;
+  const uint4* __restrict__ y4 = reinterpret_cast<const uint4*>(y);
+  const long long d8 = d / 8;
+  uint4 vr[KR], vs[SR > 0 ? SR : 1];
+  bool kept[KR];
+#pragma unroll
+  for (int j = 0; j < KR; ++j)
+    if (j < k) kept[j] = !MAY_DROP || slot_pos[(long long)t * k + j] >= 0;
+#pragma unroll
+  for (int j = 0; j < KR; ++j)
+    if (j < k) vr[j] = kept[j] ? y4[((long long)t * k + j) * d8 + g] : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+  for (int s = 0; s < SR; ++s)
+    if (s < S) vs[s] = y4[(TK + (long long)s * T + t) * d8 + g];
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int j = 0; j < 8; ++j)  // top_k <= 8
-    if (j < k && slot_pos[(long long)t * k + j] >= 0)
-      add8(acc, y + ((long long)t * k + j) * d + 8 * g);
+  for (int j = 0; j < KR; ++j)
+    if (j < k && kept[j]) add8(acc, vr[j]);
 #pragma unroll
-  for (int s = 0; s < 4; ++s)  // n_shared <= 4
-    if (s < S) add8(acc, y + (TK + (long long)s * T + t) * d + 8 * g);
+  for (int s = 0; s < SR; ++s)
+    if (s < S) add8(acc, vs[s]);
   uint32_t o[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -57,6 +70,21 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const uint16_t* __res
     o[i] = *reinterpret_cast<const uint32_t*>(&b);
   }
   *reinterpret_cast<uint4*>(out + (size_t)t * d + 8 * g) = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+template <bool MAY_DROP>
+cudaError_t launch_combine_variant(const Shape& s, const uint16_t* y, const int32_t* slot_pos,
+                                   uint16_t* out, cudaStream_t st) {
+  const dim3 grid((s.d / 8 + kThreads - 1) / kThreads, s.T);
+  const dim3 block(kThreads);
+  if (s.k <= 2 && s.S <= 1)
+    return launch_k(combine_kernel<MAY_DROP, 2, 1>, grid, block, 0, st, y, slot_pos, out, s.T,
+                    s.d, s.k, s.S);
+  if (s.S <= 1)
+    return launch_k(combine_kernel<MAY_DROP, 8, 1>, grid, block, 0, st, y, slot_pos, out, s.T,
+                    s.d, s.k, s.S);
+  return launch_k(combine_kernel<MAY_DROP, 8, 4>, grid, block, 0, st, y, slot_pos, out, s.T, s.d,
+                  s.k, s.S);
 }
 
 // dst[i] = fp16(bf16 src[i]), round to nearest even, saturating; 8 elements per thread.
@@ -98,9 +126,9 @@ cudaError_t launch_pack_f16(const uint16_t* src, uint16_t* dst, size_t n, cudaSt
 
 cudaError_t launch_combine(const Shape& s, const uint16_t* y, const int32_t* slot_pos,
                            uint16_t* out, cudaStream_t st) {
-  const dim3 grid((s.d / 8 + kThreads - 1) / kThreads, s.T);
-  return launch_k(combine_kernel, grid, dim3(kThreads), 0, st, y, slot_pos, out, s.T, s.d, s.k,
-                  s.S);
+  if (s.C < s.TK)  // a slot may be dropped
+    return launch_combine_variant<true>(s, y, slot_pos, out, st);
+  return launch_combine_variant<false>(s, y, slot_pos, out, st);
 }
 
 }  // namespace moe

@@ -234,7 +234,21 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const uint16_t* __rest
   const int t = perm_slot[p] / k;
   const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d);
   uint4* dst = reinterpret_cast<uint4*>(xp + (size_t)p * d);
-  for (int c = threadIdx.x & 31; c < d / 8; c += 32) dst[c] = src[c];
+  const int lane = threadIdx.x & 31, n = d / 8;
+  // eight 16-byte loads in flight per lane before their stores
+  for (int c0 = 0; c0 < n; c0 += 8 * 32) {
+    uint4 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int c = c0 + i * 32 + lane;
+      if (c < n) v[i] = src[c];
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int c = c0 + i * 32 + lane;
+      if (c < n) __stcs(dst + c, v[i]);
+    }
+  }
 }
 
 }  // namespace
