@@ -186,18 +186,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t fb = full_bar(stage);
         ptx::mbar_arrive_expect_tx(fb, C::kStageBytes);
         ptx::tma_load_2d(sA, tA, fb, kb * kBK, arow);
+        // one copy per weight matrix: its 64-column chunks are the map's third dimension
         if (MODE == 0) {
           // chunks [0, NCH/2): gate columns; [NCH/2, NCH): up columns of the same n range
-#pragma unroll
-          for (int c = 0; c < NCH / 2; ++c) {
-            const int n = nt * (BN / 2) + c * kChunkN;
-            ptx::tma_load_3d(sB + c * kChunkBytes, tB0, fb, n, kb * kBK, ex);
-            ptx::tma_load_3d(sB + (c + NCH / 2) * kChunkBytes, tB1, fb, n, kb * kBK, ex);
-          }
+          ptx::tma_load_4d(sB, tB0, fb, 0, kb * kBK, nt * (NCH / 2), ex);
+          ptx::tma_load_4d(sB + (NCH / 2) * kChunkBytes, tB1, fb, 0, kb * kBK, nt * (NCH / 2),
+                           ex);
         } else {
-#pragma unroll
-          for (int c = 0; c < NCH; ++c)
-            ptx::tma_load_3d(sB + c * kChunkBytes, tB0, fb, nt * BN + c * kChunkN, kb * kBK, ex);
+          ptx::tma_load_4d(sB, tB0, fb, 0, kb * kBK, nt * NCH, ex);
         }
         issued_mask |= 1u << stage;
         last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
@@ -374,9 +370,21 @@ bool make_map_a(CUtensorMap* m, const void* ptr, long long rows, long long K,
   return make_tmap_2d(m, ptr, rows, K, kBK, kBM, dt);
 }
 
+// Weights [n_exp, K, N] seen as [n_exp][N/64 chunks][K][64]: dims (64 columns, K, chunk,
+// expert), box (64, 64, chunks per copy, 1), so one copy lands `chunks` 8 KB chunks back to back.
 bool make_map_b(CUtensorMap* m, const void* ptr, long long n_exp, long long K, long long N,
-                CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
-  return make_tmap_3d(m, ptr, n_exp, K, N, kChunkN, kBK, dt);
+                int chunks, CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
+  auto fn = encode_fn_impl();
+  if (fn == nullptr || N % kChunkN != 0) return false;
+  const cuuint64_t dims[4] = {(cuuint64_t)kChunkN, (cuuint64_t)K, (cuuint64_t)(N / kChunkN),
+                              (cuuint64_t)n_exp};
+  const cuuint64_t strides[3] = {(cuuint64_t)N * 2, (cuuint64_t)kChunkN * 2,
+                                 (cuuint64_t)K * N * 2};
+  const cuuint32_t box[4] = {(cuuint32_t)kChunkN, (cuuint32_t)kBK, (cuuint32_t)chunks, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(m, dt, 4, const_cast<void*>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int MODE, int NCH, bool HF16>
@@ -400,12 +408,13 @@ cudaError_t launch_pair(const Shape& s, const FfnPtrs& p, cudaStream_t st, cudaE
   const uint16_t* Wsd = HF16 ? p.Wsh_down_f16 : p.Wsh_down;
   // ---- gate/up: A = gathered rows (routed) or x (shared); B = W_gate / W_up
   CUtensorMap m0[6];
+  const int gu_chunks = s.f % 128 == 0 ? 2 : 1;  // chunks per matrix and copy (NCH / 2)
   bool ok = make_map_a(&m0[0], p.xp, s.TK, s.d) && make_map_a(&m0[1], p.x, s.T, s.d) &&
-            make_map_b(&m0[2], p.W_gate, s.E, s.d, s.f) &&
-            make_map_b(&m0[3], p.W_up, s.E, s.d, s.f);
+            make_map_b(&m0[2], p.W_gate, s.E, s.d, s.f, gu_chunks) &&
+            make_map_b(&m0[3], p.W_up, s.E, s.d, s.f, gu_chunks);
   if (has_shared)
-    ok = ok && make_map_b(&m0[4], p.Wsh_gate, s.S, s.d, s.f) &&
-         make_map_b(&m0[5], p.Wsh_up, s.S, s.d, s.f);
+    ok = ok && make_map_b(&m0[4], p.Wsh_gate, s.S, s.d, s.f, gu_chunks) &&
+         make_map_b(&m0[5], p.Wsh_up, s.S, s.d, s.f, gu_chunks);
   else {
     m0[4] = m0[2];
     m0[5] = m0[3];
@@ -432,9 +441,11 @@ cudaError_t launch_pair(const Shape& s, const FfnPtrs& p, cudaStream_t st, cudaE
 
   // ---- down: A = H rows; B = W_down; epilogue scales by the gate and writes slot order (fp32)
   CUtensorMap m1[6];
-  ok = make_map_a(&m1[0], p.h, rows, s.f, kHType) && make_map_b(&m1[2], Wd, s.E, s.f, s.d, kHType);
+  const int dn_chunks = s.d % 256 == 0 ? 4 : (s.d % 128 == 0 ? 2 : 1);  // NCH of the down pass
+  ok = make_map_a(&m1[0], p.h, rows, s.f, kHType) &&
+       make_map_b(&m1[2], Wd, s.E, s.f, s.d, dn_chunks, kHType);
   if (has_shared)
-    ok = ok && make_map_b(&m1[4], Wsd, s.S, s.f, s.d, kHType);
+    ok = ok && make_map_b(&m1[4], Wsd, s.S, s.f, s.d, dn_chunks, kHType);
   else
     m1[4] = m1[2];
   if (!ok) return cudaErrorInvalidValue;
