@@ -36,10 +36,9 @@ L2_FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # DRAM bytes (read + write) per launch from one ncu capture of the current kernel, by
 # (workload, phase): profiles/grouped_gemm_fine_grained.md. Re-capture after changing the kernel.
-NCU_TRAFFIC = {("fine_grained", "gate_up_gemm"): (878.894336e6 + 67.953920e6),
-               ("fine_grained", "down_gemm"): (473.472000e6 + 93.796352e6)}
-# router, histogram, scan, scatter, tile list, gather, gate/up, down, combine (+ router weight
-# padding when E is not a multiple of 64)
+NCU_TRAFFIC = {}  # (workload, phase) -> DRAM bytes read + written per launch, from ncu
+
+
 def launches_per_step(cfg):
     """Kernels of one layer call: router (weight prep, GEMM, selection, exact near-tie pass),
     dispatch (histogram, scan, scatter), tile list, gather, the two grouped GEMMs (or the

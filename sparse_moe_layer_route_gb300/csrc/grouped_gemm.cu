@@ -351,6 +351,271 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ------------------------------------------------------------------------------ CTA pairs
+// The same grouped GEMM on pairs of CTAs (a cluster of two) sharing one tcgen05 MMA of M = 256:
+// a work unit is a 256-row tile of one expert x a 256-column tile; CTA rank r stages rows
+// [128 r, 128 r + 128) of A and half of the weight columns (gate/up: rank 0 the gate chunks,
+// rank 1 the up chunks; down: chunks 2 r, 2 r + 1), so each CTA's stage is 32 KB instead of 48
+// and seven stages fit. Rank 0's thread issues the MMAs (reading both CTAs' shared memory) and
+// commits to both CTAs' barriers; each CTA's epilogue reads its own 128 TMEM lanes (all 256
+// columns) exactly as in the single-CTA kernel, and both release the accumulator on rank 0.
+struct Cfg2 {
+  static constexpr int BN = 256;            // MMA N over the pair
+  static constexpr int kHalfChunks = 2;     // 64-column weight chunks staged per CTA
+  static constexpr int kStageBytes = kABytes + kHalfChunks * kChunkBytes;  // 32 KB
+  static constexpr int kStages = 7;  // 224 KB: the most that fits beside the barriers
+  static constexpr int kTmemCols = 2 * BN;  // two accumulators
+  static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+};
+
+template <int MODE, bool HF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm2_kernel(const __grid_constant__ CUtensorMap tmA_routed,
+                         const __grid_constant__ CUtensorMap tmA_shared,
+                         const __grid_constant__ CUtensorMap tmB0_routed,
+                         const __grid_constant__ CUtensorMap tmB1_routed,
+                         const __grid_constant__ CUtensorMap tmB0_shared,
+                         const __grid_constant__ CUtensorMap tmB1_shared, const GemmArgs a) {
+  using C = Cfg2;
+  constexpr int BN = C::BN;
+  constexpr int STAGES = C::kStages;
+  constexpr uint32_t IDESC =
+      ptx::idesc_f16kind_f32(2 * kBM, BN, 0, 1, (MODE == 1 && HF16) ? 0u : 1u);
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* const gbase = smem_raw + (base - raw);
+  const uint32_t bar0 = base + STAGES * C::kStageBytes;
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+  const uint32_t mma_done_bar = bar0 + 8u * (2 * STAGES + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + STAGES * C::kStageBytes +
+                                                    8 * (2 * STAGES + 5));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = ptx::cluster_rank();
+  const bool leader = rank == 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(full_bar(s), 1);   // rank 0's: one arrival + both CTAs' bytes
+      ptx::mbar_init(empty_bar(s), 1);  // one commit from rank 0's MMA thread
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(tfull_bar(b), 1);
+      ptx::mbar_init(tempty_bar(b), 8);  // rank 0's: four epilogue warps of each CTA
+    }
+    ptx::mbar_init(mma_done_bar, 1);
+    *abort_flag = 0;
+    ptx::fence_mbarrier_init();
+    ptx::prefetch_tmap(&tmA_routed);
+    ptx::prefetch_tmap(&tmB0_routed);
+    if (MODE == 0) ptx::prefetch_tmap(&tmB1_routed);
+  }
+  if (warp == 2) {
+    ptx::tmem_alloc_cg2(ptx::smem_u32(tmem_slot), C::kTmemCols);
+    ptx::tmem_relinquish_cg2();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  ptx::cluster_sync();  // both CTAs' barriers are initialised before any cross-CTA arrival
+  griddep_wait();       // everything above touched only shared memory, TMEM and parameters
+
+  const int n_mt = a.meta->n_tiles;
+  const long long total = (long long)n_mt * a.n_ntiles;
+  const long long pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- TMA producer (both)
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (long long w = pair; w < total && ok; w += n_pairs) {
+        TileEntry te;
+        int nt;
+        map_unit(w, a.n_ntiles, a.tiles, te, nt);
+        const bool shared = te.expert >= a.E;
+        const int ex = shared ? te.expert - a.E : te.expert;
+        const CUtensorMap* tA = shared ? &tmA_shared : &tmA_routed;
+        const CUtensorMap* tB =
+            MODE == 0 ? (rank == 0 ? (shared ? &tmB0_shared : &tmB0_routed)
+                                   : (shared ? &tmB1_shared : &tmB1_routed))
+                      : (shared ? &tmB0_shared : &tmB0_routed);
+        const int arow = ((MODE == 0) ? te.arow0 : te.row0) + kBM * (int)rank;
+        const int chunk0 = MODE == 0 ? nt * C::kHalfChunks : nt * 2 * C::kHalfChunks +
+                                                                 C::kHalfChunks * (int)rank;
+        for (int kb = 0; kb < a.k_blocks; ++kb) {
+          if (!ptx::mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, a.status,
+                                      MOE_DEVFAULT_PIPELINE_TIMEOUT, kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sA = base + stage * C::kStageBytes;
+          const uint32_t sB = sA + kABytes;
+          // completion is counted on rank 0's full barrier, which expects both CTAs' bytes
+          const uint32_t fb = leader ? full_bar(stage) : ptx::mapa_shared(full_bar(stage), 0);
+          if (leader) ptx::mbar_arrive_expect_tx(fb, 2 * C::kStageBytes);
+          ptx::tma_load_2d_cg2(sA, tA, fb, kb * kBK, arow);
+          ptx::tma_load_4d_cg2(sB, tB, fb, 0, kb * kBK, chunk0, ex);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ---------------------------------------------------------------- MMA issuer (rank 0)
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (long long w = pair; w < total && ok; w += n_pairs) {
+        if (!ptx::mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag, a.status,
+                                    MOE_DEVFAULT_PIPELINE_TIMEOUT, kWaitLimitNs))
+          break;
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        for (int kb = 0; kb < a.k_blocks; ++kb) {
+          if (!ptx::mbar_wait_bounded(full_bar(stage), phase, abort_flag, a.status,
+                                      MOE_DEVFAULT_PIPELINE_TIMEOUT, kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t sA = base + stage * C::kStageBytes;
+          const uint32_t sB = sA + kABytes;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint64_t adesc = ptx::smem_desc_sw128(sA + kk * 32, 16, 1024);
+            const uint64_t bdesc = ptx::smem_desc_sw128(sB + kk * 2048, kChunkBytes, 1024);
+            ptx::umma_f16_cg2(d_tmem, adesc, bdesc, IDESC, (kb | kk) != 0 ? 1u : 0u);
+          }
+          ptx::umma_commit_cg2(empty_bar(stage), 0x3);  // frees the stage in both CTAs
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        ptx::umma_commit_cg2(tfull_bar(acc), 0x3);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      // all MMAs issued by this thread have finished before TMEM is released
+      ptx::umma_commit_cg2(mma_done_bar, 0x1);
+      volatile int no_abort = 0;
+      ptx::mbar_wait_bounded(mma_done_bar, 0, &no_abort, a.status,
+                             MOE_DEVFAULT_PIPELINE_TIMEOUT, kWaitLimitNs / 4);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------------ epilogue (both)
+    const int q = warp - 4;  // TMEM lanes [32q, 32q + 32) of this CTA
+    const int row_in_tile = kBM * (int)rank + 32 * q + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (long long w = pair; w < total; w += n_pairs) {
+      TileEntry te;
+      int nt;
+      map_unit(w, a.n_ntiles, a.tiles, te, nt);
+      const bool valid = row_in_tile < te.rows;
+      const long long p = (long long)te.row0 + row_in_tile;
+      long long orow = p;
+      float gate = 1.0f;
+      if (MODE == 1 && valid && te.expert < a.E) {
+        const int slot = a.perm_slot[p];
+        orow = slot;
+        if (a.topk_w != nullptr) gate = a.topk_w[slot];
+      }
+      if (!ptx::mbar_wait_bounded(tfull_bar(acc), acc_phase, abort_flag, a.status,
+                                  MOE_DEVFAULT_PIPELINE_TIMEOUT, kWaitLimitNs))
+        break;
+      ptx::tc_fence_after();
+      const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN);
+      if (MODE == 0) {
+        uint16_t* dst = a.out + p * a.out_ld + (long long)nt * (BN / 2);
+#pragma unroll 1
+        for (int c = 0; c < BN / 2 / 32; ++c) {
+          uint32_t g[32], u[32];
+          ptx::tmem_ld_32x32b_x32(taddr + c * 32, g);
+          ptx::tmem_ld_32x32b_x32(taddr + BN / 2 + c * 32, u);
+          ptx::tmem_wait_ld();
+          uint32_t hv[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
+            const float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
+            const float h0 = g0 / (1.0f + __expf(-g0)) * u0;
+            const float h1 = g1 / (1.0f + __expf(-g1)) * u1;
+            hv[i] = HF16 ? pack_f16x2_sat(h0, h1) : pack_bf16x2(h0, h1);
+          }
+          if (valid) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              d4[i] = make_uint4(hv[4 * i], hv[4 * i + 1], hv[4 * i + 2], hv[4 * i + 3]);
+          }
+        }
+      } else {
+        uint16_t* dst = a.out + orow * a.out_ld + (long long)nt * BN;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t v[32];
+          ptx::tmem_ld_32x32b_x32(taddr + c * 32, v);
+          ptx::tmem_wait_ld();
+          uint32_t yv[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            yv[i] = pack_f16x2_sat(gate * __uint_as_float(v[2 * i]),
+                                   gate * __uint_as_float(v[2 * i + 1]));
+          if (valid) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              d4[i] = make_uint4(yv[4 * i], yv[4 * i + 1], yv[4 * i + 2], yv[4 * i + 3]);
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (leader)
+          ptx::mbar_arrive(tempty_bar(acc));
+        else
+          ptx::mbar_arrive_cluster(ptx::mapa_shared(tempty_bar(acc), 0));
+      }
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  // every copy into either CTA has landed and every MMA has finished once rank 0's MMA thread
+  // passed its final wait; neither CTA leaves (nor frees TMEM) before both get here
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync();
+  if (warp == 2) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc_cg2(tmem_base, C::kTmemCols);
+  }
+}
+
 // ------------------------------------------------------------------------------ host side
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn_impl() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = []() {
@@ -398,6 +663,31 @@ cudaError_t launch_one(const CUtensorMap (&maps)[6], const GemmArgs& args, cudaS
                   maps[2], maps[3], maps[4], maps[5], args);
 }
 
+template <int MODE, bool HF16>
+cudaError_t launch_two(const CUtensorMap (&maps)[6], const GemmArgs& args, cudaStream_t st) {
+  using C = Cfg2;
+  auto kern = grouped_gemm2_kernel<MODE, HF16>;
+  cudaError_t err =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (err != cudaSuccess) return err;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_sms() / 2 * 2);  // persistent: one CTA pair per two SMs
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5],
+                            args);
+}
+
 template <bool HF16>
 cudaError_t launch_pair(const Shape& s, const FfnPtrs& p, cudaStream_t st, cudaEvent_t ev_mid) {
   const long long rows = s.rows;
@@ -428,8 +718,12 @@ cudaError_t launch_pair(const Shape& s, const FfnPtrs& p, cudaStream_t st, cudaE
   g.k_blocks = s.d / kBK;
   g.out = p.h;
   g.out_ld = s.f;
+  const bool pairs = s.tile_m == 2 * kBM;  // 256-row tiles: the CTA-pair kernels
   cudaError_t err;
-  if (s.f % 128 == 0) {
+  if (pairs) {
+    g.n_ntiles = s.f / 128;
+    err = launch_two<0, HF16>(m0, g, st);
+  } else if (s.f % 128 == 0) {
     g.n_ntiles = s.f / 128;
     err = launch_one<0, 4, HF16>(m0, g, st);
   } else {
@@ -441,7 +735,8 @@ cudaError_t launch_pair(const Shape& s, const FfnPtrs& p, cudaStream_t st, cudaE
 
   // ---- down: A = H rows; B = W_down; epilogue scales by the gate and writes slot order (fp32)
   CUtensorMap m1[6];
-  const int dn_chunks = s.d % 256 == 0 ? 4 : (s.d % 128 == 0 ? 2 : 1);  // NCH of the down pass
+  // chunks per copy: a CTA of a pair stages half of the down pass's four
+  const int dn_chunks = pairs ? 2 : (s.d % 256 == 0 ? 4 : (s.d % 128 == 0 ? 2 : 1));
   ok = make_map_a(&m1[0], p.h, rows, s.f, kHType) &&
        make_map_b(&m1[2], Wd, s.E, s.f, s.d, dn_chunks, kHType);
   if (has_shared)
@@ -458,7 +753,10 @@ cudaError_t launch_pair(const Shape& s, const FfnPtrs& p, cudaStream_t st, cudaE
   g1.out_ld = s.d;
   g1.perm_slot = p.perm_slot;
   g1.topk_w = p.topk_w;
-  if (s.d % 256 == 0) {
+  if (pairs) {
+    g1.n_ntiles = s.d / 256;
+    return launch_two<1, HF16>(m1, g1, st);
+  } else if (s.d % 256 == 0) {
     g1.n_ntiles = s.d / 256;
     return launch_one<1, 4, HF16>(m1, g1, st);
   } else if (s.d % 128 == 0) {

@@ -60,7 +60,12 @@ Shape make_shape(const moe_config& c) {
   s.C = (int)C;
   s.reroute = c.overflow_reroute != 0 && s.C != INT_MAX;
   s.n_pblk = (int)((s.TK + kPermuteBlock - 1) / kPermuteBlock);
-  s.tile_m = c.weight_bits != 0 ? kQTileM : kTileM;
+  // Row tiles: 8 rows for quantized experts; 256 rows (CTA-pair GEMMs) when the expert segments
+  // are long enough for the pair's M = 256 MMA to pay for its padding (about T*k/E >= 320
+  // rows per expert) and the shape fits its 256-column tiles; else 128.
+  const bool pairs = c.weight_bits == 0 && c.d_ff % 128 == 0 && c.d % 256 == 0 &&
+                     (long long)c.T * c.top_k >= 320LL * c.E;
+  s.tile_m = c.weight_bits != 0 ? kQTileM : (pairs ? 2 * kTileM : kTileM);
   s.max_tiles = (int)((s.TK + s.tile_m - 1) / s.tile_m + s.E +
                       (long long)s.S * ((s.T + s.tile_m - 1) / s.tile_m));
   return s;

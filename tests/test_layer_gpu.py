@@ -21,6 +21,10 @@ SMALL = [
     dict(T=200, d=128, E=256, k=8, f=64),
     dict(T=1024, d=256, E=64, k=6, f=128, S=2, mode=W.BIAS_SELECT, bias="normal", bias_var=0.1,
          n_groups=8, topk_groups=3, capacity_factor=1.0),
+    # long expert segments (T*k >= 320 E): 256-row tiles on CTA pairs, odd tile counts included
+    dict(T=1024, d=256, E=4, k=2, f=256, S=1),
+    dict(T=700, d=512, E=4, k=2, f=384, mode=W.BIAS_SELECT, bias="normal", bias_var=0.1),
+    dict(T=1500, d=256, E=8, k=3, f=128, S=2, mode=W.GUMBEL, tau=0.5),
 ]
 
 
