@@ -36,7 +36,10 @@ L2_FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # DRAM bytes (read + write) per launch from one ncu capture of the current kernel, by
 # (workload, phase): profiles/grouped_gemm_fine_grained.md. Re-capture after changing the kernel.
-NCU_TRAFFIC = {}  # (workload, phase) -> DRAM bytes read + written per launch, from ncu
+# (workload, phase) -> DRAM bytes read + written per launch, from one ncu capture of the current
+# kernel (profiles/grouped_gemm_fine_grained.md)
+NCU_TRAFFIC = {("fine_grained", "gate_up_gemm"): (879.400448e6 + 67.677184e6),
+               ("fine_grained", "down_gemm"): (473.339648e6 + 95.139840e6)}
 
 
 def launches_per_step(cfg):
