@@ -153,7 +153,9 @@ def kernel_work(cfg, phase, n_touched, n_kept):
     if phase == "combine":
         return 0.0, (n_kept + S * T) * d * 2.0 + T * d * 2.0 + T * k * 4.0
     if phase == "tiles_gather":
-        return 0.0, 2.0 * n_kept * d * 2
+        # gathered rows written once; x read once from DRAM (repeat reads of a token's row hit
+        # L2)
+        return 0.0, n_kept * d * 2.0 + T * d * 2.0
     if phase == "dispatch":
         return 0.0, T * k * 4.0 * 4
     return 0.0, 0.0
