@@ -44,8 +44,8 @@ struct TileEntry {
 struct Meta {
   int n_tiles;        // row tiles written by the dispatch scan
   int n_kept;         // N = kept routed slots
-  int refine_count;   // near-tie tokens listed by the router (reset by the refine kernel)
-  int refine_done;    // refine CTAs finished (reset by the last one)
+  int refine_count;   // near-tie tokens listed by the router (reset by the router GEMM)
+  int unused0;
   int reroute_rounds; // proposal rounds of the last overflow re-route (diagnostic)
   int work[2];        // next work unit of the quantized gate/up and down passes
   int pad[57];
@@ -54,7 +54,7 @@ struct Meta {
 // Offsets of every buffer carved from the caller's workspace (bytes, 256-aligned).
 struct WsLayout {
   size_t status, meta, topk_idx, topk_w, counts, offsets, perm_slot, slot_pos;
-  size_t blk_hist, blk_base, tiles, wg_pad, wg_t, rpart, ncand, cand, rlist, xp, h, y, x_stage,
+  size_t blk_hist, blk_base, tiles, wg_pad, wg_t, rpart, rrec, xp, h, y, x_stage,
       u_stage, out_stage;
   // overflow re-route (zero-sized unless enabled)
   size_t sfull, maxl, pref, rr_tok, rr_exp, rr_bits, rr_ctl;
@@ -67,20 +67,20 @@ WsLayout ws_layout(const Shape& s);
 // ---- launchers (all asynchronous on `st`; return cudaGetLastError()) ----
 // Router scratch carved from the workspace.
 constexpr int kRouterMaxCand = 16;
+// One near-tie record, 128 bytes: [0] token, [1] candidate count (n > 0) or -1 (every expert),
+// [2, 2 + n) the candidate experts in index order (n <= kRouterMaxCand).
+constexpr int kRouterRecInts = 32;
 struct RouterScratch {
   uint16_t* wg_pad;  // d x round_up(E, 64) bf16, used when E is not a multiple of 64
   uint16_t* wg_t;    // E x d bf16: W_g transposed (exact near-tie pass)
   float* part;       // [splits, T, round_up(E, 64)] fp32 partial logits
-  int32_t* ncand;    // [T] near-tie candidate counts
-  int32_t* cand;     // [T, kRouterMaxCand] candidate experts
-  int32_t* rlist;    // [T] near-tie tokens
-  int* rcount;       // their number (zero between calls)
-  int* rdone;        // refine CTAs finished (zero between calls)
+  int32_t* rrec;     // [T][kRouterRecInts] near-tie records, appended by the selection
+  int* rcount;       // their number (cleared by the router GEMM at the start of each call)
   float* sfull;      // [T, E] selection scores kept for the overflow re-route, or nullptr
   float* maxl;       // [T] largest |logit| per token (with sfull)
 };
 // K slices of the router GEMM for T tokens and hidden size d.
-int router_splits(int T, int d);
+int router_splits(int T, int d, int E);
 cudaError_t launch_router(const Shape& s, const uint16_t* x, const uint16_t* W_g,
                           const float* bias, const float* u, int32_t* topk_idx, float* topk_w,
                           const RouterScratch& rs, int* status, cudaStream_t st);
@@ -181,6 +181,12 @@ int num_sms();
 // first), so launching it early (launch_k) is safe whatever precedes it.
 __device__ __forceinline__ void griddep_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Lets the next kernel on the stream (launched with programmatic stream serialization) start
+// once every CTA of this one has passed this point or exited.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // Launches `kernel` with programmatic stream serialization: it may begin while the previous

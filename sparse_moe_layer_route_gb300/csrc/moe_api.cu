@@ -92,10 +92,8 @@ WsLayout ws_layout(const Shape& s) {
   L.tiles = take(sizeof(TileEntry) * (size_t)s.max_tiles);
   L.wg_pad = take(2ull * s.d * ((s.E + 63) / 64 * 64));
   L.wg_t = take(2ull * s.d * s.E);
-  L.rpart = take(4ull * router_splits(s.T, s.d) * s.T * ((s.E + 63) / 64 * 64));
-  L.ncand = take(sizeof(int32_t) * (size_t)s.T);
-  L.cand = take(sizeof(int32_t) * (size_t)s.T * kRouterMaxCand);
-  L.rlist = take(sizeof(int32_t) * (size_t)s.T);
+  L.rpart = take(4ull * router_splits(s.T, s.d, s.E) * s.T * ((s.E + 63) / 64 * 64));
+  L.rrec = take(sizeof(int32_t) * (size_t)s.T * kRouterRecInts);
   L.xp = take(2ull * s.TK * s.d);
   L.h = take(2ull * s.rows * s.f);
   L.y = take(2ull * s.rows * s.d);
@@ -180,12 +178,9 @@ moe_status route_impl(const Shape& s, const WsLayout& L, void* ws, const uint16_
   rs.wg_pad = at<uint16_t>(ws, L.wg_pad);
   rs.wg_t = at<uint16_t>(ws, L.wg_t);
   rs.part = at<float>(ws, L.rpart);
-  rs.ncand = at<int32_t>(ws, L.ncand);
-  rs.cand = at<int32_t>(ws, L.cand);
-  rs.rlist = at<int32_t>(ws, L.rlist);
+  rs.rrec = at<int32_t>(ws, L.rrec);
   Meta* meta = at<Meta>(ws, L.meta);
   rs.rcount = &meta->refine_count;
-  rs.rdone = &meta->refine_done;
   rs.sfull = s.reroute ? at<float>(ws, L.sfull) : nullptr;
   rs.maxl = s.reroute ? at<float>(ws, L.maxl) : nullptr;
   return cuda_status(launch_router(s, x, W_g, bias, u, idx, w, rs, at<int>(ws, L.status), st));

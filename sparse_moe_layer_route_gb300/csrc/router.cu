@@ -57,7 +57,9 @@ template <int NCH>
 struct RCfg {
   static constexpr int EP = 64 * NCH;  // MMA N
   static constexpr int kStageBytes = kABytes + NCH * kChunkBytes;
-  static constexpr int kStages = (192 * 1024 / kStageBytes) > 8 ? 8 : (192 * 1024 / kStageBytes);
+  // E <= 64: four 24 KB stages, so that two CTAs share an SM; else as many as 192 KB hold (<= 8)
+  static constexpr int kStages =
+      NCH == 1 ? 4 : ((192 * 1024 / kStageBytes) > 8 ? 8 : (192 * 1024 / kStageBytes));
   static constexpr int kTmemCols = EP <= 64 ? 64 : (EP <= 128 ? 128 : 256);
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 256;
 };
@@ -67,7 +69,8 @@ template <int NCH>
 __global__ void __launch_bounds__(kThreads, 1)
     router_gemm_kernel(const __grid_constant__ CUtensorMap tmX,
                        const __grid_constant__ CUtensorMap tmW, float* __restrict__ part, int T,
-                       int kb_per_split, int k_blocks, int* status) {
+                       int kb_per_split, int k_blocks, int* status, int* rcount,
+                       int wait_at_end) {
   using C = RCfg<NCH>;
   constexpr int kStages = C::kStages;
   constexpr uint32_t IDESC = ptx::idesc_f16kind_f32(kBM, C::EP, 0, 1, 1);
@@ -113,7 +116,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  griddep_wait();  // the setup above touched only shared memory, TMEM and parameters
+  // The setup above touched only shared memory, TMEM and parameters. With wait_at_end, the
+  // preceding kernel (the weight transpose, whose output this kernel does not read) started this
+  // one after its own wait, so everything before it is complete: the wait moves to the end.
+  if (!wait_at_end) griddep_wait();
+  // the near-tie list of this call starts empty: the selection (the next kernel) appends to it
+  // and the previous call's refine pass, which read it, has completed
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *rcount = 0;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -208,6 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, C::kTmemCols);
   }
+  if (wait_at_end) griddep_wait();  // the weight transpose has completed too
 }
 
 struct SelectArgs {
@@ -216,10 +226,8 @@ struct SelectArgs {
   const float* u;
   int32_t* topk_idx;
   float* topk_w;
-  int32_t* ncand;     // [T]: 0 = decided; n > 0 = near-tie with n candidates; -1 = all E
-  int32_t* cand;      // [T, kMaxCand]
-  int32_t* rlist;     // near-tie tokens, appended
-  int* rcount;        // their number (reset to 0 by the refine kernel when it finishes)
+  int32_t* rrec;      // near-tie records, appended (layout: kRouterRecInts)
+  int* rcount;        // their number (cleared by the router GEMM before this kernel runs)
   float* sfull;       // [T, E] selection scores for the overflow re-route, or nullptr
   float* maxl_out;    // [T] largest |logit| of each row (with sfull)
   int T, E, EP, k, mode, d, splits;
@@ -227,9 +235,9 @@ struct SelectArgs {
   float tau;
 };
 
-constexpr int kSelRows = 32;              // tokens per selection CTA
-constexpr int kSelP = 8;                  // threads per token
-constexpr int kSelThreads = kSelRows * kSelP;
+constexpr int kSelWarps = 8;              // tokens per selection CTA: one warp each
+constexpr int kSelThreads = kSelWarps * 32;
+constexpr int kSelMaxPerLane = 8;         // experts per lane: E <= 256
 
 // Group-limited routing: group scores (largest member score), the Gk best groups (ties to the
 // lower group) as a bit mask, and the gap between the Gk-th and the next group score.
@@ -263,202 +271,180 @@ __device__ __forceinline__ unsigned long long pick_groups(const float* gm, int G
   return sel;
 }
 
+// Order-preserving 32-bit key of a selection score (NaN already mapped to -inf): a larger score
+// gives a larger key, -0 and +0 the same key, and every score a key above 0, which marks experts
+// that are taken or do not exist.
+__device__ __forceinline__ uint32_t score_key(float s) {
+  uint32_t b = __float_as_uint(s);
+  if (b == 0x80000000u) b = 0u;
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_score(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k ^ 0x80000000u) : ~k);
+}
+
+// One warp per token. Lane l holds experts [l*m, l*m + m) (m = ceil(E/32)): it sums their
+// partial logits over the K slices in slice order, forms their selection scores, and keeps their
+// keys. Each of the k+1 picks, in (score desc, index asc) order, is the warp's largest key, then
+// the smallest expert index among the lanes holding that key; the owner marks it taken.
 __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a) {
-  extern __shared__ __align__(16) float ssm[];
-  const int LD = a.EP + 4;  // rows stay 16-byte aligned; 128-bit reads of consecutive rows
-                            // hit distinct banks
-  float* scores = ssm;                                        // [32][LD]
-  float* maxl = scores + kSelRows * LD;                       // [32]
-  float* gmax = maxl + kSelRows;                              // [32][G]
-  unsigned long long* gsel =
-      reinterpret_cast<unsigned long long*>(gmax + kSelRows * (a.G > 0 ? a.G : 0));  // [32]
-  float* gmarg = reinterpret_cast<float*>(gsel + kSelRows);   // [32]
+  __shared__ uint32_t gkey[kSelWarps][64];  // group-limited routing: group maxima
+  __shared__ float gsc[kSelWarps][64];
   griddep_wait();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kSelWarps + warp;
+  if (t >= a.T) return;
   const bool gumbel = a.mode == MOE_ROUTE_GUMBEL;
-  const int t0 = blockIdx.x * kSelRows;
-  const int rows = min(kSelRows, a.T - t0);
-  // phase 1: the block's partial-logit tiles with coalesced 16-byte loads (every K slice of four
-  // groups in flight together), summed in slice order and turned into selection scores
-  int* maxl_bits = reinterpret_cast<int*>(maxl);  // |logit| >= 0: int order = float order
-  if (threadIdx.x < kSelRows) maxl_bits[threadIdx.x] = 0;
-  __syncthreads();
-  {
-    const int ep4 = a.EP / 4;
-    const float4* __restrict__ P = reinterpret_cast<const float4*>(a.part);
-#pragma unroll 4
-    for (int i = threadIdx.x; i < rows * ep4; i += kSelThreads) {
-      const int rr = i / ep4, c = (i - rr * ep4) * 4;
-      const int tt = t0 + rr;
-      float4 v[8];
+  const int m = (a.E + 31) >> 5;
+  const int e0 = lane * m;
+  float sc[kSelMaxPerLane];
+  uint32_t key[kSelMaxPerLane];
+  float maxabs = 0.f;
 #pragma unroll
-      for (int sp = 0; sp < 8; ++sp)
-        if (sp < a.splits) v[sp] = __ldg(P + ((size_t)sp * a.T + tt) * ep4 + c / 4);
-      float4 acc = v[0];
+  for (int i = 0; i < kSelMaxPerLane; ++i) {
+    sc[i] = -INFINITY;
+    key[i] = 0u;
+    const int e = e0 + i;
+    if (i < m && e < a.E) {
+      // at most 8 slices: every load issued before the sum, which runs in slice order
+      const float* p = a.part + (size_t)t * a.EP + e;
+      const size_t stride = (size_t)a.T * a.EP;
+      float v[8];
+#pragma unroll
+      for (int sp = 0; sp < 8; ++sp) v[sp] = sp < a.splits ? __ldg(p + sp * stride) : 0.f;
+      float l = v[0];
 #pragma unroll
       for (int sp = 1; sp < 8; ++sp)
-        if (sp < a.splits) {
-          acc.x += v[sp].x;
-          acc.y += v[sp].y;
-          acc.z += v[sp].z;
-          acc.w += v[sp].w;
-        }
-      const float lv[4] = {acc.x, acc.y, acc.z, acc.w};
-      float m = 0.f;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int e = c + q;
-        float sc = -INFINITY;
-        if (e < a.E) {
-          m = fmaxf(m, fabsf(lv[q]));
-          sc = selection_score(a.mode, lv[q],
-                               a.mode == MOE_ROUTE_BIAS_SELECT ? __ldg(a.bias + e) : 0.f,
-                               gumbel ? __ldg(a.u + (size_t)tt * a.E + e) : 0.f, a.tau);
-        }
-        scores[rr * LD + e] = sc;
-      }
-      atomicMax(&maxl_bits[rr], __float_as_int(m));
+        if (sp < a.splits) l += v[sp];
+      maxabs = fmaxf(maxabs, fabsf(l));
+      sc[i] = selection_score(a.mode, l, a.mode == MOE_ROUTE_BIAS_SELECT ? __ldg(a.bias + e) : 0.f,
+                              gumbel ? __ldg(a.u + (size_t)t * a.E + e) : 0.f, a.tau);
+      key[i] = score_key(sc[i]);
     }
   }
-  __syncthreads();
+  // |logit| >= 0: its bits order as the value
+  maxabs = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(maxabs)));
   if (a.sfull != nullptr) {
     // the overflow re-route ranks every expert of a token: keep the scores and the row scale
-    for (int i = threadIdx.x; i < rows * a.E; i += kSelThreads) {
-      const int rr = i / a.E, e = i - rr * a.E;
-      a.sfull[(size_t)(t0 + rr) * a.E + e] = scores[rr * LD + e];
-    }
-    if (threadIdx.x < rows) a.maxl_out[t0 + threadIdx.x] = maxl[threadIdx.x];
+#pragma unroll
+    for (int i = 0; i < kSelMaxPerLane; ++i)
+      if (i < m && e0 + i < a.E) a.sfull[(size_t)t * a.E + e0 + i] = sc[i];
+    if (lane == 0) a.maxl_out[t] = maxabs;
   }
-  const int r = threadIdx.x / kSelP, h = threadIdx.x % kSelP;
-  const int t = t0 + r;
-  const bool row_ok = r < rows;
-  float* srow = scores + r * LD;
-  const int chunk = ((a.E + kSelP - 1) / kSelP + 3) & ~3;  // multiple of 4: float4 reads
-  const int e_lo = h * chunk, e_hi = min(a.E, e_lo + chunk);
+  float gmarg = INFINITY;
   if (a.G > 0) {
-    // group-limited routing: experts outside the kept groups get -inf
+    // group-limited routing: experts outside the Gk best groups get -inf
     const int gsz = a.E / a.G;
-    if (row_ok)
-      for (int gi = h; gi < a.G; gi += kSelP) {
-        float m = -INFINITY;
-        for (int e = gi * gsz; e < (gi + 1) * gsz; ++e) m = fmaxf(m, srow[e]);
-        gmax[r * a.G + gi] = m;
-      }
-    __syncthreads();
-    if (row_ok && h == 0) gsel[r] = pick_groups(gmax + r * a.G, a.G, a.Gk, &gmarg[r]);
-    __syncthreads();
-    if (row_ok) {
-      const unsigned long long sel = gsel[r];
-      for (int e = e_lo; e < e_hi; ++e)
-        if (!((sel >> (e / gsz)) & 1ull)) srow[e] = -INFINITY;
-    }
+    for (int g = lane; g < a.G; g += 32) gkey[warp][g] = 0u;
     __syncwarp();
+#pragma unroll
+    for (int i = 0; i < kSelMaxPerLane; ++i)
+      if (i < m && e0 + i < a.E) atomicMax(&gkey[warp][(e0 + i) / gsz], key[i]);
+    __syncwarp();
+    for (int g = lane; g < a.G; g += 32) gsc[warp][g] = key_score(gkey[warp][g]);
+    __syncwarp();
+    unsigned long long sel = 0ull;
+    if (lane == 0) sel = pick_groups(gsc[warp], a.G, a.Gk, &gmarg);
+    sel = __shfl_sync(0xffffffffu, sel, 0);
+    gmarg = __shfl_sync(0xffffffffu, gmarg, 0);
+#pragma unroll
+    for (int i = 0; i < kSelMaxPerLane; ++i)
+      if (i < m && e0 + i < a.E && !((sel >> ((e0 + i) / gsz)) & 1ull)) {
+        sc[i] = -INFINITY;
+        key[i] = score_key(-INFINITY);
+      }
   }
+  // this lane's best remaining expert (lowest index among equal keys)
+  auto lane_best = [&](uint32_t& bk, int& be) {
+    bk = 0u;
+    be = INT_MAX;
+#pragma unroll
+    for (int i = 0; i < kSelMaxPerLane; ++i)
+      if (i < m && key[i] > bk) {
+        bk = key[i];
+        be = e0 + i;
+      }
+  };
+  uint32_t bk;
+  int be;
+  lane_best(bk, be);
   const int k = a.k;
   const int nl = k < a.E ? k + 1 : k;  // top-(k+1), or all E when k == E
-  // pass j: the best expert strictly after pick j-1 in (score desc, index asc) order; each of
-  // the token's 8 threads scans its experts, then a shuffle reduction over the 8 lanes
-  float pick_s[kList];
-  int pick_e[kList];
-  float ps = INFINITY;
-  int pe = -1;
+  float prev = 0.f, min_gap = INFINITY, sk = -INFINITY;
+  float my_s = 0.f;  // lane j < k: pick j
+  int my_e = 0;
 #pragma unroll
   for (int j = 0; j < kList; ++j) {
     if (j < nl) {
-      float bs[2] = {-INFINITY, -INFINITY};
-      int be[2] = {INT_MAX, INT_MAX};
-      if (row_ok) {
-        const float4* s4 = reinterpret_cast<const float4*>(srow);
-#pragma unroll 1
-        for (int e = e_lo; e < e_hi; e += 8) {
-          // may read up to 7 floats past this thread's range (still inside the row's padded
-          // storage or the next row); those lanes fail the ee < e_hi test below
-          const float4 v0 = s4[e >> 2], v1 = s4[(e >> 2) + 1];
-          const float vv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+      const uint32_t K = __reduce_max_sync(0xffffffffu, bk);
+      const int W = (int)__reduce_min_sync(0xffffffffu, bk == K ? (uint32_t)be : 0xffffffffu);
+      const float s_j = key_score(K);
+      if (lane == j) {
+        my_s = s_j;
+        my_e = W;
+      }
+      if (j > 0) min_gap = fminf(min_gap, prev - s_j);
+      if (j == k - 1) sk = s_j;
+      prev = s_j;
+      if (W >= e0 && W < e0 + m) {
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const int ee = e + q;
-            const float sc = vv[q];
-            const bool after = sc < ps || (sc == ps && ee > pe);
-            if (ee < e_hi && after && beats(sc, ee, bs[q & 1], be[q & 1])) {
-              bs[q & 1] = sc;
-              be[q & 1] = ee;
-            }
-          }
-        }
+        for (int i = 0; i < kSelMaxPerLane; ++i)
+          if (e0 + i == W) key[i] = 0u;
+        lane_best(bk, be);
       }
-      if (beats(bs[1], be[1], bs[0], be[0])) {
-        bs[0] = bs[1];
-        be[0] = be[1];
-      }
-#pragma unroll
-      for (int off = kSelP / 2; off > 0; off >>= 1) {
-        const float os = __shfl_xor_sync(0xffffffffu, bs[0], off);
-        const int oe = __shfl_xor_sync(0xffffffffu, be[0], off);
-        if (beats(os, oe, bs[0], be[0])) {
-          bs[0] = os;
-          be[0] = oe;
-        }
-      }
-      pick_s[j] = bs[0];
-      pick_e[j] = be[0];
-      ps = bs[0];
-      pe = be[0];
     }
   }
-  if (row_ok && h == 0) {
-    // near-tie test (scores in their own units: GUMBEL scores carry 1/tau)
-    float min_gap = INFINITY;
+  // near-tie test (scores in their own units: GUMBEL scores carry 1/tau)
+  float band = router_band(a.d, maxabs);
+  if (gumbel) band /= a.tau;
+  // a listed token gets a record: the token, then -1 (re-decide every expert) or its candidates,
+  // every expert scoring within the band of the k-th score, in index order
+  const bool group_tie = a.G > 0 && gmarg < band;
+  if (group_tie || min_gap < band) {
+    int mine = 0;
+    if (!group_tie) {
 #pragma unroll
-    for (int j = 1; j < kList; ++j)
-      if (j < nl) min_gap = fminf(min_gap, pick_s[j - 1] - pick_s[j]);
-    float sk = pick_s[0];
-#pragma unroll
-    for (int j = 0; j < kMaxK; ++j)
-      if (j == k - 1) sk = pick_s[j];
-    float band = router_band(a.d, maxl[r]);
-    if (gumbel) band /= a.tau;
-    int nc = 0;
-    if (a.G > 0 && gmarg[r] < band) {
-      nc = -1;  // the group decision itself is uncertain: recompute every expert exactly
-      a.rlist[atomicAdd(a.rcount, 1)] = t;
-    } else if (min_gap < band) {
-      // candidates: every expert scoring within the band of the k-th score
-      for (int e = 0; e < a.E; ++e) {
-        if (srow[e] >= sk - band) {
-          if (nc < kMaxCand) a.cand[(size_t)t * kMaxCand + nc] = e;
-          ++nc;
-        }
-      }
-      nc = nc <= kMaxCand ? nc : -1;
-      a.rlist[atomicAdd(a.rcount, 1)] = t;
+      for (int i = 0; i < kSelMaxPerLane; ++i)
+        if (i < m && e0 + i < a.E && sc[i] >= sk - band) ++mine;
     }
-    a.ncand[t] = nc;
-    {
-      // gates: softmax over the selected logits (PLAIN: the score; BIAS_SELECT: score - bias,
-      // within one rounding of the logit) or over the selected scores (GUMBEL)
-      float av[kMaxK];
-      float mx = -INFINITY;
+    int before = mine;
 #pragma unroll
-      for (int j = 0; j < kMaxK; ++j)
-        if (j < k) {
-          av[j] = a.mode == MOE_ROUTE_BIAS_SELECT ? pick_s[j] - a.bias[pick_e[j]] : pick_s[j];
-          mx = fmaxf(mx, av[j]);
-        }
-      float sum = 0.f;
-#pragma unroll
-      for (int j = 0; j < kMaxK; ++j)
-        if (j < k) {
-          av[j] = expf(av[j] - mx);
-          sum += av[j];
-        }
-      const float inv = 1.0f / sum;
-#pragma unroll
-      for (int j = 0; j < kMaxK; ++j)
-        if (j < k) {
-          a.topk_idx[(size_t)t * k + j] = pick_e[j];
-          a.topk_w[(size_t)t * k + j] = av[j] * inv;
-        }
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, before, off);
+      if (lane >= off) before += o;
     }
+    int nc = __shfl_sync(0xffffffffu, before, 31);
+    before -= mine;
+    nc = (!group_tie && nc <= kMaxCand) ? nc : -1;
+    int slot = 0;
+    if (lane == 0) slot = atomicAdd(a.rcount, 1);
+    int32_t* rec = a.rrec + (size_t)__shfl_sync(0xffffffffu, slot, 0) * kRouterRecInts;
+    if (lane == 0) {
+      rec[0] = t;
+      rec[1] = nc;
+    }
+    if (nc > 0) {
+#pragma unroll
+      for (int i = 0; i < kSelMaxPerLane; ++i)
+        if (i < m && e0 + i < a.E && sc[i] >= sk - band) rec[2 + before++] = e0 + i;
+    }
+  }
+  // gates: softmax over the selected logits (PLAIN: the score; BIAS_SELECT: score - bias,
+  // within one rounding of the logit) or over the selected scores (GUMBEL); lane j holds pick j
+  float av = -INFINITY;
+  if (lane < k) av = a.mode == MOE_ROUTE_BIAS_SELECT ? my_s - __ldg(a.bias + my_e) : my_s;
+  float mx = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < kMaxK; ++j)
+    if (j < k) mx = fmaxf(mx, __shfl_sync(0xffffffffu, av, j));
+  const float ex = lane < k ? expf(av - mx) : 0.f;
+  float sum = 0.f;
+#pragma unroll
+  for (int j = 0; j < kMaxK; ++j)
+    if (j < k) sum += __shfl_sync(0xffffffffu, ex, j);
+  if (lane < k) {
+    a.topk_idx[(size_t)t * k + lane] = my_e;
+    a.topk_w[(size_t)t * k + lane] = ex * (1.0f / sum);
   }
 }
 
@@ -472,6 +458,9 @@ __global__ void __launch_bounds__(kThreads) prep_router_kernel(const uint16_t* _
                                                                int E, int EP) {
   __shared__ uint16_t tile[32][33];
   griddep_wait();
+  // without a padded copy the router GEMM does not read this kernel's output: let it start now
+  // (it takes its wait at its end, so the selection and the refine pass still follow both)
+  if (Wp == nullptr) griddep_launch_dependents();
   const int j0 = blockIdx.x * 32, e0 = blockIdx.y * 32;
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
   for (int r = ty; r < 32; r += 8) {
@@ -494,8 +483,7 @@ __global__ void __launch_bounds__(kThreads) prep_router_kernel(const uint16_t* _
 // equal W_g columns give equal logits.
 __global__ void __launch_bounds__(kThreads) refine_kernel(
     const uint16_t* __restrict__ x, const uint16_t* __restrict__ WT, const float* __restrict__ bias,
-    const float* __restrict__ u, const int32_t* __restrict__ ncand,
-    const int32_t* __restrict__ cand, const int32_t* __restrict__ rlist, int* rcount, int* rdone,
+    const float* __restrict__ u, const int32_t* __restrict__ rrec, const int* rcount,
     int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, int T, int d, int E, int k,
     int mode, float tau, int G, int Gk) {
   __shared__ float red[kThreads / 32][kMaxCand];
@@ -503,18 +491,41 @@ __global__ void __launch_bounds__(kThreads) refine_kernel(
   __shared__ float cl[256], cs[256];
   griddep_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nf = *(volatile int*)rcount;
+  // the first record is read together with the count (a record past the count is never used)
+  int4 rv[(2 + kMaxCand) / 4 + 1];
+  auto load_rec = [&](int fi) {
+    const int4* rp = reinterpret_cast<const int4*>(rrec + (size_t)fi * kRouterRecInts);
+#pragma unroll
+    for (int i = 0; i < (2 + kMaxCand) / 4 + 1; ++i) rv[i] = rp[i];
+  };
+  if (blockIdx.x < T) load_rec(blockIdx.x);
+  const int nf = *rcount;
   for (int fi = blockIdx.x; fi < nf; fi += gridDim.x) {
-    const int t = rlist[fi];
-    const int n_c = ncand[t];
+    if (fi != (int)blockIdx.x) load_rec(fi);
+    const int* rec = reinterpret_cast<const int*>(rv);
+    const int t = rec[0];
+    const int n_c = rec[1];
     const int nc = n_c > 0 ? n_c : E;
-    for (int i = threadIdx.x; i < nc; i += kThreads)
-      ce[i] = n_c > 0 ? cand[(size_t)t * kMaxCand + i] : i;
-    __syncthreads();
     const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * d);
     const int d8 = d / 8;
     for (int c0 = 0; c0 < nc; c0 += kMaxCand) {
       const int cn = min(kMaxCand, nc - c0);
+      // this chunk's experts, read by every thread (the candidate list is 64 bytes)
+      // this chunk's experts (a listed chunk is the record's whole list: c0 = 0)
+      int ec[kMaxCand];
+#pragma unroll
+      for (int c = 0; c < kMaxCand; ++c) ec[c] = c < cn ? (n_c > 0 ? rec[2 + c] : c0 + c) : 0;
+      // warp 0's lane c < cn: its expert's bias / noise, loaded while the dot products run
+      float bias_c = 0.f, u_c = 0.f;
+      if (warp == 0 && lane < cn) {
+        int e = c0 + lane;
+#pragma unroll
+        for (int c = 0; c < kMaxCand; ++c)
+          if (c == lane) e = ec[c];
+        if (mode == MOE_ROUTE_BIAS_SELECT) bias_c = bias[e];
+        if (mode == MOE_ROUTE_GUMBEL) u_c = u[(size_t)t * E + e];
+        ce[c0 + lane] = e;
+      }
       float acc[kMaxCand];
 #pragma unroll
       for (int c = 0; c < kMaxCand; ++c) acc[c] = 0.f;
@@ -523,12 +534,14 @@ __global__ void __launch_bounds__(kThreads) refine_kernel(
       for (int g = threadIdx.x; g < d8; g += kThreads) {
         const uint4 xv = xr[g];
         const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+        uint4 wv[kMaxCand];
+#pragma unroll
+        for (int c = 0; c < kMaxCand; ++c)
+          if (c < cn) wv[c] = reinterpret_cast<const uint4*>(WT + (size_t)ec[c] * d)[g];
 #pragma unroll
         for (int c = 0; c < kMaxCand; ++c) {
           if (c < cn) {
-            const uint4 wv =
-                reinterpret_cast<const uint4*>(WT + (size_t)ce[c0 + c] * d)[g];
-            const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+            const uint32_t ww[4] = {wv[c].x, wv[c].y, wv[c].z, wv[c].w};
             float sacc = acc[c];
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
@@ -548,14 +561,11 @@ __global__ void __launch_bounds__(kThreads) refine_kernel(
         if (lane == 0) red[warp][c] = v;
       }
       __syncthreads();
-      if (threadIdx.x < cn) {
+      if (warp == 0 && lane < cn) {
         float l = 0.f;
-        for (int w = 0; w < kThreads / 32; ++w) l += red[w][threadIdx.x];
-        const int e = ce[c0 + threadIdx.x];
-        cl[c0 + threadIdx.x] = l;
-        cs[c0 + threadIdx.x] =
-            selection_score(mode, l, mode == MOE_ROUTE_BIAS_SELECT ? bias[e] : 0.f,
-                            mode == MOE_ROUTE_GUMBEL ? u[(size_t)t * E + e] : 0.f, tau);
+        for (int w = 0; w < kThreads / 32; ++w) l += red[w][lane];
+        cl[c0 + lane] = l;
+        cs[c0 + lane] = selection_score(mode, l, bias_c, u_c, tau);
       }
       __syncthreads();
     }
@@ -584,65 +594,90 @@ __global__ void __launch_bounds__(kThreads) refine_kernel(
       for (int e = 0; e < E; ++e)
         if (!((sel >> (e / gsz)) & 1ull)) cs[e] = -INFINITY;
     }
-    if (threadIdx.x == 0) {
-      // selection among the candidates by (score desc, index asc)
-      uint32_t used[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-      int esel[kMaxK];
-      float asel[kMaxK];
+    if (n_c < 0 && G > 0) __syncthreads();
+    if (warp == 0) {
+      // selection among the candidates by (score desc, index asc): lane l holds candidates
+      // l, l + 32, ...; each pick is the warp's largest key, then the smallest expert index
+      uint32_t key[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int c = lane + 32 * i;
+        key[i] = c < nc ? score_key(cs[c]) : 0u;
+      }
+      float my_a = 0.f;
+      int my_e = 0;
       for (int j = 0; j < k; ++j) {
-        int best = -1;
-        for (int i = 0; i < nc; ++i) {
-          if ((used[i >> 5] >> (i & 31)) & 1u) continue;
-          if (best < 0 || beats(cs[i], ce[i], cs[best], ce[best])) best = i;
+        uint32_t bk = 0u;
+        int be = INT_MAX, bi = -1;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int c = lane + 32 * i;
+          if (key[i] > bk || (key[i] == bk && key[i] != 0u && ce[c] < be)) {
+            bk = key[i];
+            be = ce[c];
+            bi = i;
+          }
         }
-        used[best >> 5] |= 1u << (best & 31);
-        esel[j] = ce[best];
-        asel[j] = (mode == MOE_ROUTE_GUMBEL) ? cs[best] : cl[best];
+        const uint32_t K = __reduce_max_sync(0xffffffffu, bk);
+        const int W = (int)__reduce_min_sync(0xffffffffu, bk == K ? (uint32_t)be : 0xffffffffu);
+        const bool mine = bk == K && be == W;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (mine && i == bi) key[i] = 0u;
+        // the pick's gate input: the logit, or the score for GUMBEL
+        const unsigned ow = __ballot_sync(0xffffffffu, mine);
+        const int src = __ffs(ow) - 1;
+        float av = 0.f;
+        if (mine) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            if (i == bi) av = mode == MOE_ROUTE_GUMBEL ? cs[lane + 32 * i] : cl[lane + 32 * i];
+        }
+        av = __shfl_sync(0xffffffffu, av, src);
+        if (lane == j) {
+          my_a = av;
+          my_e = W;
+        }
       }
-      float mx = asel[0];
-      for (int j = 1; j < k; ++j) mx = fmaxf(mx, asel[j]);
-      float ex[kMaxK], sum = 0.f;
-      for (int j = 0; j < k; ++j) {
-        ex[j] = expf(asel[j] - mx);
-        sum += ex[j];
-      }
-      const float inv = 1.0f / sum;
-      for (int j = 0; j < k; ++j) {
-        topk_idx[(size_t)t * k + j] = esel[j];
-        topk_w[(size_t)t * k + j] = ex[j] * inv;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j)
+        if (j < k) mx = fmaxf(mx, __shfl_sync(0xffffffffu, my_a, j));
+      const float ex = lane < k ? expf(my_a - mx) : 0.f;
+      float sum = 0.f;
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j)
+        if (j < k) sum += __shfl_sync(0xffffffffu, ex, j);
+      if (lane < k) {
+        topk_idx[(size_t)t * k + lane] = my_e;
+        topk_w[(size_t)t * k + lane] = ex * (1.0f / sum);
       }
     }
     __syncthreads();
-  }
-  // the last CTA to finish resets the list for the next call (all CTAs have read the count)
-  if (threadIdx.x == 0) {
-    __threadfence();
-    if (atomicAdd(rdone, 1) == (int)gridDim.x - 1) {
-      *rcount = 0;
-      *rdone = 0;
-    }
   }
 }
 
 template <int NCH>
 cudaError_t launch_gemm(const CUtensorMap& mx, const CUtensorMap& mw, float* part, int T,
                         int n_mt, int splits, int kb_per_split, int k_blocks, int* status,
-                        cudaStream_t st) {
+                        int* rcount, int wait_at_end, cudaStream_t st) {
   using C = RCfg<NCH>;
   cudaError_t err = cudaFuncSetAttribute(router_gemm_kernel<NCH>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmemBytes);
   if (err != cudaSuccess) return err;
   return launch_k(router_gemm_kernel<NCH>, dim3(n_mt, splits), dim3(kThreads), C::kSmemBytes, st,
-                  mx, mw, part, T, kb_per_split, k_blocks, status);
+                  mx, mw, part, T, kb_per_split, k_blocks, status, rcount, wait_at_end);
 }
 
 }  // namespace
 
-int router_splits(int T, int d) {
+int router_splits(int T, int d, int E) {
   const int n_mt = (T + kBM - 1) / kBM;
   const int k_blocks = d / kBK;
-  int sp = 152 / n_mt;  // fill the GPU's SMs with (row tile, K slice) CTAs
+  // fill the GPU's 152 SMs with (row tile, K slice) CTAs: two per SM when E <= 64 (their
+  // four-stage ring fits twice), else one
+  int sp = (E <= 64 ? 2 * 152 : 152) / n_mt;
   // at most 8 slices (the selection reads every slice) and at least 4 K blocks per slice
   const int cap = k_blocks / 4 < 8 ? (k_blocks / 4 > 1 ? k_blocks / 4 : 1) : 8;
   if (sp > cap) sp = cap;
@@ -667,14 +702,14 @@ cudaError_t launch_router(const Shape& s, const uint16_t* x, const uint16_t* W_g
     return cudaErrorInvalidValue;
   const int n_mt = (s.T + kBM - 1) / kBM;
   const int k_blocks = s.d / kBK;
-  const int splits = router_splits(s.T, s.d);
+  const int splits = router_splits(s.T, s.d, s.E);
   const int kbs = (k_blocks + splits - 1) / splits;
   cudaError_t err;
   switch (EP / 64) {
-    case 1: err = launch_gemm<1>(mx, mw, rs.part, s.T, n_mt, splits, kbs, k_blocks, status, st); break;
-    case 2: err = launch_gemm<2>(mx, mw, rs.part, s.T, n_mt, splits, kbs, k_blocks, status, st); break;
-    case 3: err = launch_gemm<3>(mx, mw, rs.part, s.T, n_mt, splits, kbs, k_blocks, status, st); break;
-    default: err = launch_gemm<4>(mx, mw, rs.part, s.T, n_mt, splits, kbs, k_blocks, status, st); break;
+    case 1: err = launch_gemm<1>(mx, mw, rs.part, s.T, n_mt, splits, kbs, k_blocks, status, rs.rcount, EP == s.E ? 1 : 0, st); break;
+    case 2: err = launch_gemm<2>(mx, mw, rs.part, s.T, n_mt, splits, kbs, k_blocks, status, rs.rcount, EP == s.E ? 1 : 0, st); break;
+    case 3: err = launch_gemm<3>(mx, mw, rs.part, s.T, n_mt, splits, kbs, k_blocks, status, rs.rcount, EP == s.E ? 1 : 0, st); break;
+    default: err = launch_gemm<4>(mx, mw, rs.part, s.T, n_mt, splits, kbs, k_blocks, status, rs.rcount, EP == s.E ? 1 : 0, st); break;
   }
   if (err != cudaSuccess) return err;
   SelectArgs a;
@@ -683,9 +718,7 @@ cudaError_t launch_router(const Shape& s, const uint16_t* x, const uint16_t* W_g
   a.u = u;
   a.topk_idx = topk_idx;
   a.topk_w = topk_w;
-  a.ncand = rs.ncand;
-  a.cand = rs.cand;
-  a.rlist = rs.rlist;
+  a.rrec = rs.rrec;
   a.rcount = rs.rcount;
   a.sfull = rs.sfull;
   a.maxl_out = rs.maxl;
@@ -699,19 +732,13 @@ cudaError_t launch_router(const Shape& s, const uint16_t* x, const uint16_t* W_g
   a.G = s.G;
   a.Gk = s.Gk;
   a.tau = s.tau;
-  const size_t smem =
-      sizeof(float) * ((size_t)kSelRows * (EP + 4) + kSelRows + (size_t)kSelRows * s.G +
-                       2 * kSelRows + kSelRows);
-  err = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem);
-  if (err != cudaSuccess) return err;
-  err = launch_k(select_kernel, dim3((s.T + kSelRows - 1) / kSelRows), dim3(kSelThreads), smem,
+  err = launch_k(select_kernel, dim3((s.T + kSelWarps - 1) / kSelWarps), dim3(kSelThreads), 0,
                  st, a);
   if (err != cudaSuccess) return err;
-  const int rgrid = 2 * num_sms();
+  const int rgrid = num_sms();  // one CTA per SM (its registers allow no second)
   return launch_k(refine_kernel, dim3(rgrid), dim3(kThreads), 0, st, x, (const uint16_t*)rs.wg_t,
-                  bias, u, (const int32_t*)rs.ncand, (const int32_t*)rs.cand,
-                  (const int32_t*)rs.rlist, rs.rcount, rs.rdone, topk_idx, topk_w, s.T, s.d, s.E,
+                  bias, u, (const int32_t*)rs.rrec, (const int*)rs.rcount, topk_idx, topk_w, s.T,
+                  s.d, s.E,
                   s.k, s.mode, s.tau, s.G, s.Gk);
 }
 
