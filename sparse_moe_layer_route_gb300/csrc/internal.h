@@ -80,7 +80,7 @@ struct RouterScratch {
   float* maxl;       // [T] largest |logit| per token (with sfull)
 };
 // K slices of the router GEMM for T tokens and hidden size d.
-int router_splits(int T, int d, int E);
+int router_splits(int T, int d);
 cudaError_t launch_router(const Shape& s, const uint16_t* x, const uint16_t* W_g,
                           const float* bias, const float* u, int32_t* topk_idx, float* topk_w,
                           const RouterScratch& rs, int* status, cudaStream_t st);

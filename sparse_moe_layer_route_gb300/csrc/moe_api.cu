@@ -92,7 +92,7 @@ WsLayout ws_layout(const Shape& s) {
   L.tiles = take(sizeof(TileEntry) * (size_t)s.max_tiles);
   L.wg_pad = take(2ull * s.d * ((s.E + 63) / 64 * 64));
   L.wg_t = take(2ull * s.d * s.E);
-  L.rpart = take(4ull * router_splits(s.T, s.d, s.E) * s.T * ((s.E + 63) / 64 * 64));
+  L.rpart = take(4ull * router_splits(s.T, s.d) * s.T * ((s.E + 63) / 64 * 64));
   L.rrec = take(sizeof(int32_t) * (size_t)s.T * kRouterRecInts);
   L.xp = take(2ull * s.TK * s.d);
   L.h = take(2ull * s.rows * s.f);

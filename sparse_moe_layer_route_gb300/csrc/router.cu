@@ -57,9 +57,7 @@ template <int NCH>
 struct RCfg {
   static constexpr int EP = 64 * NCH;  // MMA N
   static constexpr int kStageBytes = kABytes + NCH * kChunkBytes;
-  // E <= 64: four 24 KB stages, so that two CTAs share an SM; else as many as 192 KB hold (<= 8)
-  static constexpr int kStages =
-      NCH == 1 ? 4 : ((192 * 1024 / kStageBytes) > 8 ? 8 : (192 * 1024 / kStageBytes));
+  static constexpr int kStages = (192 * 1024 / kStageBytes) > 8 ? 8 : (192 * 1024 / kStageBytes);
   static constexpr int kTmemCols = EP <= 64 ? 64 : (EP <= 128 ? 128 : 256);
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 256;
 };
@@ -672,12 +670,10 @@ cudaError_t launch_gemm(const CUtensorMap& mx, const CUtensorMap& mw, float* par
 
 }  // namespace
 
-int router_splits(int T, int d, int E) {
+int router_splits(int T, int d) {
   const int n_mt = (T + kBM - 1) / kBM;
   const int k_blocks = d / kBK;
-  // fill the GPU's 152 SMs with (row tile, K slice) CTAs: two per SM when E <= 64 (their
-  // four-stage ring fits twice), else one
-  int sp = (E <= 64 ? 2 * 152 : 152) / n_mt;
+  int sp = 152 / n_mt;  // fill the GPU's SMs with (row tile, K slice) CTAs
   // at most 8 slices (the selection reads every slice) and at least 4 K blocks per slice
   const int cap = k_blocks / 4 < 8 ? (k_blocks / 4 > 1 ? k_blocks / 4 : 1) : 8;
   if (sp > cap) sp = cap;
@@ -702,7 +698,7 @@ cudaError_t launch_router(const Shape& s, const uint16_t* x, const uint16_t* W_g
     return cudaErrorInvalidValue;
   const int n_mt = (s.T + kBM - 1) / kBM;
   const int k_blocks = s.d / kBK;
-  const int splits = router_splits(s.T, s.d, s.E);
+  const int splits = router_splits(s.T, s.d);
   const int kbs = (k_blocks + splits - 1) / splits;
   cudaError_t err;
   switch (EP / 64) {
