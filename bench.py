@@ -44,12 +44,12 @@ NCU_TRAFFIC = {("fine_grained", "gate_up_gemm"): (879.400448e6 + 67.677184e6),
 
 def launches_per_step(cfg):
     """Kernels of one layer call: router (weight prep, GEMM, selection, exact near-tie pass),
-    dispatch (histogram, scan, scatter), tile list, gather, the two grouped GEMMs (or the
-    two quantized FFN passes) and the combine; the overflow re-route adds its three kernels and a
-    second dispatch."""
-    n = 12
+    dispatch (histogram with the scan and the tile list in its last CTA, scatter), gather, the two
+    grouped GEMMs (or the two quantized FFN passes) and the combine; the overflow re-route adds its
+    three kernels and a second dispatch."""
+    n = 10
     if getattr(cfg, "reroute", False) and cfg.capacity_factor > 0:
-        n += 3 + 3
+        n += 3 + 2
     return n
 
 

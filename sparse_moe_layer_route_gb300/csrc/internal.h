@@ -45,7 +45,7 @@ struct Meta {
   int n_tiles;        // row tiles written by the dispatch scan
   int n_kept;         // N = kept routed slots
   int refine_count;   // near-tie tokens listed by the router (reset by the router GEMM)
-  int unused0;
+  int dispatch_ticket; // dispatch histogram CTAs finished (reset by the last one)
   int reroute_rounds; // proposal rounds of the last overflow re-route (diagnostic)
   int work[2];        // next work unit of the quantized gate/up and down passes
   int pad[57];
@@ -114,20 +114,24 @@ struct RerouteArgs {
 };
 cudaError_t launch_reroute(const RerouteArgs& a, cudaStream_t st);
 
+// Dispatch: histogram (its last CTA also scans, and builds the row-tile list into tiles/meta
+// unless tiles is nullptr), then the stable scatter. *ticket is zero before and after.
 cudaError_t launch_permute(const Shape& s, const int32_t* topk_idx, int32_t* counts,
                            int32_t* offsets, int32_t* perm_slot, int32_t* slot_pos,
-                           int32_t* blk_hist, int32_t* blk_base, int* status, cudaStream_t st);
+                           int32_t* blk_hist, int32_t* blk_base, int* ticket, int* status,
+                           TileEntry* tiles, Meta* meta, cudaStream_t st);
 
 // moe_permute_noalloc: the same kernels with their scratch in a static device array.
 cudaError_t launch_permute_noalloc(const Shape& s, const int32_t* topk_idx, int32_t* counts,
                                    int32_t* offsets, int32_t* perm_slot, int32_t* slot_pos,
                                    int* fault_bits, cudaStream_t st);
 
-// Builds the row-tile list from offsets (routed) plus the shared experts' identity segments,
-// and gathers x rows into expert order (xp[p] = x[perm_slot[p] / k] for p < offsets[E]).
+// Builds the row-tile list from offsets (routed) plus the shared experts' identity segments
+// (unless the dispatch already did, tiles_built), and gathers x rows into expert order
+// (xp[p] = x[perm_slot[p] / k] for p < offsets[E]).
 cudaError_t launch_tiles_and_gather(const Shape& s, const uint16_t* x, const int32_t* perm_slot,
                                     const int32_t* offsets, uint16_t* xp, TileEntry* tiles,
-                                    Meta* meta, cudaStream_t st);
+                                    Meta* meta, bool tiles_built, cudaStream_t st);
 
 struct FfnPtrs {
   const uint16_t* x;

@@ -186,12 +186,16 @@ moe_status route_impl(const Shape& s, const WsLayout& L, void* ws, const uint16_
   return cuda_status(launch_router(s, x, W_g, bias, u, idx, w, rs, at<int>(ws, L.status), st));
 }
 
+// with_tiles: the FFN follows, so the dispatch also builds its row-tile list
 moe_status permute_impl(const Shape& s, const WsLayout& L, void* ws, const int32_t* idx,
                         int32_t* counts, int32_t* offsets, int32_t* perm_slot, int32_t* slot_pos,
-                        cudaStream_t st) {
+                        cudaStream_t st, bool with_tiles = false) {
+  Meta* meta = at<Meta>(ws, L.meta);
   return cuda_status(launch_permute(s, idx, counts, offsets, perm_slot, slot_pos,
                                     at<int32_t>(ws, L.blk_hist), at<int32_t>(ws, L.blk_base),
-                                    at<int>(ws, L.status), st));
+                                    &meta->dispatch_ticket, at<int>(ws, L.status),
+                                    with_tiles ? at<TileEntry>(ws, L.tiles) : nullptr,
+                                    with_tiles ? meta : nullptr, st));
 }
 
 moe_status reroute_impl(const Shape& s, const WsLayout& L, void* ws, const uint16_t* x,
@@ -243,10 +247,11 @@ moe_status ffn_impl(const Shape& s, const WsLayout& L, void* ws, const uint16_t*
                     const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wd,
                     const uint16_t* Wsg, const uint16_t* Wsu, const uint16_t* Wsd,
                     const uint16_t* Wd16, const uint16_t* Wsd16, uint16_t* y,
-                    cudaStream_t st, cudaEvent_t ev_gathered = nullptr,
+                    cudaStream_t st, bool tiles_built = false, cudaEvent_t ev_gathered = nullptr,
                     cudaEvent_t ev_gate_up = nullptr) {
   cudaError_t e = launch_tiles_and_gather(s, x, perm_slot, offsets, at<uint16_t>(ws, L.xp),
-                                          at<TileEntry>(ws, L.tiles), at<Meta>(ws, L.meta), st);
+                                          at<TileEntry>(ws, L.tiles), at<Meta>(ws, L.meta),
+                                          tiles_built, st);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   if (ev_gathered != nullptr && cudaEventRecord(ev_gathered, st) != cudaSuccess)
     return MOE_ERR_CUDA;
@@ -283,9 +288,11 @@ bool qweights_ok(const moe_config* c, const moe_qweights* q) {
 moe_status qffn_impl(const Shape& s, int bits, const WsLayout& L, void* ws, const uint16_t* x,
                      const int32_t* perm_slot, const int32_t* offsets, const float* topk_w,
                      const moe_qweights* qw, uint16_t* y, cudaStream_t st,
-                     cudaEvent_t ev_gathered = nullptr, cudaEvent_t ev_gate_up = nullptr) {
+                     bool tiles_built = false, cudaEvent_t ev_gathered = nullptr,
+                     cudaEvent_t ev_gate_up = nullptr) {
   cudaError_t e = launch_tiles_and_gather(s, x, perm_slot, offsets, at<uint16_t>(ws, L.xp),
-                                          at<TileEntry>(ws, L.tiles), at<Meta>(ws, L.meta), st);
+                                          at<TileEntry>(ws, L.tiles), at<Meta>(ws, L.meta),
+                                          tiles_built, st);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   if (ev_gathered != nullptr && cudaEventRecord(ev_gathered, st) != cudaSuccess)
     return MOE_ERR_CUDA;
@@ -333,25 +340,28 @@ moe_status layer_impl(const moe_config* cfg, const moe_weights* w, const uint16_
   if ((r = route_impl(s, L, ws, x, w->W_g, w->expert_bias, gumbel_u, idx, gw, st)) != MOE_OK)
     return r;
   if (!mark(1)) return MOE_ERR_CUDA;
-  if ((r = permute_impl(s, L, ws, idx, counts, offsets, perm_slot, slot_pos, st)) != MOE_OK)
+  // the last dispatch also builds the FFN's row-tile list
+  if ((r = permute_impl(s, L, ws, idx, counts, offsets, perm_slot, slot_pos, st,
+                        !s.reroute)) != MOE_OK)
     return r;
   if (s.reroute) {
     // Level 2: dropped slots move to the best expert with room, then the final dispatch
     if ((r = reroute_impl(s, L, ws, x, w->expert_bias, gumbel_u, idx, gw, counts, slot_pos,
                           st)) != MOE_OK)
       return r;
-    if ((r = permute_impl(s, L, ws, idx, counts, offsets, perm_slot, slot_pos, st)) != MOE_OK)
+    if ((r = permute_impl(s, L, ws, idx, counts, offsets, perm_slot, slot_pos, st, true)) !=
+        MOE_OK)
       return r;
   }
   if (!mark(2)) return MOE_ERR_CUDA;
   uint16_t* y = at<uint16_t>(ws, L.y);
   if (quant)
-    r = qffn_impl(s, cfg->weight_bits, L, ws, x, perm_slot, offsets, gw, w->quant, y, st,
+    r = qffn_impl(s, cfg->weight_bits, L, ws, x, perm_slot, offsets, gw, w->quant, y, st, true,
                   ev ? ev[3] : nullptr, ev ? ev[4] : nullptr);
   else
     r = ffn_impl(s, L, ws, x, perm_slot, offsets, gw, w->W_gate, w->W_up, w->W_down,
                  w->Wsh_gate, w->Wsh_up, w->Wsh_down, w->W_down_f16, w->Wsh_down_f16, y, st,
-                 ev ? ev[3] : nullptr, ev ? ev[4] : nullptr);
+                 true, ev ? ev[3] : nullptr, ev ? ev[4] : nullptr);
   if (r != MOE_OK) return r;
   if (!mark(5)) return MOE_ERR_CUDA;
   if ((r = cuda_status(launch_combine(s, y, slot_pos, out, st))) != MOE_OK) return r;

@@ -19,13 +19,85 @@ constexpr int kThreads = 256;
 constexpr int kSlotsPerThread = kPermuteBlock / kThreads;  // 4
 constexpr int kMaxE = 256;
 
-// Per-block expert histogram of kPermuteBlock consecutive slots.
+// Row-tile list of the grouped GEMMs: routed experts' segments cut into tile_m-row tiles, then
+// each shared expert's identity segment over all T tokens. Thread e < E holds expert e's
+// segment [o0, o0 + kept); n_kept is the sum of kept over all experts. Called by every thread of
+// one CTA of kThreads threads.
+__device__ void build_tiles(int o0, int kept, int n_kept, int E, int S, int T, long long TK,
+                            int tile_m, TileEntry* __restrict__ tiles, Meta* meta,
+                            int* warp_tot) {
+  const int e = threadIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nt = (kept + tile_m - 1) / tile_m;
+  int v = nt;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, v, off);
+    if (lane >= off) v += n;
+  }
+  __syncthreads();  // warp_tot may still be read by the caller's previous scan
+  if (lane == 31) warp_tot[warp] = v;
+  __syncthreads();
+  int wbase = 0, total = 0;
+  for (int w = 0; w < kThreads / 32; ++w) {
+    if (w < warp) wbase += warp_tot[w];
+    total += warp_tot[w];
+  }
+  const int start = wbase + v - nt;
+  for (int i = 0; i < nt; ++i) {
+    TileEntry te;
+    te.expert = e;
+    te.row0 = o0 + i * tile_m;
+    te.rows = min(tile_m, kept - i * tile_m);
+    te.arow0 = te.row0;
+    te.g0 = start;
+    te.gn = nt;
+    tiles[start + i] = te;
+  }
+  const int per_shared = (T + tile_m - 1) / tile_m;
+  for (int i = threadIdx.x; i < S * per_shared; i += kThreads) {
+    const int s = i / per_shared, m = i % per_shared;
+    TileEntry te;
+    te.expert = E + s;
+    te.row0 = (int)(TK + (long long)s * T + (long long)m * tile_m);
+    te.rows = min(tile_m, T - m * tile_m);
+    te.arow0 = m * tile_m;
+    te.g0 = total + s * per_shared;
+    te.gn = per_shared;
+    tiles[total + i] = te;
+  }
+  if (threadIdx.x == 0) {
+    meta->n_tiles = total + S * per_shared;
+    meta->n_kept = n_kept;
+    meta->work[0] = 0;  // work counters of the quantized FFN passes
+    meta->work[1] = 0;
+  }
+}
+
+// The tile list the last dispatch CTA builds as well (tiles == nullptr: none).
+struct TileJob {
+  TileEntry* tiles;
+  Meta* meta;
+  int S, T, tile_m;
+};
+
+// Per-block expert histogram of kPermuteBlock consecutive slots. The last CTA to finish (a ticket
+// counter, which it resets for the next call) then takes the per-expert running sums over the
+// blocks (blk_base), the counts, the capacity clamp and the exclusive scan of kept counts
+// (offsets), and, when asked, the row-tile list.
 __global__ void __launch_bounds__(kThreads) hist_kernel(const int32_t* __restrict__ topk_idx,
-                                                        long long TK, int E,
+                                                        long long TK, int E, int C,
                                                         int32_t* __restrict__ blk_hist,
-                                                        int* status) {
-  griddep_wait();
+                                                        int32_t* __restrict__ blk_base,
+                                                        int32_t* __restrict__ counts,
+                                                        int32_t* __restrict__ offsets,
+                                                        int* ticket, int* status, TileJob tj) {
+  constexpr int kBatchInts = 8192;  // 32 KB staging of blk_hist rows
   __shared__ int h[kMaxE];
+  __shared__ int stage[kBatchInts];
+  __shared__ int warp_tot[kThreads / 32];
+  __shared__ int is_last;
+  griddep_wait();
   for (int e = threadIdx.x; e < E; e += kThreads) h[e] = 0;
   __syncthreads();
   const long long base = (long long)blockIdx.x * kPermuteBlock;
@@ -45,26 +117,22 @@ __global__ void __launch_bounds__(kThreads) hist_kernel(const int32_t* __restric
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += kThreads)
     blk_hist[(size_t)blockIdx.x * E + e] = h[e];
-}
-
-// Single block: per-expert running sums over the dispatch blocks (blk_base), counts, the
-// capacity clamp and the exclusive scan of kept counts (offsets).
-__global__ void __launch_bounds__(kThreads) scan_kernel(const int32_t* __restrict__ blk_hist,
-                                                        int n_blk, int E, int C,
-                                                        int32_t* __restrict__ blk_base,
-                                                        int32_t* __restrict__ counts,
-                                                        int32_t* __restrict__ offsets) {
-  constexpr int kBatchInts = 8192;  // 32 KB staging of blk_hist rows
-  __shared__ int stage[kBatchInts];
-  __shared__ int warp_tot[kThreads / 32];
-  griddep_wait();
+  // publish this block's row, then take a ticket; the last block sees every row
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) is_last = atomicAdd(ticket, 1) == (int)gridDim.x - 1;
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  const int n_blk = gridDim.x;
   const int e = threadIdx.x;
   const int rows_per_batch = kBatchInts / E;
   int run = 0;
   for (int b0 = 0; b0 < n_blk; b0 += rows_per_batch) {
     const int nb = min(rows_per_batch, n_blk - b0);
     __syncthreads();
-    for (int i = threadIdx.x; i < nb * E; i += kThreads) stage[i] = blk_hist[(size_t)b0 * E + i];
+    for (int i = threadIdx.x; i < nb * E; i += kThreads)
+      stage[i] = __ldcg(blk_hist + (size_t)b0 * E + i);
     __syncthreads();
     if (e < E) {
       for (int b = 0; b < nb; ++b) {
@@ -88,13 +156,20 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(const int32_t* __restric
   }
   if (lane == 31) warp_tot[warp] = v;
   __syncthreads();
-  int wbase = 0;
-  for (int w = 0; w < warp; ++w) wbase += warp_tot[w];
+  int wbase = 0, n_kept = 0;
+  for (int w = 0; w < kThreads / 32; ++w) {
+    if (w < warp) wbase += warp_tot[w];
+    n_kept += warp_tot[w];
+  }
   const int incl = wbase + v;
   if (e < E) {
     offsets[e] = incl - kept;
     if (e == E - 1) offsets[E] = incl;
   }
+  if (threadIdx.x == 0) *ticket = 0;  // every block has taken its ticket
+  if (tj.tiles != nullptr)
+    build_tiles(incl - kept, kept, n_kept, E, tj.S, tj.T, TK, tj.tile_m, tj.tiles, tj.meta,
+                warp_tot);
 }
 
 // Stable scatter: the rank of a slot inside its expert is (slots of that expert in earlier
@@ -161,8 +236,7 @@ __global__ void __launch_bounds__(kThreads) scatter_kernel(
   }
 }
 
-// Row-tile list of the grouped GEMMs: routed experts' segments cut into kTileM-row tiles, then
-// each shared expert's identity segment over all T tokens.
+// The row-tile list from given expert offsets (the FFN entry point without a dispatch).
 __global__ void __launch_bounds__(kThreads) tiles_kernel(const int32_t* __restrict__ offsets,
                                                          int E, int S, int T, long long TK,
                                                          int tile_m,
@@ -171,55 +245,12 @@ __global__ void __launch_bounds__(kThreads) tiles_kernel(const int32_t* __restri
   __shared__ int warp_tot[kThreads / 32];
   griddep_wait();
   const int e = threadIdx.x;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int o0 = 0, kept = 0;
   if (e < E) {
     o0 = offsets[e];
     kept = offsets[e + 1] - o0;
   }
-  const int nt = (kept + tile_m - 1) / tile_m;
-  int v = nt;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int n = __shfl_up_sync(0xffffffffu, v, off);
-    if (lane >= off) v += n;
-  }
-  if (lane == 31) warp_tot[warp] = v;
-  __syncthreads();
-  int wbase = 0, total = 0;
-  for (int w = 0; w < kThreads / 32; ++w) {
-    if (w < warp) wbase += warp_tot[w];
-    total += warp_tot[w];
-  }
-  const int start = wbase + v - nt;
-  for (int i = 0; i < nt; ++i) {
-    TileEntry te;
-    te.expert = e;
-    te.row0 = o0 + i * tile_m;
-    te.rows = min(tile_m, kept - i * tile_m);
-    te.arow0 = te.row0;
-    te.g0 = start;
-    te.gn = nt;
-    tiles[start + i] = te;
-  }
-  const int per_shared = (T + tile_m - 1) / tile_m;
-  for (int i = threadIdx.x; i < S * per_shared; i += kThreads) {
-    const int s = i / per_shared, m = i % per_shared;
-    TileEntry te;
-    te.expert = E + s;
-    te.row0 = (int)(TK + (long long)s * T + (long long)m * tile_m);
-    te.rows = min(tile_m, T - m * tile_m);
-    te.arow0 = m * tile_m;
-    te.g0 = total + s * per_shared;
-    te.gn = per_shared;
-    tiles[total + i] = te;
-  }
-  if (threadIdx.x == 0) {
-    meta->n_tiles = total + S * per_shared;
-    meta->n_kept = offsets[E];
-    meta->work[0] = 0;  // work counters of the quantized FFN passes
-    meta->work[1] = 0;
-  }
+  build_tiles(o0, kept, offsets[E], E, S, T, TK, tile_m, tiles, meta, warp_tot);
 }
 
 // xp[p, :] = x[perm_slot[p] / k, :] for p < N. One warp per row, 16-byte vectors.
@@ -255,12 +286,11 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const uint16_t* __rest
 
 cudaError_t launch_permute(const Shape& s, const int32_t* topk_idx, int32_t* counts,
                            int32_t* offsets, int32_t* perm_slot, int32_t* slot_pos,
-                           int32_t* blk_hist, int32_t* blk_base, int* status, cudaStream_t st) {
+                           int32_t* blk_hist, int32_t* blk_base, int* ticket, int* status,
+                           TileEntry* tiles, Meta* meta, cudaStream_t st) {
+  const TileJob tj{tiles, meta, s.S, s.T, s.tile_m};
   cudaError_t e = launch_k(hist_kernel, dim3(s.n_pblk), dim3(kThreads), 0, st, topk_idx, s.TK,
-                           s.E, blk_hist, status);
-  if (e == cudaSuccess)
-    e = launch_k(scan_kernel, dim3(1), dim3(kThreads), 0, st, (const int32_t*)blk_hist, s.n_pblk,
-                 s.E, s.C, blk_base, counts, offsets);
+                           s.E, s.C, blk_hist, blk_base, counts, offsets, ticket, status, tj);
   if (e == cudaSuccess)
     e = launch_k(scatter_kernel, dim3(s.n_pblk), dim3(kThreads), 0, st, topk_idx, s.TK, s.E, s.C,
                  (const int32_t*)blk_base, (const int32_t*)offsets, perm_slot, slot_pos);
@@ -269,8 +299,9 @@ cudaError_t launch_permute(const Shape& s, const int32_t* topk_idx, int32_t* cou
 
 // ---- allocation-free dispatch -----------------------------------------------------------
 // Scratch of moe_permute_noalloc for callers that cannot allocate: 64 ints (256 B) hold a status
-// word used when the caller passes no fault word, then the per-block histograms and the
-// per-block running sums, each up to (MOE_NOALLOC_MAX_SLOTS / kPermuteBlock) x 256 ints.
+// word used when the caller passes no fault word ([0]) and the dispatch's ticket counter ([1],
+// zero at load and after every dispatch), then the per-block histograms and the per-block
+// running sums, each up to (MOE_NOALLOC_MAX_SLOTS / kPermuteBlock) x 256 ints.
 namespace {
 constexpr int kNoallocBlocks = MOE_NOALLOC_MAX_SLOTS / kPermuteBlock;
 constexpr int kNoallocInts = 64 + 2 * kNoallocBlocks * kMaxE;
@@ -316,15 +347,17 @@ cudaError_t launch_permute_noalloc(const Shape& s, const int32_t* topk_idx, int3
   int32_t* blk_hist = scratch + 64;
   int32_t* blk_base = blk_hist + (size_t)kNoallocBlocks * kMaxE;
   return launch_permute(s, topk_idx, counts, offsets, perm_slot, slot_pos, blk_hist, blk_base,
-                        status, st);
+                        scratch + 1, status, nullptr, nullptr, st);
 }
 
 cudaError_t launch_tiles_and_gather(const Shape& s, const uint16_t* x, const int32_t* perm_slot,
                                     const int32_t* offsets, uint16_t* xp, TileEntry* tiles,
-                                    Meta* meta, cudaStream_t st) {
-  cudaError_t e = launch_k(tiles_kernel, dim3(1), dim3(kThreads), 0, st, offsets, s.E, s.S, s.T,
-                           s.TK, s.tile_m, tiles, meta);
-  if (e != cudaSuccess) return e;
+                                    Meta* meta, bool tiles_built, cudaStream_t st) {
+  if (!tiles_built) {
+    const cudaError_t e = launch_k(tiles_kernel, dim3(1), dim3(kThreads), 0, st, offsets, s.E, s.S,
+                                   s.T, s.TK, s.tile_m, tiles, meta);
+    if (e != cudaSuccess) return e;
+  }
   const long long rows_per_blk = kThreads / 32;
   const long long grid = (s.TK + rows_per_blk - 1) / rows_per_blk;
   return launch_k(gather_kernel, dim3((unsigned)grid), dim3(kThreads), 0, st, x, perm_slot,
