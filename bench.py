@@ -8,7 +8,9 @@ A step is one moe_layer_forward call over one batch of the workload (inputs resi
 Between timed steps a 256 MB buffer is written to flush L2. Each step is timed with CUDA events on
 the launching stream; the K steps are bracketed by a barrier and a device synchronize.
 `e2e` is the same metric through moe_layer_forward_host (pinned host x in, host out, copies in
-the timed region). `roofline` is for the step's dominant kernel, timed live with events recorded
+the timed region), run as a serving loop buffers it (calls rotate over three streams and three workspaces, so the
+other calls' copies overlap one call's compute; events around the whole loop);
+the one-call-at-a-time latency is reported beside it as `e2e.serial`. `roofline` is for the step's dominant kernel, timed live with events recorded
 between the layer's phases (moe_layer_forward_profiled). `cpu_baseline` times the fp64 CPU
 oracle on a bounded sample of the same workload. With N > 1 (torchrun) every rank runs an
 independent replica of the layer (the layer has no cross-token exchange): value = N*T / max time.
@@ -423,32 +425,81 @@ def main():
     # ---- the same step replayed from a CUDA graph (launch overhead removed; L2 still flushed)
     graph = graph_replay(step, flush, stream, min(args.steps, 200))
 
-    # ---- e2e: host buffers through moe_layer_forward_host
+    # ---- e2e: host buffers through moe_layer_forward_host (pinned x in, out back to the host,
+    # both copies inside every call). Two measurements:
+    #  * serial: one call at a time, L2 flushed before each, CUDA events around each call (latency);
+    #  * serving loop (the reported value): successive calls rotate over three streams and three
+    #    workspaces, as a server buffers its batches, so the other calls' copies run on the copy
+    #    engines while one call computes (a stream runs its copy-in, compute and copy-out in order,
+    #    so three keep the compute busy when the copies take up to its time each); events bracket the whole loop, so every step's
+    #    copies and compute are inside the timed region. It is used when the expert weights one
+    #    step streams are more than twice the L2 flush size (no flush needed); otherwise the
+    #    serial figure is reported. The same loop on device buffers is reported beside it.
     x_h = inp_host["x"].pin_memory()
     u_h = inp_host["u"].pin_memory() if inp_host.get("u") is not None else None
-    out_h = torch.empty((T, d), dtype=torch.bfloat16).pin_memory()
+    NBUF = 3
+    out_h = [torch.empty((T, d), dtype=torch.bfloat16).pin_memory() for _ in range(NBUF)]
+    ws2 = [ws] + [M.alloc_workspace(mc, dev) for _ in range(NBUF - 1)]
+    streams2 = [stream] + [torch.cuda.Stream(device=dev) for _ in range(NBUF - 1)]
     n_e2e = min(args.steps, 200)
     e_s = [torch.cuda.Event(enable_timing=True) for _ in range(n_e2e)]
     e_e = [torch.cuda.Event(enable_timing=True) for _ in range(n_e2e)]
     for i in range(3):
-        M.layer_forward_host(mc, weights, x_h, u_h, out_h, ws)
+        M.layer_forward_host(mc, weights, x_h, u_h, out_h[0], ws)
     torch.cuda.synchronize()
     for i in range(n_e2e):
         flush.fill_(i & 0xFF)
         e_s[i].record(stream)
-        M.layer_forward_host(mc, weights, x_h, u_h, out_h, ws)
+        M.layer_forward_host(mc, weights, x_h, u_h, out_h[0], ws)
         e_e[i].record(stream)
     torch.cuda.synchronize()
+    e2e_serial_ms = sum(a.elapsed_time(b) for a, b in zip(e_s, e_e)) / n_e2e
+    n_touched_now = touched_experts(counts.cpu().tolist(), M_capacity(cfg))[0]
+    streamed = (n_touched_now + cfg.S) * 3 * cfg.d * cfg.f * weight_bytes_per_element(cfg)
+    flush_each = streamed < 2 * L2_FLUSH_BYTES
+    for i in range(2 * NBUF):
+        M.layer_forward_host(mc, weights, x_h, u_h, out_h[i % NBUF], ws2[i % NBUF],
+                             stream=streams2[i % NBUF])
+    torch.cuda.synchronize()
+    out_d2 = [out] + [torch.empty_like(out) for _ in range(NBUF - 1)]
+    ro2 = [ro] + [M.make_route_out() for _ in range(NBUF - 1)]
+
+    def serving_loop(host):
+        """Per-step ms of n_e2e calls rotating over the streams and workspaces."""
+        p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        p0.record(stream)
+        for st_b in streams2[1:]:
+            st_b.wait_event(p0)
+        for i in range(n_e2e):
+            j = i % NBUF
+            if host:
+                M.layer_forward_host(mc, weights, x_h, u_h, out_h[j], ws2[j], stream=streams2[j])
+            else:
+                M.layer_forward(mc, weights, inp["x"], u, out_d2[j], ro2[j], ws2[j],
+                                stream=streams2[j])
+        for st_b in streams2[1:]:
+            stream.wait_stream(st_b)
+        p1.record(stream)
+        torch.cuda.synchronize()
+        return p0.elapsed_time(p1) / n_e2e
+
+    # with weights that fit L2 a flush would have to sit inside the loop: report the serial figure
+    loop_ms = serving_loop(True) if not flush_each else None
+    loop_dev_ms = serving_loop(False) if not flush_each else None
+    e2e_ms = loop_ms if loop_ms is not None else e2e_serial_ms
     clk = clocks.stop()
-    e2e_ms = sum(a.elapsed_time(b) for a, b in zip(e_s, e_e)) / n_e2e
-    faults = M.device_status(ws)
+    faults = 0
+    for w_ in ws2:
+        faults |= M.device_status(w_)
     if faults:
         raise SystemExit(f"device fault bits {faults:#x} during the timed region")
     h2d = T * d * 2 + (T * E * 4 if u_h is not None else 0)
     d2h = T * d * 2
 
     # ---- max over ranks (replicas: no data-path collective, only this timing reduction)
-    ms, e2e_ms = max_over_ranks([ms, e2e_ms], dist, dev)
+    ms, e2e_ms, e2e_serial_ms = max_over_ranks([ms, e2e_ms, e2e_serial_ms], dist, dev)
+    if loop_dev_ms is not None:
+        loop_dev_ms = max_over_ranks([loop_dev_ms], dist, dev)[0]
 
     counts_h = counts.cpu().tolist()
     C = M_capacity(cfg)
@@ -480,7 +531,23 @@ def main():
             "layer_roofline": lr,
             "kernels": kernels,
             "e2e": {"value": replica_throughput(world, T, e2e_ms), "unit": "tokens/s",
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                    "mode": ("serving loop: calls rotate over 3 streams and 3 workspaces; "
+                             "events around the whole loop; L2 not flushed: each step streams "
+                             "%.2f GB of expert weights" % (streamed / 1e9)
+                             if loop_ms is not None else
+                             "serial: one call at a time, L2 flushed before each, events around "
+                             "each call (the weights fit L2, so a loop would need the flush "
+                             "inside its window)"),
+                    "serial": {"value": replica_throughput(world, T, e2e_serial_ms),
+                               "ms_per_step": e2e_serial_ms,
+                               "mode": "one call at a time, L2 flushed before each, events around "
+                                       "each call"},
+                    "device_serving_loop": (None if loop_dev_ms is None else
+                                            {"value": replica_throughput(world, T, loop_dev_ms),
+                                             "ms_per_step": loop_dev_ms,
+                                             "mode": "the same loop through moe_layer_forward "
+                                                     "on device buffers (no copies)"})},
             "gpu_launches": launches_per_step(cfg) * args.steps,
             "clocks": clk,
             "routing": {"experts_hit": n_touched, "kept_slots": n_kept, "capacity": C,
