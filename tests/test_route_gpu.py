@@ -20,6 +20,10 @@ CASES = [  # T, d, E, k, mode, bias
     (200, 128, 256, 8, W.PLAIN, "zero"),
     (64, 192, 100, 5, W.GUMBEL, "zero"),
     (96, 128, 8, 8, W.BIAS_SELECT, "normal"),
+    # experts per lane of the selection warp: one lane of two (33), three (96), seven (200)
+    (333, 256, 33, 3, W.BIAS_SELECT, "normal"),
+    (250, 256, 96, 4, W.GUMBEL, "zero"),
+    (130, 192, 200, 7, W.BIAS_SELECT, "zipf"),
 ]
 
 
@@ -158,3 +162,24 @@ def test_group_near_ties_are_decided_exactly():
     assert (top_is_pair & ~exempt).sum() > 100     # many non-exempt group near-ties exercised
     diff = (idx != r["topk_idx"]).any(1)
     assert not (diff & ~exempt).any(), np.nonzero(diff & ~exempt)[0][:10]
+
+
+def test_route_zero_columns_tie_lowest_index():
+    """All-zero router columns give logits of exactly zero on both sides (every product is a
+    signed zero), so those experts tie at score 0 in PLAIN mode; the lower index must win, in the
+    oracle's order, wherever they reach the top-k."""
+    cfg = W.small_config(T=400, d=256, E=12, k=5, f=64, seed=5)
+    inp = W.make_routing_inputs(cfg)
+    Wg = inp["W_g"].clone()
+    for c in (2, 5, 6, 11):
+        Wg[:, c] = 0
+    inp["W_g"] = Wg
+    idx, w = run_route(cfg, inp)
+    r = oracle_for(cfg, inp)
+    s = -np.sort(-r["scores"], 1)[:, : cfg.k + 1]
+    gaps = s[:, :-1] - s[:, 1:]
+    inexact = ((gaps > 0) & (gaps < O.TIE_MARGIN)).any(1)   # inexact near-ties stay exempt
+    same = (idx == r["topk_idx"]).all(1)
+    assert (same | inexact).all(), np.nonzero(~(same | inexact))[0][:10]
+    zero_picked = np.isin(r["topk_idx"], (2, 5, 6, 11)).sum(1)
+    assert (zero_picked >= 2).sum() > 20       # zero-score ties were really decided
