@@ -13,11 +13,16 @@
 // Why this shape. At decode sizes an expert sees one or two rows, so the layer is bound by the
 // bytes of the weights it touches; the kernel streams each code once with 16-byte coalesced
 // loads (a warp reads 512 contiguous bytes per load) and the arithmetic per code has to stay
-// below the memory time. The codes become exact fp16 integers (q - z) in registers (a byte or
-// nibble placed into the mantissa of 1024.0, minus 1024 + z), feed mma.sync m16n8k16 as the A
-// operand straight from registers (weights as the M side, up to 8 tokens as N), and each 128-row
-// group's fp32 partial sums are multiplied by the group's scale in fp32, so every product and sum
-// is the one of the dequantized weights (q - z) * s. A tcgen05 MMA would need the dequantized
+// below the memory time. A code becomes an exact fp16 integer in one instruction: a byte, or a
+// nibble, placed into the mantissa of 1024.0 gives 1024 + q (a nibble that sits 4 bits up gives
+// 1024 + 16 q, and the rows stored that way take a scale 16 times smaller). These feed mma.sync
+// m16n8k16 as the A operand straight from registers (weights as the M side, up to 8 tokens as
+// N); every product is exact and the sums are fp32. Per 128-row group the constant is removed
+// once, (1024 + z) * sum(b) with sum(b) from one more MMA against an all-ones fragment, and the
+// group's fp32 scale applied: the result is the dequantized weights' (q - z) * s dot product up
+// to the fp32 rounding of the offset (about 1e-4 of it, far below the fp16 rows' rounding). The
+// zero-point subtraction thus leaves the per-code path, which at 4 bits was the limit (the
+// kernel issue-bound below the memory rate). A tcgen05 MMA would need the dequantized
 // tile in shared memory first: 2 more bytes written and read per weight on top of the code, more
 // shared-memory traffic than the SM has at the HBM rate of 1-byte codes.
 #include <cuda_fp16.h>
@@ -111,28 +116,23 @@ struct QArgs {
   int E, K, N;
 };
 
-__device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, uint32_t b) {
-  const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&a),
-                            *reinterpret_cast<const __half2*>(&b));
-  return *reinterpret_cast<const uint32_t*>(&r);
-}
-
-// A fragment (q - z as exact fp16) of one 16x16 step from its 8 codes.
+// A fragment of one 16x16 step from its 8 codes, as fp16 integers 1024 + q.
 // 8-bit: lo = codes j0..j3, hi = codes j4..j7 (one byte each).
-__device__ __forceinline__ void a_frag8(uint32_t lo, uint32_t hi, uint32_t z0, uint32_t z1,
-                                        uint32_t (&a)[4]) {
-  a[0] = hsub2_u32(__byte_perm(lo, 0x64646464u, 0x4140), z0);  // (j0, j1) row g
-  a[1] = hsub2_u32(__byte_perm(lo, 0x64646464u, 0x4342), z1);  // (j2, j3) row g + 8
-  a[2] = hsub2_u32(__byte_perm(hi, 0x64646464u, 0x4140), z0);  // (j4, j5) row g
-  a[3] = hsub2_u32(__byte_perm(hi, 0x64646464u, 0x4342), z1);  // (j6, j7) row g + 8
+__device__ __forceinline__ void a_frag8(uint32_t lo, uint32_t hi, uint32_t (&a)[4]) {
+  a[0] = __byte_perm(lo, 0x64646464u, 0x4140);  // (j0, j1) row g
+  a[1] = __byte_perm(lo, 0x64646464u, 0x4342);  // (j2, j3) row g + 8
+  a[2] = __byte_perm(hi, 0x64646464u, 0x4140);  // (j4, j5) row g
+  a[3] = __byte_perm(hi, 0x64646464u, 0x4342);  // (j6, j7) row g + 8
 }
 
-// 4-bit: one word; slot j at bit 16 * (j % 2) + 4 * (j / 2).
-__device__ __forceinline__ void a_frag4(uint32_t w, uint32_t z0, uint32_t z1, uint32_t (&a)[4]) {
-  a[0] = hsub2_u32((w & 0x000F000Fu) | 0x64006400u, z0);
-  a[1] = hsub2_u32(((w >> 4) & 0x000F000Fu) | 0x64006400u, z1);
-  a[2] = hsub2_u32(((w >> 8) & 0x000F000Fu) | 0x64006400u, z0);
-  a[3] = hsub2_u32(((w >> 12) & 0x000F000Fu) | 0x64006400u, z1);
+// 4-bit: one word; slot j at bit 16 * (j % 2) + 4 * (j / 2). Rows g + 8 (slots 2, 3, 6, 7) sit
+// at bits 4-7 of their byte and stay there: 1024 + 16 q, undone by their scale (1/16).
+__device__ __forceinline__ void a_frag4(uint32_t w, uint32_t (&a)[4]) {
+  const uint32_t w8 = w >> 8;
+  a[0] = (w & 0x000F000Fu) | 0x64006400u;   // row g:     1024 + q
+  a[1] = (w & 0x00F000F0u) | 0x64006400u;   // row g + 8: 1024 + 16 q
+  a[2] = (w8 & 0x000F000Fu) | 0x64006400u;  // row g
+  a[3] = (w8 & 0x00F000F0u) | 0x64006400u;  // row g + 8
 }
 
 __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
@@ -183,15 +183,16 @@ __device__ __forceinline__ void issue_group(uint32_t ring, int stage, const QMat
                    mats[m].q + ((tile0 + t) * KP + (size_t)grp * NL + l) * 512 + lane * 16);
 }
 
-// Scale (fp32) and zero-point (fp16 1024 + z, doubled) of this lane's two rows n, n + 8 of
-// every tile in one group, for every matrix of the unit.
+// Per group, for this lane's two rows n, n + 8 of every tile and every matrix of the unit: the
+// scale (fp32) and the constant the MMA's A values carry, 1024 + z; for 4-bit rows n + 8, whose
+// values are 1024 + 16 q, the scale / 16 and 1024 + 16 z (both exact).
 template <int NM, int TL>
 struct GroupQ {
   float sc[NM][TL][2];
-  uint32_t zz[NM][TL][2];
+  float off[NM][TL][2];
 };
 
-template <int NM, int TL>
+template <int BITS, int NM, int TL>
 __device__ __forceinline__ void load_group_q(GroupQ<NM, TL>& q, const QMat* mats, int ex_ix,
                                              int grp, int groups, int N, int n, bool ok) {
 #pragma unroll
@@ -201,9 +202,11 @@ __device__ __forceinline__ void load_group_q(GroupQ<NM, TL>& q, const QMat* mats
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const size_t ix = ((size_t)ex_ix * groups + (ok ? grp : 0)) * N + n + 16 * t + 8 * h;
-        q.sc[m][t][h] = __half2float(__ushort_as_half(mats[m].s[ix]));
-        const uint32_t zh = 0x6400u | mats[m].z[ix];
-        q.zz[m][t][h] = zh | (zh << 16);
+        const float sc = __half2float(__ushort_as_half(mats[m].s[ix]));
+        const float z = (float)mats[m].z[ix];
+        const bool up = BITS == 4 && h == 1;
+        q.sc[m][t][h] = up ? sc * 0.0625f : sc;
+        q.off[m][t][h] = up ? 1024.f + 16.f * z : 1024.f + z;
       }
 }
 
@@ -213,12 +216,14 @@ __device__ __forceinline__ void compute_group(const uint4 (&code)[NM][TL][NL],
                                               const GroupQ<NM, TL>& q,
                                               float (&acc)[NM][TL][4]) {
   float cg[NM][TL][4];
+  float sb[4] = {0.f, 0.f, 0.f, 0.f};  // sum of the group's activations per token (2c, 2c + 1)
 #pragma unroll
   for (int m = 0; m < NM; ++m)
 #pragma unroll
     for (int t = 0; t < TL; ++t)
 #pragma unroll
       for (int i = 0; i < 4; ++i) cg[m][t][i] = 0.f;
+  const uint32_t ones[4] = {0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u};  // fp16 1.0
 #pragma unroll
   for (int st = 0; st < 8; ++st) {
     uint32_t b0 = bq[st][0], b1 = bq[st][1];
@@ -226,6 +231,7 @@ __device__ __forceinline__ void compute_group(const uint4 (&code)[NM][TL][NL],
       b0 = bf16x2_to_f16x2(b0);
       b1 = bf16x2_to_f16x2(b1);
     }
+    mma16816(sb, ones, b0, b1);
 #pragma unroll
     for (int m = 0; m < NM; ++m)
 #pragma unroll
@@ -234,25 +240,26 @@ __device__ __forceinline__ void compute_group(const uint4 (&code)[NM][TL][NL],
         if (BITS == 8) {
           const uint4 v = code[m][t][st / 2];
           const uint32_t lo = (st & 1) ? v.z : v.x, hi = (st & 1) ? v.w : v.y;
-          a_frag8(lo, hi, q.zz[m][t][0], q.zz[m][t][1], af);
+          a_frag8(lo, hi, af);
         } else {
           const uint4 v = code[m][t][st / 4];
           const int qq = st & 3;
-          a_frag4(qq == 0 ? v.x : qq == 1 ? v.y : qq == 2 ? v.z : v.w, q.zz[m][t][0],
-                  q.zz[m][t][1], af);
+          a_frag4(qq == 0 ? v.x : qq == 1 ? v.y : qq == 2 ? v.z : v.w, af);
         }
         mma16816(cg[m][t], af, b0, b1);
       }
   }
+  // element i: row n + 8 (i / 2) of the tile, token 2c + i % 2
 #pragma unroll
   for (int m = 0; m < NM; ++m)
 #pragma unroll
-    for (int t = 0; t < TL; ++t) {
-      acc[m][t][0] = fmaf(q.sc[m][t][0], cg[m][t][0], acc[m][t][0]);
-      acc[m][t][1] = fmaf(q.sc[m][t][0], cg[m][t][1], acc[m][t][1]);
-      acc[m][t][2] = fmaf(q.sc[m][t][1], cg[m][t][2], acc[m][t][2]);
-      acc[m][t][3] = fmaf(q.sc[m][t][1], cg[m][t][3], acc[m][t][3]);
-    }
+    for (int t = 0; t < TL; ++t)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int h = i >> 1;
+        acc[m][t][i] = fmaf(q.sc[m][t][h], fmaf(-q.off[m][t][h], sb[i & 1], cg[m][t][i]),
+                            acc[m][t][i]);
+      }
 }
 
 // 16-column tiles per work unit: 4-bit groups carry half the bytes of 8-bit ones, so a 4-bit
@@ -333,7 +340,7 @@ __global__ void __launch_bounds__(kQThreads) qffn_kernel(const QArgs a) {
       bq[st][1] = tok_ok ? brow[(st * 16 + 2 * c + 8) / 2] : 0u;
     }
     GroupQ<NM, TL> gq;
-    load_group_q<NM, TL>(gq, mats, ex_ix, 0, groups, a.N, n, true);
+    load_group_q<BITS, NM, TL>(gq, mats, ex_ix, 0, groups, a.N, n, true);
     for (int grp = 0; grp < groups; ++grp) {
       const int ahead = grp + kStages - 1;
       if (ahead < groups)
@@ -359,7 +366,7 @@ __global__ void __launch_bounds__(kQThreads) qffn_kernel(const QArgs a) {
         bn[st][1] = ok ? brow[(k0 + 2 * c + 8) / 2] : 0u;
       }
       GroupQ<NM, TL> gn;
-      load_group_q<NM, TL>(gn, mats, ex_ix, grp + 1, groups, a.N, n, grp + 1 < groups);
+      load_group_q<BITS, NM, TL>(gn, mats, ex_ix, grp + 1, groups, a.N, n, grp + 1 < groups);
       compute_group<BITS, MODE, NM, TL, NL>(code, bq, gq, acc);
 #pragma unroll
       for (int st = 0; st < 8; ++st) {
