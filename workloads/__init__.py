@@ -90,6 +90,17 @@ CONFIGS = {
         "decode_int4", T=64, d=7168, E=128, k=2, f=2048, S=1, mode=PLAIN, seed=2, weight_bits=4,
         description="the decode shape with 4-bit group-wise quantized experts (128 weights per "
                     "group)"),
+    # profiling size of the decode shape (32 routed experts: about 3 GB of weights on the device)
+    "decode_e32_int4": LayerConfig(
+        "decode_e32_int4", T=64, d=7168, E=32, k=2, f=2048, S=1, mode=PLAIN, seed=2,
+        weight_bits=4,
+        description="decode shape with 32 routed experts + 1 shared, 4-bit experts (profiling "
+                    "size)"),
+    "decode_e32_int8": LayerConfig(
+        "decode_e32_int8", T=64, d=7168, E=32, k=2, f=2048, S=1, mode=PLAIN, seed=2,
+        weight_bits=8,
+        description="decode shape with 32 routed experts + 1 shared, 8-bit experts (profiling "
+                    "size)"),
     "gumbel": LayerConfig(
         "gumbel", T=8192, d=4096, E=16, k=2, f=14336, S=0, mode=GUMBEL, tau=0.5, seed=4,
         description="Gumbel top-2: T=8192 d=4096 E=16 k=2 d_ff=14336, tau=0.5"),
