@@ -315,6 +315,7 @@ moe_status layer_impl(const moe_config* cfg, const moe_weights* w, const uint16_
   moe_status r = check_cfg(cfg);
   if (r != MOE_OK) return r;
   if (!w || !x || !out || !w->W_g) return MOE_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(x) % 16 != 0) return MOE_ERR_INVALID_ARG;
   const bool quant = cfg->weight_bits != 0;
   if (quant) {
     if (!qweights_ok(cfg, w->quant)) return MOE_ERR_INVALID_ARG;
@@ -486,6 +487,7 @@ moe_status moe_grouped_ffn(const moe_config* cfg, const uint16_t* x, const int32
   if (cfg->weight_bits != 0) return MOE_ERR_INVALID_ARG;  // see moe_grouped_ffn_quantized
   if (!x || !perm_slot || !offsets || !W_gate || !W_up || !W_down || !y_slot)
     return MOE_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(x) % 16 != 0) return MOE_ERR_INVALID_ARG;
   if (cfg->n_shared > 0 && (!Wsh_gate || !Wsh_up || !Wsh_down)) return MOE_ERR_INVALID_ARG;
   if (W_down_f16 && cfg->n_shared > 0 && !Wsh_down_f16) return MOE_ERR_INVALID_ARG;
   if ((r = check_ws(cfg, ws, ws_bytes)) != MOE_OK) return r;

@@ -89,6 +89,13 @@ def test_entry_points_validate_before_any_launch(lib):
     assert lib.moe_grouped_ffn(ctypes.byref(scfg), fake, fake, fake, fake, fake, fake, fake,
                                fake, fake, fake, fake, None, fake, fake,
                                M.workspace_size(scfg), None) == 1
+    # rows of x move in 16-byte pieces: a misaligned x is refused before any launch
+    assert lib.moe_grouped_ffn(ctypes.byref(cfg), fake + 2, fake, fake, fake, fake, fake, fake,
+                               None, None, None, None, None, fake, fake, need, None) == 1
+    wf = M.MoeWeights()
+    wf.W_g = wf.W_gate = wf.W_up = wf.W_down = fake
+    assert lib.moe_layer_forward(ctypes.byref(cfg), ctypes.byref(wf), fake + 8, None, fake, None,
+                                 fake, need, None) == 1
     # pack: NULL / misaligned pointers
     assert lib.moe_pack_f16(None, fake, 16, None) == 1
     assert lib.moe_pack_f16(fake + 2, fake, 16, None) == 1
