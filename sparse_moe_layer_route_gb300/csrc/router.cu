@@ -8,14 +8,14 @@
 // (logits - log(-log u)) / tau from "GPT-4 Has 1.8 Trillion Parameters. It Uses 2% of Them Per
 // Token", §3.1 门控网络.
 //
-// Two kernels (plus the per-call weight preparation):
+// Three kernels after the per-call weight preparation (prep_router_kernel):
 //  * router_gemm_kernel: CTA (row tile of 128 tokens, K slice). Warp 0 streams x tiles [128 x 64]
 //    (K-major) and W_g chunks [64 x 64] (expert-major, i.e. N-major) with TMA; warp 1 issues
 //    tcgen05.mma (M=128, N=E rounded up to 64, K=16) into TMEM; warps 4-7 write the fp32 partial
 //    logits of the slice. Splitting K fills the GPU when T is small (one row tile at decode).
-//  * select_kernel: 32 tokens per CTA, 8 threads per token. The K-slice partials summed in slice
-//    order, selection scores, top-(k+1) by k+1 argmax passes (each thread over its eighth of the
-//    experts, then a 3-step shuffle reduction), softmax gates and the near-tie test.
+//  * select_kernel: one warp per token. The K-slice partials summed in slice order, selection
+//    scores, top-(k+1) by k+1 warp-wide key reductions (largest key, then the lowest expert index
+//    holding it), softmax gates and the near-tie test.
 //  * refine_kernel: the exact re-decision of the near-tie tokens (below).
 //
 // Exactness. The tensor core's fp32 accumulation differs from an exactly rounded dot product by
