@@ -42,6 +42,21 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # kernel (profiles/grouped_gemm_fine_grained.md)
 NCU_TRAFFIC = {("fine_grained", "gate_up_gemm"): (879.400448e6 + 67.677184e6),
                ("fine_grained", "down_gemm"): (473.339648e6 + 95.139840e6)}
+# captured on the 32-expert decode shape (31 routed experts touched + the shared one); every
+# touched expert's weights are read once, so a launch's DRAM bytes scale with the experts touched:
+# (DRAM read per touched expert, DRAM write per launch)
+NCU_TRAFFIC_PER_EXPERT = {("decode", "gate_up_gemm"): (1.884023e9 / 32, 3.743488e6),
+                          ("decode", "down_gemm"): (0.942734e9 / 32, 1.710592e6)}
+
+
+def ncu_traffic(cfg, kernel, n_touched):
+    """DRAM bytes per launch of the dominant kernel from an ncu capture, or None."""
+    if (cfg.name, kernel) in NCU_TRAFFIC:
+        return NCU_TRAFFIC[(cfg.name, kernel)]
+    if (cfg.name, kernel) in NCU_TRAFFIC_PER_EXPERT:
+        per_expert, writes = NCU_TRAFFIC_PER_EXPERT[(cfg.name, kernel)]
+        return per_expert * (n_touched + cfg.S) + writes
+    return None
 
 
 def launches_per_step(cfg):
@@ -509,7 +524,7 @@ def main():
     fl, by = kernel_work(cfg, dom, n_touched, n_kept)
     roof = roofline_for(dom, fl, by, phase_ms[dom] / 1e3, peaks)
     roof["kernel"] = dom
-    roof["traffic"] = NCU_TRAFFIC.get((cfg.name, dom))
+    roof["traffic"] = ncu_traffic(cfg, dom, n_touched)
     roof["peak_source"] = f"{peak_src} ({'bf16 burst' if roof['unit'] == 'TFLOP/s' else 'copy'})"
     kernels = {}
     for ph in M.PROFILE_PHASES:

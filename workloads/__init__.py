@@ -91,6 +91,10 @@ CONFIGS = {
         description="the decode shape with 4-bit group-wise quantized experts (128 weights per "
                     "group)"),
     # profiling size of the decode shape (32 routed experts: about 3 GB of weights on the device)
+    "decode_e32": LayerConfig(
+        "decode_e32", T=64, d=7168, E=32, k=2, f=2048, S=1, mode=PLAIN, seed=2,
+        description="decode shape with 32 routed experts + 1 shared, bf16 experts (profiling "
+                    "size)"),
     "decode_e32_int4": LayerConfig(
         "decode_e32_int4", T=64, d=7168, E=32, k=2, f=2048, S=1, mode=PLAIN, seed=2,
         weight_bits=4,
