@@ -1,6 +1,7 @@
 // Router: logits = x . W_g on the tensor cores (bf16 inputs, fp32 accumulation in TMEM), then
-// per token the selection score, top-k with lower-index tie-breaking and softmax gates, all in the
-// epilogue. Logits never leave the chip.
+// per token the selection score, top-k with lower-index tie-breaking and softmax gates. The GEMM
+// writes fp32 partial logits per K slice ([splits, T, EP], a few MB that stay in L2) and the
+// selection kernel adds them; the full logits exist only in the selection's registers.
 //
 // Method: "大模型MoE稀疏激活原理与工程实践", §3.1 路由器 (linear router without bias, top-k with
 // sorted=True, softmax over the selected logits); bias-adjusted selection from
