@@ -56,6 +56,7 @@ struct WsLayout {
   size_t status, meta, topk_idx, topk_w, counts, offsets, perm_slot, slot_pos;
   size_t blk_hist, blk_base, tiles, wg_pad, wg_t, rpart, rrec, xp, h, y, x_stage,
       u_stage, out_stage;
+  size_t x16, sbx, tail_acc, tail_ticket;  // quantized experts only
   // overflow re-route (zero-sized unless enabled)
   size_t sfull, maxl, pref, rr_tok, rr_exp, rr_bits, rr_ctl;
   size_t total;
@@ -126,8 +127,11 @@ cudaError_t launch_permute_noalloc(const Shape& s, const int32_t* topk_idx, int3
                                    int32_t* offsets, int32_t* perm_slot, int32_t* slot_pos,
                                    int* fault_bits, cudaStream_t st);
 
-// Builds the row-tile list from offsets (routed) plus the shared experts' identity segments
-// (unless the dispatch already did, tiles_built), and gathers x rows into expert order
+// Builds the row-tile list from offsets (routed) plus the shared experts' identity segments.
+cudaError_t launch_tiles(const Shape& s, const int32_t* offsets, TileEntry* tiles, Meta* meta,
+                         cudaStream_t st);
+// launch_tiles (unless the dispatch already built the list, tiles_built), then gathers x rows
+// into expert order
 // (xp[p] = x[perm_slot[p] / k] for p < offsets[E]).
 cudaError_t launch_tiles_and_gather(const Shape& s, const uint16_t* x, const int32_t* perm_slot,
                                     const int32_t* offsets, uint16_t* xp, TileEntry* tiles,
@@ -156,7 +160,11 @@ cudaError_t launch_quantize(int bits, int n_mat, int K, int N, const uint16_t* W
                             uint16_t* scale, uint8_t* zero, cudaStream_t st);
 struct QFfnPtrs {
   const uint16_t* x;          // [T, d] bf16
-  const uint16_t* xp;         // gathered rows [T*k, d] bf16
+  uint16_t* x16;              // [T, d] fp16 copy of x (launch_quant_act)
+  float* sbx;                 // [T, d / 128] sums of x16 over each 128-column group
+  float* tail_acc;            // [tail_cap][16][32] partials of split tail units
+  int* tail_ticket;           // [2][tail_cap]: per pass, pieces finished per tail unit
+  int tail_cap;               // quant_tail_cap()
   uint16_t* h;                // H [rows, f] fp16
   uint16_t* y;                // Y [rows, d] fp16, slot order
   const int32_t* perm_slot;   // [T*k]
@@ -165,6 +173,11 @@ struct QFfnPtrs {
   Meta* meta;
   const moe_qweights* qw;
 };
+// Pieces of split tail units the quantized passes can hold (at most one per resident warp).
+int quant_tail_cap();
+// The quantized passes' activations: x16 = fp16(x) and its 128-column group sums sbx; also
+// zeroes the passes' tail tickets.
+cudaError_t launch_quant_act(const Shape& s, const QFfnPtrs& p, cudaStream_t st);
 // ev_mid (optional): recorded on st between the gate/up and the down pass.
 cudaError_t launch_quant_ffn(const Shape& s, int bits, const QFfnPtrs& p, cudaStream_t st,
                              cudaEvent_t ev_mid = nullptr);

@@ -94,7 +94,12 @@ WsLayout ws_layout(const Shape& s) {
   L.wg_t = take(2ull * s.d * s.E);
   L.rpart = take(4ull * router_splits(s.T, s.d) * s.T * ((s.E + 63) / 64 * 64));
   L.rrec = take(sizeof(int32_t) * (size_t)s.T * kRouterRecInts);
-  L.xp = take(2ull * s.TK * s.d);
+  const bool quant = s.tile_m == kQTileM;
+  L.xp = take(quant ? 0 : 2ull * s.TK * s.d);  // the quantized passes read x16 by token
+  L.x16 = take(quant ? 2ull * s.T * s.d : 0);
+  L.sbx = take(quant ? 4ull * s.T * (s.d / 128) : 0);
+  L.tail_acc = take(quant ? 4ull * quant_tail_cap() * 16 * 32 : 0);
+  L.tail_ticket = take(quant ? 4ull * 2 * quant_tail_cap() : 0);
   L.h = take(2ull * s.rows * s.f);
   L.y = take(2ull * s.rows * s.d);
   L.x_stage = take(2ull * s.T * s.d);
@@ -290,15 +295,20 @@ moe_status qffn_impl(const Shape& s, int bits, const WsLayout& L, void* ws, cons
                      const moe_qweights* qw, uint16_t* y, cudaStream_t st,
                      bool tiles_built = false, cudaEvent_t ev_gathered = nullptr,
                      cudaEvent_t ev_gate_up = nullptr) {
-  cudaError_t e = launch_tiles_and_gather(s, x, perm_slot, offsets, at<uint16_t>(ws, L.xp),
-                                          at<TileEntry>(ws, L.tiles), at<Meta>(ws, L.meta),
-                                          tiles_built, st);
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
-  if (ev_gathered != nullptr && cudaEventRecord(ev_gathered, st) != cudaSuccess)
+  if (!tiles_built &&
+      launch_tiles(s, offsets, at<TileEntry>(ws, L.tiles), at<Meta>(ws, L.meta), st) !=
+          cudaSuccess)
     return MOE_ERR_CUDA;
   QFfnPtrs p;
   p.x = x;
-  p.xp = at<uint16_t>(ws, L.xp);
+  p.x16 = at<uint16_t>(ws, L.x16);
+  p.sbx = at<float>(ws, L.sbx);
+  p.tail_acc = at<float>(ws, L.tail_acc);
+  p.tail_ticket = at<int>(ws, L.tail_ticket);
+  p.tail_cap = quant_tail_cap();
+  if (launch_quant_act(s, p, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (ev_gathered != nullptr && cudaEventRecord(ev_gathered, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
   p.h = at<uint16_t>(ws, L.h);
   p.y = y;
   p.perm_slot = perm_slot;

@@ -350,12 +350,17 @@ cudaError_t launch_permute_noalloc(const Shape& s, const int32_t* topk_idx, int3
                         scratch + 1, status, nullptr, nullptr, st);
 }
 
+cudaError_t launch_tiles(const Shape& s, const int32_t* offsets, TileEntry* tiles, Meta* meta,
+                         cudaStream_t st) {
+  return launch_k(tiles_kernel, dim3(1), dim3(kThreads), 0, st, offsets, s.E, s.S, s.T, s.TK,
+                  s.tile_m, tiles, meta);
+}
+
 cudaError_t launch_tiles_and_gather(const Shape& s, const uint16_t* x, const int32_t* perm_slot,
                                     const int32_t* offsets, uint16_t* xp, TileEntry* tiles,
                                     Meta* meta, bool tiles_built, cudaStream_t st) {
   if (!tiles_built) {
-    const cudaError_t e = launch_k(tiles_kernel, dim3(1), dim3(kThreads), 0, st, offsets, s.E, s.S,
-                                   s.T, s.TK, s.tile_m, tiles, meta);
+    const cudaError_t e = launch_tiles(s, offsets, tiles, meta, st);
     if (e != cudaSuccess) return e;
   }
   const long long rows_per_blk = kThreads / 32;

@@ -5,10 +5,12 @@
 // quantize_kernel     one thread per (matrix, group of 128 input rows, output column): min/max,
 //                     fp16 scale, zero-point and codes, all in float64; codes are written in the
 //                     fragment order of include/moe.h (moe_qmatrix).
-// qffn_kernel<B, M>   the expert FFN on the codes, one warp per (expert, 32 output columns):
-//                     M = 0 gate/up with the SwiGLU epilogue into H (fp16), M = 1 down with the
-//                     gate scale into the slot-ordered fp16 rows Y (the same buffers and layouts
-//                     as the bf16 grouped GEMM, so dispatch and combine are shared).
+// act_prep_kernel     x16 = fp16(x) once per token, with each 128-column group's sum; the
+//                     gate/up pass reads its rows by token (no gathered copy).
+// qffn_kernel<B, M>   the expert FFN on the codes, one warp per (8-row tile, 16 or 32 output
+//                     columns): M = 0 gate/up with the SwiGLU epilogue into H (fp16), M = 1 down
+//                     with the gate scale into the slot-ordered fp16 rows Y (the same buffers and
+//                     layouts as the bf16 grouped GEMM, so dispatch and combine are shared).
 //
 // Why this shape. At decode sizes an expert sees one or two rows, so the layer is bound by the
 // bytes of the weights it touches; the kernel streams each code once with 16-byte coalesced
@@ -18,8 +20,8 @@
 // 1024 + 16 q, and the rows stored that way take a scale 16 times smaller). These feed mma.sync
 // m16n8k16 as the A operand straight from registers (weights as the M side, up to 8 tokens as
 // N); every product is exact and the sums are fp32. Per 128-row group the constant is removed
-// once, (1024 + z) * sum(b) with sum(b) from one more MMA against an all-ones fragment, and the
-// group's fp32 scale applied: the result is the dequantized weights' (q - z) * s dot product up
+// once, (1024 + z) * sum(b), and the group's fp32 scale applied; sum(b) comes precomputed with
+// x16 (gate/up) or from one more MMA against an all-ones fragment (down): the result is the dequantized weights' (q - z) * s dot product up
 // to the fp32 rounding of the offset (about 1e-4 of it, far below the fp16 rows' rounding). The
 // zero-point subtraction thus leaves the per-code path, which at 4 bits was the limit (the
 // kernel issue-bound below the memory rate). A tcgen05 MMA would need the dequantized
@@ -98,6 +100,12 @@ __global__ void __launch_bounds__(256) quantize_kernel(const uint16_t* __restric
 }
 
 // ------------------------------------------------------------------------------ FFN
+// bf16 pair -> fp16 pair (activations of the gate/up pass)
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
+  const __half2 h = __floats2half2_rn(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
 struct QMat {
   const uint8_t* q;
   const uint16_t* s;
@@ -106,15 +114,58 @@ struct QMat {
 
 struct QArgs {
   QMat routed[2], shared[2];  // M = 0: gate, up; M = 1: down (index 0)
-  const uint16_t* src;        // M = 0: gathered rows Xp [T*k, K] bf16; M = 1: H [rows, K] fp16
-  const uint16_t* x;          // M = 0: x [T, K] bf16 (shared experts' rows)
+  const uint16_t* src;        // M = 0: x16 [T, K] fp16, read by token; M = 1: H [rows, K] fp16
+  const float* bsum;          // M = 0: sbx [T, K / 128], the group sums of x16
   uint16_t* out;              // M = 0: H [rows, N] fp16; M = 1: Y [rows, N] fp16
   const TileEntry* tiles;     // 8-row tiles of every expert's rows (device-written)
   Meta* meta;                 // tile count and the work counters
-  const int32_t* perm_slot;   // M = 1
+  const int32_t* perm_slot;   // slot of each expert-ordered row
   const float* topk_w;        // M = 1 (NULL: gate 1)
-  int E, K, N;
+  float* tail_acc;            // partial accumulators of split tail units (see qffn_kernel)
+  int* tail_ticket;           // pieces finished per split tail unit (zero between launches)
+  int tail_cap;               // pieces tail_acc holds
+  int E, K, N, top_k;
 };
+
+// x16[t, :] = fp16(x[t, :]) (round to nearest, as the MMA operand takes it) and
+// sbx[t, g] = the fp32 sum of x16[t, 128 g : 128 g + 128]: each lane adds its 8 values in column
+// order, then 16 lanes combine by a fixed tree. One warp per (token, 256 columns): two groups.
+__global__ void __launch_bounds__(256) act_prep_kernel(const uint16_t* __restrict__ x, int T,
+                                                       int K, uint16_t* __restrict__ x16,
+                                                       float* __restrict__ sbx,
+                                                       int* __restrict__ tickets, int n_tickets) {
+  griddep_wait();
+  // the FFN passes' tail tickets start at zero (each pass leaves them zero, but a fresh
+  // workspace holds anything)
+  for (int i = blockIdx.x * 256 + threadIdx.x; i < n_tickets; i += gridDim.x * 256) tickets[i] = 0;
+  const int lane = threadIdx.x & 31;
+  const int chunks = K / 8, groups = K / kGroup;
+  const int passes = (chunks + 31) / 32;
+  const long long items = (long long)T * passes;
+  for (long long w = blockIdx.x * 8LL + (threadIdx.x >> 5); w < items; w += gridDim.x * 8LL) {
+    const long long t = w / passes;
+    const uint4* src = reinterpret_cast<const uint4*>(x + t * K);
+    uint4* dst = reinterpret_cast<uint4*>(x16 + t * K);
+    const int c = (int)(w % passes) * 32 + lane;  // lanes 0-15: one group, 16-31: the next
+    float sum = 0.f;
+    if (c < chunks) {
+      const uint4 v = src[c];
+      const uint4 h = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y),
+                                 bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
+      dst[c] = h;
+      const uint32_t hw[4] = {h.x, h.y, h.z, h.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hw[i]));
+        sum += f.x;
+        sum += f.y;
+      }
+    }
+#pragma unroll
+    for (int o = 1; o < 16; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if ((lane & 15) == 0 && c < chunks) sbx[t * groups + c / 16] = sum;
+  }
+}
 
 // A fragment of one 16x16 step from its 8 codes, as fp16 integers 1024 + q.
 // 8-bit: lo = codes j0..j3, hi = codes j4..j7 (one byte each).
@@ -144,11 +195,6 @@ __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// bf16 pair -> fp16 pair (activations of the gate/up pass)
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
-  const __half2 h = __floats2half2_rn(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
-  return *reinterpret_cast<const uint32_t*>(&h);
-}
 
 __device__ __forceinline__ uint16_t f16_sat(float v) {
   return __half_as_ushort(__float2half_rn(fminf(fmaxf(v, -65504.f), 65504.f)));
@@ -210,28 +256,28 @@ __device__ __forceinline__ void load_group_q(GroupQ<NM, TL>& q, const QMat* mats
       }
 }
 
+// The group's activation sum per token 2c + j (this lane's accumulator columns): M = 0 takes it
+// from sb_in (precomputed by act_prep_kernel), M = 1 forms it with one more MMA per step against
+// an all-ones A fragment.
 template <int BITS, int MODE, int NM, int TL, int NL>
 __device__ __forceinline__ void compute_group(const uint4 (&code)[NM][TL][NL],
                                               const uint32_t (&bq)[8][2],
-                                              const GroupQ<NM, TL>& q,
+                                              const float (&sb_in)[2], const GroupQ<NM, TL>& q,
                                               float (&acc)[NM][TL][4]) {
   float cg[NM][TL][4];
-  float sb[4] = {0.f, 0.f, 0.f, 0.f};  // sum of the group's activations per token (2c, 2c + 1)
 #pragma unroll
   for (int m = 0; m < NM; ++m)
 #pragma unroll
     for (int t = 0; t < TL; ++t)
 #pragma unroll
       for (int i = 0; i < 4; ++i) cg[m][t][i] = 0.f;
+  float sb[4] = {sb_in[0], sb_in[1], 0.f, 0.f};
+  if (MODE == 1) sb[0] = sb[1] = 0.f;
   const uint32_t ones[4] = {0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u};  // fp16 1.0
 #pragma unroll
   for (int st = 0; st < 8; ++st) {
-    uint32_t b0 = bq[st][0], b1 = bq[st][1];
-    if (MODE == 0) {
-      b0 = bf16x2_to_f16x2(b0);
-      b1 = bf16x2_to_f16x2(b1);
-    }
-    mma16816(sb, ones, b0, b1);
+    const uint32_t b0 = bq[st][0], b1 = bq[st][1];
+    if (MODE == 1) mma16816(sb, ones, b0, b1);
 #pragma unroll
     for (int m = 0; m < NM; ++m)
 #pragma unroll
@@ -280,8 +326,12 @@ __host__ __device__ constexpr int ring_bytes_per_warp() {
 // Each warp keeps kStages groups of codes in flight through its shared-memory ring (cp.async,
 // 16 bytes per lane per block); the activations of the next group are loaded into registers
 // while the current one is computed.
+// Register budgets (minimum CTAs per SM): 4-bit gate/up 1, so it keeps its ~160 registers
+// (three CTAs per SM, measured faster than 128 registers at four); 8-bit gate/up 4, which its
+// 48 KB ring allows anyway; the down passes the compiler's default (0: none given).
 template <int BITS, int MODE>
-__global__ void __launch_bounds__(kQThreads) qffn_kernel(const QArgs a) {
+__global__ void __launch_bounds__(kQThreads, MODE == 0 ? (BITS == 8 ? 4 : 1) : 0)
+    qffn_kernel(const QArgs a) {
   constexpr int NM = MODE == 0 ? 2 : 1;  // matrices per unit (gate and up, or down)
   constexpr int NL = BITS == 8 ? 4 : 2;  // 512-byte code blocks per group, matrix and tile
   constexpr int TL = tiles_per_unit<BITS>();
@@ -294,37 +344,81 @@ __global__ void __launch_bounds__(kQThreads) qffn_kernel(const QArgs a) {
   griddep_wait();
   const int n_tiles = a.meta->n_tiles;
   const int strips = a.N / (16 * TL);
-  const long long units = (long long)n_tiles * strips;
+  const int units = n_tiles * strips;  // < 2^31: tiles of 8 rows x column strips
   const int KP = a.K / (16 * (BITS == 8 ? 2 : 4));
   const int groups = a.K / kGroup;
   int* counter = &a.meta->work[MODE];
+  // Tail split. Units have equal length, so with W warps the last, partial round leaves most
+  // warps idle. The first `full` units run whole; each of the `tail` remaining ones is cut into
+  // S pieces over group ranges. S (the same on every warp) minimises the tail's time: rounds of
+  // pieces x piece length, a piece costing its groups plus about kPieceCost groups of start-up
+  // and reduction. Each piece stores its partial accumulators; the last piece of a unit to
+  // finish (ticket) adds all of them in piece order and runs the epilogue.
+  constexpr int kPieceCost = 3;
+  const int W = gridDim.x * (kQThreads / 32);
+  const int full = units / W * W, tail = units - full;
+  int S = 1;
+  // (the down pass's units span only d_ff / 128 groups, too few for pieces to pay: measured)
+  if (MODE == 0 && tail > 0) {
+    long long best = (long long)((tail + W - 1) / W) * (groups + kPieceCost);  // x S = 1
+    for (int s2 = 2; s2 <= 16 && s2 <= groups && tail * s2 <= a.tail_cap; ++s2) {
+      const long long r = (tail * s2 + W - 1) / W;
+      // r (groups / s2 + kPieceCost) < best / S, in integers
+      if (r * (groups + kPieceCost * s2) * S < best * s2) {
+        best = r * (groups + kPieceCost * s2);
+        S = s2;
+      }
+    }
+  }
+  const int work = full + tail * S;
+  constexpr int F = NM * TL * 4;  // accumulators per lane
   while (true) {
-    long long u = 0;
-    if (lane == 0) u = atomicAdd(counter, 1);
-    u = __shfl_sync(0xffffffffu, u, 0);
-    if (u >= units) break;
+    int v = 0;
+    if (lane == 0) v = atomicAdd(counter, 1);
+    v = __shfl_sync(0xffffffffu, v, 0);
+    if (v >= work) break;
+    int u = v;
+    int gA = 0, gB = groups, piece = -1;
+    if (MODE == 0 && S > 1 && v >= full) {
+      piece = (v - full) % S;
+      u = full + (v - full) / S;
+      gA = piece * groups / S;
+      gB = (piece + 1) * groups / S;
+    }
     const TileEntry te = a.tiles[u % n_tiles];
-    const int strip = (int)(u / n_tiles);
+    const int strip = u / n_tiles;
     const bool shared = te.expert >= a.E;
     const int ex_ix = shared ? te.expert - a.E : te.expert;
     const QMat* mats = shared ? a.shared : a.routed;
     const size_t tile0 = (size_t)ex_ix * (a.N / 16) + (size_t)strip * TL;
-    // start the ring: groups 0 .. kStages - 2
+    // start the ring: groups gA .. gA + kStages - 2 (stage = (group - gA) % kStages)
 #pragma unroll
     for (int s = 0; s < kStages - 1; ++s) {
-      if (s < groups) issue_group<NM, TL, NL>(ring, s, mats, tile0, s, KP, lane);
+      if (gA + s < gB) issue_group<NM, TL, NL>(ring, s, mats, tile0, gA + s, KP, lane);
       cp_async_commit();
     }
-    // this lane's B-fragment token: M = 0 reads Xp (routed) or x (shared) rows, M = 1 H rows
+    // Row r of the tile reads, in M = 0, x16 row (shared) arow0 + r or (routed) the token of
+    // slot perm_slot[row0 + r]; in M = 1, H row row0 + r. This lane's B fragments come from row
+    // g; its accumulator columns are rows 2c and 2c + 1, whose activation sums it needs.
+    auto src_row = [&](int r) -> long long {
+      if (MODE == 1) return te.row0 + r;
+      return shared ? te.arow0 + r : a.perm_slot[te.row0 + r] / a.top_k;
+    };
     const int tok = g;
     const bool tok_ok = tok < te.rows;
-    const uint16_t* srow;
-    if (MODE == 0)
-      srow = shared ? a.x + (size_t)(te.arow0 + (tok_ok ? tok : 0)) * a.K
-                    : a.src + (size_t)(te.row0 + (tok_ok ? tok : 0)) * a.K;
-    else
-      srow = a.src + (size_t)(te.row0 + (tok_ok ? tok : 0)) * a.K;
-    const uint32_t* brow = reinterpret_cast<const uint32_t*>(srow);
+    const uint32_t* brow =
+        reinterpret_cast<const uint32_t*>(a.src + src_row(tok_ok ? tok : 0) * a.K);
+    // M = 0: the group sums of the two x16 rows, sbx[row][grp]
+    const float* bsum_j[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+      bsum_j[j] = MODE == 0 && 2 * c + j < te.rows ? a.bsum + src_row(2 * c + j) * groups
+                                                    : nullptr;
+    auto load_sums = [&](int grp, float (&sb)[2]) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+        sb[j] = bsum_j[j] != nullptr && grp < gB ? bsum_j[j][grp] : 0.f;
+    };
     const int n = strip * 16 * TL + g;  // this lane's rows of tile t: n + 16 t and n + 16 t + 8
     float acc[NM][TL][4];
 #pragma unroll
@@ -336,19 +430,22 @@ __global__ void __launch_bounds__(kQThreads) qffn_kernel(const QArgs a) {
     uint32_t bq[8][2];
 #pragma unroll
     for (int st = 0; st < 8; ++st) {
-      bq[st][0] = tok_ok ? brow[(st * 16 + 2 * c) / 2] : 0u;
-      bq[st][1] = tok_ok ? brow[(st * 16 + 2 * c + 8) / 2] : 0u;
+      const int k0 = (gA * 8 + st) * 16;
+      bq[st][0] = tok_ok ? brow[(k0 + 2 * c) / 2] : 0u;
+      bq[st][1] = tok_ok ? brow[(k0 + 2 * c + 8) / 2] : 0u;
     }
     GroupQ<NM, TL> gq;
-    load_group_q<BITS, NM, TL>(gq, mats, ex_ix, 0, groups, a.N, n, true);
-    for (int grp = 0; grp < groups; ++grp) {
+    load_group_q<BITS, NM, TL>(gq, mats, ex_ix, gA, groups, a.N, n, true);
+    float sb[2];
+    load_sums(gA, sb);
+    for (int grp = gA; grp < gB; ++grp) {
       const int ahead = grp + kStages - 1;
-      if (ahead < groups)
-        issue_group<NM, TL, NL>(ring, ahead % kStages, mats, tile0, ahead, KP, lane);
+      if (ahead < gB)
+        issue_group<NM, TL, NL>(ring, (ahead - gA) % kStages, mats, tile0, ahead, KP, lane);
       cp_async_commit();
       cp_async_wait<kStages - 1>();  // this lane's copies of group grp have landed
       uint4 code[NM][TL][NL];
-      const int stage = grp % kStages;
+      const int stage = (grp - gA) % kStages;
 #pragma unroll
       for (int m = 0; m < NM; ++m)
 #pragma unroll
@@ -361,21 +458,56 @@ __global__ void __launch_bounds__(kQThreads) qffn_kernel(const QArgs a) {
 #pragma unroll
       for (int st = 0; st < 8; ++st) {
         const int k0 = ((grp + 1) * 8 + st) * 16;
-        const bool ok = tok_ok && grp + 1 < groups;
+        const bool ok = tok_ok && grp + 1 < gB;
         bn[st][0] = ok ? brow[(k0 + 2 * c) / 2] : 0u;
         bn[st][1] = ok ? brow[(k0 + 2 * c + 8) / 2] : 0u;
       }
       GroupQ<NM, TL> gn;
-      load_group_q<BITS, NM, TL>(gn, mats, ex_ix, grp + 1, groups, a.N, n, grp + 1 < groups);
-      compute_group<BITS, MODE, NM, TL, NL>(code, bq, gq, acc);
+      load_group_q<BITS, NM, TL>(gn, mats, ex_ix, grp + 1, groups, a.N, n, grp + 1 < gB);
+      float sbn[2];
+      load_sums(grp + 1, sbn);
+      compute_group<BITS, MODE, NM, TL, NL>(code, bq, sb, gq, acc);
 #pragma unroll
       for (int st = 0; st < 8; ++st) {
         bq[st][0] = bn[st][0];
         bq[st][1] = bn[st][1];
       }
       gq = gn;
+      sb[0] = sbn[0];
+      sb[1] = sbn[1];
     }
     cp_async_wait<0>();
+    if (MODE == 0 && piece >= 0) {
+      // a piece of a split tail unit: park the partials; the unit's last piece adds them
+      const int tu = u - full;
+      float* mine = a.tail_acc + (size_t)(tu * S + piece) * F * 32;
+#pragma unroll
+      for (int m = 0; m < NM; ++m)
+#pragma unroll
+        for (int t = 0; t < TL; ++t)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) mine[((m * TL + t) * 4 + i) * 32 + lane] = acc[m][t][i];
+      __threadfence();
+      __syncwarp();
+      int done = 0;
+      if (lane == 0) done = atomicAdd(a.tail_ticket + tu, 1);
+      done = __shfl_sync(0xffffffffu, done, 0);
+      if (done != S - 1) continue;
+      __threadfence();  // the other pieces' partials, published before their tickets
+#pragma unroll
+      for (int m = 0; m < NM; ++m)
+#pragma unroll
+        for (int t = 0; t < TL; ++t)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float* p0 = a.tail_acc + (size_t)tu * S * F * 32 +
+                              ((m * TL + t) * 4 + i) * 32 + lane;
+            float sum = __ldcg(p0);
+            for (int q = 1; q < S; ++q) sum += __ldcg(p0 + q * F * 32);
+            acc[m][t][i] = sum;
+          }
+      if (lane == 0) a.tail_ticket[tu] = 0;  // ready for the next launch
+    }
     // epilogue: element i of tile t is (column n + 16 t + 8 (i / 2), token 2 c + i % 2)
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -422,6 +554,15 @@ cudaError_t launch_quantize(int bits, int n_mat, int K, int N, const uint16_t* W
   return cudaGetLastError();
 }
 
+int quant_tail_cap() { return 64 * num_sms(); }  // warps an SM can hold, over the GPU
+
+cudaError_t launch_quant_act(const Shape& s, const QFfnPtrs& p, cudaStream_t st) {
+  const long long items = (long long)s.T * ((s.d / 8 + 31) / 32);  // warps of work
+  const int grid = (int)std::min<long long>((items + 7) / 8, 8LL * num_sms());
+  return launch_k(act_prep_kernel, dim3(grid), dim3(256), 0, st, p.x, s.T, s.d, p.x16, p.sbx,
+                  p.tail_ticket, 2 * p.tail_cap);
+}
+
 cudaError_t launch_quant_ffn(const Shape& s, int bits, const QFfnPtrs& p, cudaStream_t st,
                              cudaEvent_t ev_mid) {
   QArgs a{};
@@ -430,6 +571,10 @@ cudaError_t launch_quant_ffn(const Shape& s, int bits, const QFfnPtrs& p, cudaSt
   a.meta = p.meta;
   a.perm_slot = p.perm_slot;
   a.topk_w = p.topk_w;
+  a.top_k = s.k;
+  a.tail_acc = p.tail_acc;
+  a.tail_cap = p.tail_cap;
+  a.tail_ticket = p.tail_ticket;  // gate/up; the down pass uses the next tail_cap
   const int sms = num_sms();
   // persistent: as many CTAs as fit (work units come from the counters in Meta)
   auto smem_of = [&](int mode) {
@@ -454,8 +599,8 @@ cudaError_t launch_quant_ffn(const Shape& s, int bits, const QFfnPtrs& p, cudaSt
   a.routed[1] = {p.qw->up.q, p.qw->up.scale, p.qw->up.zero};
   a.shared[0] = {p.qw->sh_gate.q, p.qw->sh_gate.scale, p.qw->sh_gate.zero};
   a.shared[1] = {p.qw->sh_up.q, p.qw->sh_up.scale, p.qw->sh_up.zero};
-  a.src = p.xp;
-  a.x = p.x;
+  a.src = p.x16;
+  a.bsum = p.sbx;
   a.out = p.h;
   a.K = s.d;
   a.N = s.f;
@@ -475,7 +620,8 @@ cudaError_t launch_quant_ffn(const Shape& s, int bits, const QFfnPtrs& p, cudaSt
   a.shared[0] = {p.qw->sh_down.q, p.qw->sh_down.scale, p.qw->sh_down.zero};
   a.shared[1] = a.shared[0];
   a.src = p.h;
-  a.x = nullptr;
+  a.bsum = nullptr;
+  a.tail_ticket = p.tail_ticket + p.tail_cap;
   a.out = p.y;
   a.K = s.f;
   a.N = s.d;

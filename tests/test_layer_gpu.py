@@ -121,7 +121,7 @@ def test_concurrent_streams_match_serial():
     """Every piece of per-call state lives in the caller's workspace, so calls on separate
     streams and workspaces may overlap on the GPU (a serving loop does this). Layers of different
     kinds (CTA-pair GEMMs, single-CTA GEMMs with a capacity limit, the overflow re-route with its
-    cooperative kernel, 8-bit experts) launched back to back on their own streams give the same
+    cooperative kernel, 8- and 4-bit experts) launched back to back on their own streams give the same
     bytes as the same calls made one at a time."""
     kinds = [
         dict(T=1024, d=256, E=4, k=2, f=256, S=1),
@@ -130,6 +130,9 @@ def test_concurrent_streams_match_serial():
         dict(T=1024, d=256, E=32, k=2, f=128, mode=W.BIAS_SELECT, bias="zipf",
              capacity_factor=1.25, reroute=True),
         dict(T=96, d=256, E=8, k=2, f=256, S=1, weight_bits=8),
+        # 4-bit experts: every gate/up unit is split along K, and its pieces may finish in any
+        # order; their partials are still added in piece order
+        dict(T=96, d=512, E=8, k=2, f=256, S=1, weight_bits=4),
     ]
     runs = []
     for i, kw in enumerate(kinds):
