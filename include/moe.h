@@ -177,11 +177,14 @@ typedef struct {
  * the same for all of them). Host only; no CUDA call. */
 moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes);
 
-/* Clears the device status word at the start of ws (a 4-byte cudaMemsetAsync on stream).
- * Call once after allocating a workspace; moe_device_status clears it again after reading. */
+/* Clears the device status word and the counter block at the start of ws (a 512-byte
+ * cudaMemsetAsync on stream). Call once after allocating a workspace; moe_device_status clears
+ * the status word again after reading it. Every other workspace buffer is written before it is
+ * read within each call. */
 moe_status moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream);
 
-/* Steps 1-4. Router: logits in fp32 (never stored), selection score, top-k, gates.
+/* Steps 1-4. Router: logits in fp32 (per-K-slice partial sums pass through the workspace; the
+ * full logits exist only in the selection kernel's registers), selection score, top-k, gates.
  *   x [T, d] bf16, W_g [d, E] bf16, expert_bias [E] fp32 (BIAS_SELECT; else may be NULL),
  *   gumbel_u [T, E] fp32 (GUMBEL; else may be NULL).
  *   Writes topk_idx [T, k] int32 (descending score, ties to the lower index) and
