@@ -179,8 +179,9 @@ moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes);
 
 /* Clears the device status word and the counter block at the start of ws (a 512-byte
  * cudaMemsetAsync on stream). Call once after allocating a workspace; moe_device_status clears
- * the status word again after reading it. Every other workspace buffer is written before it is
- * read within each call. */
+ * the status word again after reading it. The counters in that block are left zero by every
+ * call that completes; every other workspace buffer is written before it is read within a
+ * call. */
 moe_status moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* Steps 1-4. Router: logits in fp32 (per-K-slice partial sums pass through the workspace; the
