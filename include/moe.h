@@ -33,8 +33,9 @@
  *   - All tensor pointers are caller-owned DEVICE memory unless the name ends in _host.
  *     The library allocates nothing on the device and keeps no per-call global state; every
  *     scratch buffer lives in the caller's workspace `ws` (see moe_workspace_size).
- *   - Tensor pointers are 16-byte aligned (TMA tiles and the gather move 16-byte pieces); an x
- *     that is not returns MOE_ERR_INVALID_ARG from the entry points that run the FFN on it.
+ *   - Tensor pointers are 16-byte aligned (TMA tiles, the gather and the exact dot products move
+ *     16-byte pieces); an x that is not returns MOE_ERR_INVALID_ARG from every entry point that
+ *     takes x.
  *   - Row-major layouts. bf16 tensors are passed as uint16_t bit patterns.
  *     x [T, d]; W_g [d, E]; W_gate, W_up [E, d, d_ff]; W_down [E, d_ff, d];
  *     shared expert weights [S, d, d_ff] / [S, d_ff, d]; expert_bias fp32 [E];

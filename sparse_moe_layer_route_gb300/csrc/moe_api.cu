@@ -405,6 +405,7 @@ moe_status moe_route(const moe_config* cfg, const uint16_t* x, const uint16_t* W
   moe_status r = check_cfg(cfg);
   if (r != MOE_OK) return r;
   if (!x || !W_g || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(x) % 16 != 0) return MOE_ERR_INVALID_ARG;
   if (cfg->mode == MOE_ROUTE_BIAS_SELECT && !expert_bias) return MOE_ERR_INVALID_ARG;
   if (cfg->mode == MOE_ROUTE_GUMBEL && !gumbel_u) return MOE_ERR_INVALID_ARG;
   if ((r = check_ws(cfg, ws, ws_bytes)) != MOE_OK) return r;
@@ -436,6 +437,7 @@ moe_status moe_overflow_reroute(const moe_config* cfg, const uint16_t* x,
   if (r != MOE_OK) return r;
   if (cfg->overflow_reroute == 0) return MOE_ERR_INVALID_ARG;
   if (!x || !topk_idx || !topk_w || !counts || !slot_pos) return MOE_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(x) % 16 != 0) return MOE_ERR_INVALID_ARG;
   if (cfg->mode == MOE_ROUTE_BIAS_SELECT && !expert_bias) return MOE_ERR_INVALID_ARG;
   if (cfg->mode == MOE_ROUTE_GUMBEL && !gumbel_u) return MOE_ERR_INVALID_ARG;
   if ((r = check_ws(cfg, ws, ws_bytes)) != MOE_OK) return r;
@@ -466,6 +468,7 @@ moe_status moe_grouped_ffn_quantized(const moe_config* cfg, const uint16_t* x,
   if (r != MOE_OK) return r;
   if (cfg->weight_bits == 0) return MOE_ERR_INVALID_ARG;
   if (!x || !perm_slot || !offsets || !y_slot || !qweights_ok(cfg, qw)) return MOE_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(x) % 16 != 0) return MOE_ERR_INVALID_ARG;
   if ((r = check_ws(cfg, ws, ws_bytes)) != MOE_OK) return r;
   const Shape s = make_shape(*cfg);
   const WsLayout L = ws_layout(s);

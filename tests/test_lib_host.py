@@ -96,6 +96,19 @@ def test_entry_points_validate_before_any_launch(lib):
     wf.W_g = wf.W_gate = wf.W_up = wf.W_down = fake
     assert lib.moe_layer_forward(ctypes.byref(cfg), ctypes.byref(wf), fake + 8, None, fake, None,
                                  fake, need, None) == 1
+    # the router's and the re-route's exact dot products and the quantized passes' activation
+    # prep read x in 16-byte pieces too
+    assert lib.moe_route(ctypes.byref(cfg), fake + 2, fake, None, None, fake, fake, fake, need,
+                         None) == 1
+    rcfg = M.MoeConfig.make(64, 128, 8, 2, 128, capacity_factor=1.0, overflow_reroute=1)
+    assert lib.moe_overflow_reroute(ctypes.byref(rcfg), fake + 4, None, None, fake, fake, fake,
+                                    fake, fake, M.workspace_size(rcfg), None) == 1
+    qcfg = M.MoeConfig.make(64, 128, 8, 2, 128, weight_bits=8)
+    qm = M.MoeQMatrix(q=fake, scale=fake, zero=fake)
+    qw = M.MoeQWeights(gate=qm, up=qm, down=qm)
+    assert lib.moe_grouped_ffn_quantized(ctypes.byref(qcfg), fake + 6, fake, fake, None,
+                                         ctypes.byref(qw), fake, fake, M.workspace_size(qcfg),
+                                         None) == 1
     # pack: NULL / misaligned pointers
     assert lib.moe_pack_f16(None, fake, 16, None) == 1
     assert lib.moe_pack_f16(fake + 2, fake, 16, None) == 1
