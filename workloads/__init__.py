@@ -90,6 +90,12 @@ CONFIGS = {
         "decode_int4", T=64, d=7168, E=128, k=2, f=2048, S=1, mode=PLAIN, seed=2, weight_bits=4,
         description="the decode shape with 4-bit group-wise quantized experts (128 weights per "
                     "group)"),
+    # profiling size of the skewed prefill with re-route: the same routing (x, W_g and the bias
+    # are drawn before the experts), d_ff = 128 (about 1 GB on the device)
+    "skewed_reroute_f128": LayerConfig(
+        "skewed_reroute_f128", T=16384, d=7168, E=128, k=2, f=128, S=0, mode=BIAS_SELECT,
+        capacity_factor=1.25, seed=3, bias="zipf", zipf_s=1.1, reroute=True,
+        description="the skewed prefill with re-route at d_ff=128 (profiling size)"),
     # profiling size of the decode shape (32 routed experts: about 3 GB of weights on the device)
     "decode_e32": LayerConfig(
         "decode_e32", T=64, d=7168, E=32, k=2, f=2048, S=1, mode=PLAIN, seed=2,
