@@ -66,7 +66,7 @@ def launches_per_step(cfg):
     three kernels and a second dispatch."""
     n = 10
     if getattr(cfg, "reroute", False) and cfg.capacity_factor > 0:
-        n += 3 + 2
+        n += 4 + 2
     return n
 
 

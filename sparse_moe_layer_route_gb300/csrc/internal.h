@@ -48,7 +48,8 @@ struct Meta {
   int dispatch_ticket; // dispatch histogram CTAs finished (reset by the last one)
   int reroute_rounds; // proposal rounds of the last overflow re-route (diagnostic)
   int work[2];        // next work unit of the quantized gate/up and down passes
-  int pad[57];
+  int reroute_exact;  // first windows listed for the re-route's exact pass (zero between calls)
+  int pad[56];
 };
 
 // Offsets of every buffer carved from the caller's workspace (bytes, 256-aligned).
@@ -103,6 +104,8 @@ struct RerouteArgs {
   uint8_t* pref;           // [T, PS] preference lists (expert ids < 256), PS = E rounded up to 16
   int32_t *plen, *dem, *ptr, *held;  // [T] each: list length, dropped slots, next position, kept
   int32_t *rlen, *ext_list;          // [T] each: exactly ordered prefix, tokens needing more
+  int32_t* ex_list;        // [T] tokens whose first window waits for reroute_exact_kernel
+  int32_t* ex_count;       // their number (zero between calls)
   int32_t *room, *cut, *touched;     // [E] each
   uint32_t* bits;          // [E, W] proposals held by each expert, bit t of word t / 32
   int32_t* rejected;       // [1024] turn-aways per round

@@ -110,7 +110,7 @@ WsLayout ws_layout(const Shape& s) {
   L.sfull = take(rr ? 4ull * s.T * s.E : 0);
   L.maxl = take(rr ? 4ull * s.T : 0);
   L.pref = take(rr ? (size_t)s.T * ((s.E + 15) / 16 * 16) : 0);
-  L.rr_tok = take(rr ? 4ull * 6 * s.T : 0);     // plen, dem, ptr, held, rlen, ext_list
+  L.rr_tok = take(rr ? 4ull * 7 * s.T : 0);     // plen, dem, ptr, held, rlen, ext_list, ex_list
   L.rr_exp = take(rr ? 4ull * 3 * s.E : 0);     // room, cut, touched
   L.rr_bits = take(rr ? 4ull * s.E * W : 0);
   L.rr_ctl = take(rr ? 4ull * (2 * 1024 + 2) : 0);  // per-round counters, barrier
@@ -225,6 +225,8 @@ moe_status reroute_impl(const Shape& s, const WsLayout& L, void* ws, const uint1
   a.held = tok + 3 * (size_t)s.T;
   a.rlen = tok + 4 * (size_t)s.T;
   a.ext_list = tok + 5 * (size_t)s.T;
+  a.ex_list = tok + 6 * (size_t)s.T;
+  a.ex_count = &at<Meta>(ws, L.meta)->reroute_exact;
   int32_t* ex = at<int32_t>(ws, L.rr_exp);
   a.room = ex;
   a.cut = ex + s.E;

@@ -14,6 +14,8 @@
 //                           positions whose adjacent gaps lie inside the tensor-core error band
 //                           is re-ordered by exact fp32 dot products. Also resets the per-expert
 //                           state and the proposal bitmaps.
+//   reroute_exact_kernel    the first windows that need exact dot products, a CTA per token
+//                           (the prep kernel lists them instead of computing them per warp).
 //   reroute_da_kernel       cooperative (all CTAs resident), rounds of
 //                             A. every token with unmet demand proposes to its next experts,
 //                                skipping experts already full with better tokens; a token that
@@ -55,6 +57,11 @@ __device__ __forceinline__ uint64_t globaltimer() {
   uint64_t t;
   asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
   return t;
+}
+
+// Bulk prefetch of [p, p + bytes) into L2 (p and bytes multiples of 16); no completion to wait on.
+__device__ __forceinline__ void l2_prefetch(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 // float -> uint32 with the same order (every float but NaN; scores are never NaN here)
@@ -118,16 +125,58 @@ __device__ __forceinline__ WarpScratch warp_scratch(uint8_t* smem, int warp, int
   return w;
 }
 
+__device__ __forceinline__ float window_band(const RerouteArgs& a, int t) {
+  float band = router_band(a.d, a.maxl[t]);
+  if (a.mode == MOE_ROUTE_GUMBEL) band /= a.tau;
+  return band;
+}
+
+// Window positions [0, n) with a neighbour (inside the window) closer than the band, compacted
+// into ws.mpos; returns their number. One warp; all lanes call it.
+__device__ __forceinline__ int window_members(const WarpScratch& ws, int n, float band, int lane) {
+  int nm = 0;
+  for (int c0 = 0; c0 < n; c0 += 32) {
+    const int i = c0 + lane;
+    bool mem = false;
+    if (i < n) {
+      if (i > 0) mem = ws.sw[i - 1] - ws.sw[i] < band;
+      if (i + 1 < n) mem = mem || ws.sw[i] - ws.sw[i + 1] < band;
+    }
+    const unsigned mm = __ballot_sync(0xffffffffu, mem);
+    if (mem) ws.mpos[nm + __popc(mm & ((1u << lane) - 1u))] = i;
+    nm += __popc(mm);
+  }
+  return nm;
+}
+
+// Each member moves to its exact rank inside its run (ws.ex holds the members' exact scores):
+// pref[w0 + rank] = its expert. Threads j = first, first + step, ... take member j.
+__device__ __forceinline__ void rank_members(const RerouteArgs& a, int t, int w0, int n,
+                                             float band, const WarpScratch& ws, int nm,
+                                             int first, int step) {
+  uint8_t* prefw = a.pref + (size_t)t * a.PS;
+  for (int m = first; m < nm; m += step) {
+    const int i = ws.mpos[m];
+    int lo = i, hi = i;
+    while (lo > 0 && ws.sw[lo - 1] - ws.sw[lo] < band) --lo;
+    while (hi + 1 < n && ws.sw[hi] - ws.sw[hi + 1] < band) ++hi;
+    int r = lo;
+    for (int i2 = lo; i2 <= hi; ++i2) r += beats(ws.ex[i2], ws.pe[i2], ws.ex[i], ws.pe[i]) ? 1 : 0;
+    prefw[w0 + r] = (uint8_t)ws.pe[i];
+  }
+}
+
 // Orders positions [w0, w1) of token t's list exactly, where w1 = min(L, w0 + kWindow) moved on
 // to the end of the run it falls in; returns w1. Positions before w0 are already final and w0
 // starts a run. The caller has put the experts and tensor-core scores of positions w0..L-1 into
-// ws.pe / ws.sw (index = position - w0). One warp; all lanes call it.
+// ws.pe / ws.sw (index = position - w0). One warp; all lanes call it. With defer (first windows,
+// w0 = 0), a window that needs exact dot products is left in tensor-core order and its token
+// listed for reroute_exact_kernel, which orders it the same way with a whole CTA.
 __device__ int refine_window(const RerouteArgs& a, int t, int w0, int L, const WarpScratch& ws,
-                             int lane) {
+                             int lane, bool defer = false) {
   if (w0 >= L) return L;
   const int E = a.E;
-  float band = router_band(a.d, a.maxl[t]);
-  if (a.mode == MOE_ROUTE_GUMBEL) band /= a.tau;
+  const float band = window_band(a, t);
   // window end: extend while the gap across it is inside the band
   const int m = L - w0;  // positions available
   int n = min(m, kWindow);
@@ -143,19 +192,12 @@ __device__ int refine_window(const RerouteArgs& a, int t, int w0, int L, const W
   }
   const int w1 = w0 + n;
   // members: positions with a neighbour inside the band
-  int nm = 0;
-  for (int c0 = 0; c0 < n; c0 += 32) {
-    const int i = c0 + lane;
-    bool mem = false;
-    if (i < n) {
-      if (i > 0) mem = ws.sw[i - 1] - ws.sw[i] < band;
-      if (i + 1 < n) mem = mem || ws.sw[i] - ws.sw[i + 1] < band;
-    }
-    const unsigned mm = __ballot_sync(0xffffffffu, mem);
-    if (mem) ws.mpos[nm + __popc(mm & ((1u << lane) - 1u))] = i;
-    nm += __popc(mm);
-  }
+  const int nm = window_members(ws, n, band, lane);
   if (nm == 0) return w1;
+  if (defer) {
+    if (lane == 0) a.ex_list[atomicAdd(a.ex_count, 1)] = t;
+    return w1;
+  }
   __syncwarp();
   // exact selection scores of the members, kDotBatch dot products per pass over x
   const uint4* x4 = reinterpret_cast<const uint4*>(a.x + (size_t)t * a.d);
@@ -205,17 +247,7 @@ __device__ int refine_window(const RerouteArgs& a, int t, int w0, int L, const W
     }
   }
   __syncwarp();
-  // each member moves to its exact rank inside its run
-  uint8_t* prefw = a.pref + (size_t)t * a.PS;
-  for (int m = lane; m < nm; m += 32) {
-    const int i = ws.mpos[m];
-    int lo = i, hi = i;
-    while (lo > 0 && ws.sw[lo - 1] - ws.sw[lo] < band) --lo;
-    while (hi + 1 < n && ws.sw[hi] - ws.sw[hi + 1] < band) ++hi;
-    int r = lo;
-    for (int i2 = lo; i2 <= hi; ++i2) r += beats(ws.ex[i2], ws.pe[i2], ws.ex[i], ws.pe[i]) ? 1 : 0;
-    prefw[w0 + r] = (uint8_t)ws.pe[i];
-  }
+  rank_members(a, t, w0, n, band, ws, nm, lane, 32);
   __syncwarp();
   return w1;
 }
@@ -280,7 +312,7 @@ __device__ void prep_token(const RerouteArgs& a, int t, int lane, const WarpScra
     }
   }
   __syncwarp();
-  const int r = refine_window(a, t, 0, L, ws, lane);
+  const int r = refine_window(a, t, 0, L, ws, lane, /*defer=*/true);
   if (lane == 0) {
     a.plen[t] = L;
     a.rlen[t] = r;
@@ -314,6 +346,102 @@ __global__ void __launch_bounds__(kThreads) reroute_prep_kernel(const RerouteArg
   }
   for (int t = blockIdx.x * kWarps + warp; t < a.T; t += gridDim.x * kWarps)
     prep_token<V>(a, t, lane, ws);
+}
+
+// The first windows the prep kernel listed: the same ordering as refine_window, with the exact
+// dot products spread over a whole CTA (each thread a strided share of the d / 8 16-byte chunks,
+// one round of loads for d up to 8192) instead of one warp (seven dependent rounds at d = 7168).
+// A CTA per listed token at a time; the partial sums are added by a fixed tree (shuffles, then
+// the warps in order), so results are deterministic.
+__global__ void __launch_bounds__(kThreads) reroute_exact_kernel(const RerouteArgs a) {
+  __shared__ float s_sw[256], s_ex[256];
+  __shared__ int s_pe[256], s_mpos[256];
+  __shared__ float red[kWarps][kDotBatch];
+  __shared__ int s_nm;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  WarpScratch ws;
+  ws.sw = s_sw;
+  ws.ex = s_ex;
+  ws.pe = s_pe;
+  ws.mpos = s_mpos;
+  griddep_wait();
+  const int count = *a.ex_count;
+  const int d8 = a.d / 8;
+  if (threadIdx.x == 0 && blockIdx.x < count)
+    l2_prefetch(a.x + (size_t)a.ex_list[blockIdx.x] * a.d, (uint32_t)a.d * 2u);
+  for (int li = blockIdx.x; li < count; li += gridDim.x) {
+    const int t = a.ex_list[li];
+    // the next listed token's x row comes into L2 while this one is ordered
+    if (threadIdx.x == 0 && li + gridDim.x < count)
+      l2_prefetch(a.x + (size_t)a.ex_list[li + gridDim.x] * a.d, (uint32_t)a.d * 2u);
+    const int n = a.rlen[t];  // the window the prep kernel closed, positions [0, n)
+    for (int i = threadIdx.x; i < n; i += kThreads) {
+      const int e = a.pref[(size_t)t * a.PS + i];
+      s_pe[i] = e;
+      s_sw[i] = a.sfull[(size_t)t * a.E + e];
+    }
+    __syncthreads();
+    const float band = window_band(a, t);
+    if (warp == 0) {
+      const int nm = window_members(ws, n, band, lane);
+      if (lane == 0) s_nm = nm;
+    }
+    __syncthreads();
+    const int nm = s_nm;
+    const uint4* x4 = reinterpret_cast<const uint4*>(a.x + (size_t)t * a.d);
+    for (int b0 = 0; b0 < nm; b0 += kDotBatch) {
+      const int nb = min(kDotBatch, nm - b0);
+      const uint4* w4[kDotBatch];
+#pragma unroll
+      for (int c = 0; c < kDotBatch; ++c)
+        w4[c] = reinterpret_cast<const uint4*>(a.WgT + (size_t)s_pe[s_mpos[b0 + (c < nb ? c : 0)]] *
+                                                          a.d);
+      float acc[kDotBatch];
+#pragma unroll
+      for (int c = 0; c < kDotBatch; ++c) acc[c] = 0.f;
+#pragma unroll 4
+      for (int g = threadIdx.x; g < d8; g += kThreads) {
+        const uint4 xv = x4[g];
+        const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+        for (int c = 0; c < kDotBatch; ++c) {
+          if (c < nb) {
+            const uint4 wv = w4[c][g];
+            const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+            float v = acc[c];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              v = fmaf(__uint_as_float(xw[h] << 16), __uint_as_float(ww[h] << 16), v);
+              v = fmaf(__uint_as_float(xw[h] & 0xFFFF0000u), __uint_as_float(ww[h] & 0xFFFF0000u),
+                       v);
+            }
+            acc[c] = v;
+          }
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < kDotBatch; ++c) {
+        float v = acc[c];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+        if (lane == 0) red[warp][c] = v;
+      }
+      __syncthreads();
+      if (threadIdx.x < nb) {
+        const int c = threadIdx.x;
+        float v = red[0][c];
+        for (int w = 1; w < kWarps; ++w) v += red[w][c];
+        const int i = s_mpos[b0 + c];
+        const int e = s_pe[i];
+        s_ex[i] = selection_score(a.mode, v, a.mode == MOE_ROUTE_BIAS_SELECT ? a.bias[e] : 0.f,
+                                  a.mode == MOE_ROUTE_GUMBEL ? a.u[(size_t)t * a.E + e] : 0.f,
+                                  a.tau);
+      }
+      __syncthreads();
+    }
+    rank_members(a, t, 0, n, band, ws, nm, threadIdx.x, kThreads);
+    __syncthreads();
+  }
 }
 
 // Grid-wide barrier for the cooperative launch. Returns false when the wait ran past its bound
@@ -485,6 +613,8 @@ __global__ void __launch_bounds__(kThreads) reroute_da_kernel(const RerouteArgs 
 __global__ void __launch_bounds__(kThreads) reroute_finalize_kernel(const RerouteArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   griddep_wait();
+  // the exact pass's list is empty again for the next call (the pass has completed)
+  if (blockIdx.x == 0 && threadIdx.x == 0) *a.ex_count = 0;
   for (int t = blockIdx.x * kWarps + warp; t < a.T; t += gridDim.x * kWarps) {
     if (a.dem[t] == 0) continue;
     const int len = a.ptr[t];
@@ -551,6 +681,8 @@ cudaError_t launch_reroute(const RerouteArgs& args, cudaStream_t st) {
   const int tok_blocks = (a.T + kWarps - 1) / kWarps;
   err = launch_k(prep, dim3(tok_blocks < 8 * sms ? tok_blocks : 8 * sms), dim3(kThreads), smem,
                  st, a);
+  if (err != cudaSuccess) return err;
+  err = launch_k(reroute_exact_kernel, dim3(8 * sms), dim3(kThreads), 0, st, a);
   if (err != cudaSuccess) return err;
   // proposal rounds: every CTA resident (cooperative launch), one CTA per SM at most
   int per_sm = 0;
