@@ -45,9 +45,16 @@
  *     synchronously (nothing is enqueued then). Errors detected by the kernels (an expert index
  *     outside [0, E), a pipeline wait that timed out) are recorded in a status word inside `ws`
  *     and read with moe_device_status.
- *   - Supported sizes: T >= 1; 1 <= E <= 256; 1 <= top_k <= min(E, 8); 0 <= n_shared <= 4;
+ *   - Supported sizes: T >= 0; 1 <= E <= 256; 1 <= top_k <= min(E, 8); 0 <= n_shared <= 4;
  *     d and d_ff multiples of 64; T * (top_k + n_shared) < 2^31. Anything else returns
- *     MOE_ERR_UNSUPPORTED.
+ *     MOE_ERR_UNSUPPORTED (a negative T returns MOE_ERR_INVALID_ARG).
+ *   - An empty batch (T = 0) is valid everywhere and launches no kernel. The configuration is
+ *     still validated; tensor pointers and the workspace are not examined (an empty tensor may
+ *     pass NULL). Only the per-expert dispatch outputs are non-empty: moe_permute and
+ *     moe_permute_noalloc (which require counts and offsets) and moe_layer_forward(_profiled)
+ *     (for the members of route_out that are given) clear counts [E] and offsets [E + 1] with
+ *     cudaMemsetAsync on the stream; moe_permute_noalloc also clears fault_bits if given;
+ *     moe_layer_forward_profiled records its seven events back to back.
  */
 #ifndef MOE_GB300_H
 #define MOE_GB300_H
@@ -63,7 +70,8 @@ typedef struct CUstream_st* moe_stream_t; /* identical to cudaStream_t */
 
 typedef enum {
   MOE_OK = 0,
-  MOE_ERR_INVALID_ARG = 1,   /* NULL pointer where one is required, non-positive size, bad mode */
+  MOE_ERR_INVALID_ARG = 1,   /* NULL pointer where one is required, negative T or non-positive
+                                other size, bad mode */
   MOE_ERR_UNSUPPORTED = 2,   /* sizes outside the supported range above */
   MOE_ERR_WORKSPACE = 3,     /* ws is NULL, misaligned (needs 256 B) or smaller than required */
   MOE_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed (launch, tensor-map encode) */
@@ -175,7 +183,8 @@ typedef struct {
 } moe_route_out;
 
 /* Bytes of workspace every entry point below needs for this config (an upper bound that is
- * the same for all of them). Host only; no CUDA call. */
+ * the same for all of them; 512 for an empty batch, T = 0, which only moe_workspace_init and
+ * moe_device_status use). Host only; no CUDA call. */
 moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes);
 
 /* Clears the device status word and the counter block at the start of ws (a 512-byte

@@ -139,7 +139,7 @@ namespace {
 
 moe_status check_cfg(const moe_config* c) {
   if (c == nullptr) return MOE_ERR_INVALID_ARG;
-  if (c->T < 1 || c->d < 1 || c->E < 1 || c->top_k < 1 || c->d_ff < 1 || c->n_shared < 0)
+  if (c->T < 0 || c->d < 1 || c->E < 1 || c->top_k < 1 || c->d_ff < 1 || c->n_shared < 0)
     return MOE_ERR_INVALID_ARG;
   if (c->mode < MOE_ROUTE_PLAIN || c->mode > MOE_ROUTE_GUMBEL) return MOE_ERR_INVALID_ARG;
   if (c->mode == MOE_ROUTE_GUMBEL && !(c->tau > 0.f && std::isfinite(c->tau)))
@@ -175,6 +175,16 @@ T* at(void* ws, size_t off) {
 }
 
 moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// An empty batch (T = 0) launches no kernel and reads no tensor. The dispatch's per-expert
+// outputs are its only non-empty results: every expert receives nothing, so counts [E] and
+// offsets [E + 1] are cleared (each only if given).
+moe_status clear_dispatch(int E, int32_t* counts, int32_t* offsets, cudaStream_t st) {
+  if (counts && cudaMemsetAsync(counts, 0, 4ull * E, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (offsets && cudaMemsetAsync(offsets, 0, 4ull * (E + 1), st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
 
 moe_status route_impl(const Shape& s, const WsLayout& L, void* ws, const uint16_t* x,
                       const uint16_t* W_g, const float* bias, const float* u, int32_t* idx,
@@ -326,6 +336,12 @@ moe_status layer_impl(const moe_config* cfg, const moe_weights* w, const uint16_
                       size_t ws_bytes, cudaStream_t st, cudaEvent_t const* ev) {
   moe_status r = check_cfg(cfg);
   if (r != MOE_OK) return r;
+  if (cfg->T == 0) {
+    // the phase events are still recorded, back to back, so that every elapsed time is defined
+    for (int i = 0; ev != nullptr && i < 7; ++i)
+      if (cudaEventRecord(ev[i], st) != cudaSuccess) return MOE_ERR_CUDA;
+    return ro ? clear_dispatch(cfg->E, ro->counts, ro->offsets, st) : MOE_OK;
+  }
   if (!w || !x || !out || !w->W_g) return MOE_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(x) % 16 != 0) return MOE_ERR_INVALID_ARG;
   const bool quant = cfg->weight_bits != 0;
@@ -389,7 +405,8 @@ moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes) {
   moe_status r = check_cfg(cfg);
   if (r != MOE_OK) return r;
   if (bytes == nullptr) return MOE_ERR_INVALID_ARG;
-  *bytes = ws_layout(make_shape(*cfg)).total;
+  // an empty batch needs only the status word and the meta block that moe_workspace_init clears
+  *bytes = cfg->T == 0 ? 512 : ws_layout(make_shape(*cfg)).total;
   return MOE_OK;
 }
 
@@ -406,6 +423,7 @@ moe_status moe_route(const moe_config* cfg, const uint16_t* x, const uint16_t* W
                      float* topk_w, void* ws, size_t ws_bytes, moe_stream_t stream) {
   moe_status r = check_cfg(cfg);
   if (r != MOE_OK) return r;
+  if (cfg->T == 0) return MOE_OK;
   if (!x || !W_g || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(x) % 16 != 0) return MOE_ERR_INVALID_ARG;
   if (cfg->mode == MOE_ROUTE_BIAS_SELECT && !expert_bias) return MOE_ERR_INVALID_ARG;
@@ -422,6 +440,10 @@ moe_status moe_permute(const moe_config* cfg, const int32_t* topk_idx, int32_t* 
                        size_t ws_bytes, moe_stream_t stream) {
   moe_status r = check_cfg(cfg);
   if (r != MOE_OK) return r;
+  if (cfg->T == 0) {
+    if (!counts || !offsets) return MOE_ERR_INVALID_ARG;
+    return clear_dispatch(cfg->E, counts, offsets, (cudaStream_t)stream);
+  }
   if (!topk_idx || !counts || !offsets || !perm_slot || !slot_pos) return MOE_ERR_INVALID_ARG;
   if ((r = check_ws(cfg, ws, ws_bytes)) != MOE_OK) return r;
   const Shape s = make_shape(*cfg);
@@ -438,6 +460,7 @@ moe_status moe_overflow_reroute(const moe_config* cfg, const uint16_t* x,
   moe_status r = check_cfg(cfg);
   if (r != MOE_OK) return r;
   if (cfg->overflow_reroute == 0) return MOE_ERR_INVALID_ARG;
+  if (cfg->T == 0) return MOE_OK;
   if (!x || !topk_idx || !topk_w || !counts || !slot_pos) return MOE_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(x) % 16 != 0) return MOE_ERR_INVALID_ARG;
   if (cfg->mode == MOE_ROUTE_BIAS_SELECT && !expert_bias) return MOE_ERR_INVALID_ARG;
@@ -469,6 +492,7 @@ moe_status moe_grouped_ffn_quantized(const moe_config* cfg, const uint16_t* x,
   moe_status r = check_cfg(cfg);
   if (r != MOE_OK) return r;
   if (cfg->weight_bits == 0) return MOE_ERR_INVALID_ARG;
+  if (cfg->T == 0) return MOE_OK;
   if (!x || !perm_slot || !offsets || !y_slot || !qweights_ok(cfg, qw)) return MOE_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(x) % 16 != 0) return MOE_ERR_INVALID_ARG;
   if ((r = check_ws(cfg, ws, ws_bytes)) != MOE_OK) return r;
@@ -483,6 +507,12 @@ moe_status moe_permute_noalloc(const moe_config* cfg, const int32_t* topk_idx, i
                                int32_t* fault_bits, moe_stream_t stream) {
   moe_status r = check_cfg(cfg);
   if (r != MOE_OK) return r;
+  if (cfg->T == 0) {
+    if (!counts || !offsets) return MOE_ERR_INVALID_ARG;
+    if (fault_bits && cudaMemsetAsync(fault_bits, 0, 4, (cudaStream_t)stream) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    return clear_dispatch(cfg->E, counts, offsets, (cudaStream_t)stream);
+  }
   if (!topk_idx || !counts || !offsets || !perm_slot || !slot_pos) return MOE_ERR_INVALID_ARG;
   const Shape s = make_shape(*cfg);
   if (s.TK > MOE_NOALLOC_MAX_SLOTS) return MOE_ERR_UNSUPPORTED;
@@ -500,6 +530,7 @@ moe_status moe_grouped_ffn(const moe_config* cfg, const uint16_t* x, const int32
   moe_status r = check_cfg(cfg);
   if (r != MOE_OK) return r;
   if (cfg->weight_bits != 0) return MOE_ERR_INVALID_ARG;  // see moe_grouped_ffn_quantized
+  if (cfg->T == 0) return MOE_OK;
   if (!x || !perm_slot || !offsets || !W_gate || !W_up || !W_down || !y_slot)
     return MOE_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(x) % 16 != 0) return MOE_ERR_INVALID_ARG;
@@ -516,6 +547,7 @@ moe_status moe_combine(const moe_config* cfg, const uint16_t* y_slot, const int3
                        uint16_t* out, void* ws, size_t ws_bytes, moe_stream_t stream) {
   moe_status r = check_cfg(cfg);
   if (r != MOE_OK) return r;
+  if (cfg->T == 0) return MOE_OK;
   if (!y_slot || !slot_pos || !out) return MOE_ERR_INVALID_ARG;
   if ((r = check_ws(cfg, ws, ws_bytes)) != MOE_OK) return r;
   const Shape s = make_shape(*cfg);
@@ -545,6 +577,7 @@ moe_status moe_layer_forward_host(const moe_config* cfg, const moe_weights* w,
                                   moe_stream_t stream) {
   moe_status r = check_cfg(cfg);
   if (r != MOE_OK) return r;
+  if (cfg->T == 0) return MOE_OK;
   if (!x_host || !out_host) return MOE_ERR_INVALID_ARG;
   if (cfg->mode == MOE_ROUTE_GUMBEL && !gumbel_u_host) return MOE_ERR_INVALID_ARG;
   if ((r = check_ws(cfg, ws, ws_bytes)) != MOE_OK) return r;

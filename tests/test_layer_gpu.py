@@ -157,3 +157,38 @@ def test_concurrent_streams_match_serial():
         for (cfg, inp, mc, weights, ws, out), ref in zip(runs, serial):
             assert M.device_status(ws) == 0
             assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), cfg.name
+
+
+def test_empty_batch_clears_only_the_per_expert_outputs():
+    """T = 0 launches no kernel: the dispatch outputs counts [E] and offsets [E + 1] are cleared
+    (every expert receives nothing), the fault word of the allocation-free dispatch is cleared,
+    the profiled layer still records all seven events, and the workspace stays clean."""
+    dev, E, k = "cuda", 8, 2
+    cfg = M.MoeConfig.make(0, 128, E, k, 128, n_shared=1, capacity_factor=1.0)
+    ws = M.alloc_workspace(cfg)
+    assert ws.numel() == 512
+    i32 = dict(dtype=torch.int32, device=dev)
+    empty = torch.empty((0, k), **i32)
+
+    def filled():
+        return torch.full((E,), -7, **i32), torch.full((E + 1,), -7, **i32)
+
+    counts, offsets = filled()
+    M.permute(cfg, empty, counts, offsets, empty.view(-1), empty.view(-1), ws)
+    counts2, offsets2 = filled()
+    fault = torch.full((1,), 99, **i32)
+    M.permute_noalloc(cfg, empty, counts2, offsets2, empty.view(-1), empty.view(-1), fault)
+    counts3, offsets3 = filled()
+    x = torch.empty((0, 128), dtype=torch.bfloat16, device=dev)
+    out = torch.empty((0, 128), dtype=torch.bfloat16, device=dev)
+    Wg = torch.zeros((128, E), dtype=torch.bfloat16, device=dev)
+    w = M.make_weights(Wg, None, None, None, None)      # no expert weight is read
+    M.layer_forward(cfg, w, x, None, out, M.make_route_out(counts=counts3, offsets=offsets3), ws)
+    events = [torch.cuda.Event(enable_timing=True) for _ in range(7)]
+    M.layer_forward_profiled(cfg, w, x, None, out, None, ws, events)
+    torch.cuda.synchronize()
+    for c, o in ((counts, offsets), (counts2, offsets2), (counts3, offsets3)):
+        assert torch.equal(c, torch.zeros_like(c)) and torch.equal(o, torch.zeros_like(o))
+    assert int(fault.item()) == 0
+    assert all(events[i].elapsed_time(events[i + 1]) >= 0.0 for i in range(6))
+    assert M.device_status(ws) == 0

@@ -45,7 +45,7 @@ def test_workspace_size_and_layout(lib):
 
 
 @pytest.mark.parametrize("kw,status", [
-    (dict(T=0), 1), (dict(E=0), 1), (dict(top_k=0), 1), (dict(mode=3), 1),
+    (dict(T=-1), 1), (dict(T=0), 0), (dict(T=0, E=300), 2), (dict(E=0), 1), (dict(top_k=0), 1), (dict(mode=3), 1),
     (dict(mode=2, tau=0.0), 1), (dict(E=300), 2), (dict(top_k=9, E=16), 2),
     (dict(top_k=5, E=4), 2), (dict(d=100), 2), (dict(d_ff=96), 2), (dict(n_shared=5), 2),
     (dict(overflow_reroute=2), 1), (dict(overflow_reroute=1, n_groups=4, topk_groups=2), 2),
@@ -161,3 +161,32 @@ def test_quantize_weights_validation(lib):
     cfg0 = M.MoeConfig.make(64, 128, 8, 2, 128)
     assert lib.moe_grouped_ffn_quantized(ctypes.byref(cfg0), P, P, P, None, ctypes.byref(q), P,
                                          P, 1 << 30, None) == 1            # weight_bits 0
+
+
+def test_empty_batch_is_a_no_op_on_the_host(lib):
+    """T = 0: the configuration is still validated, tensor pointers and the workspace are not
+    examined, and the entry points that have nothing to clear return MOE_OK without a CUDA call
+    (this machine may have no GPU at all)."""
+    cfg = M.MoeConfig.make(0, 128, 8, 2, 128, n_shared=1, mode=M.ROUTE_GUMBEL, tau=0.5,
+                           capacity_factor=1.0, overflow_reroute=1)
+    n = ctypes.c_size_t(0)
+    assert lib.moe_workspace_size(ctypes.byref(cfg), ctypes.byref(n)) == 0 and n.value == 512
+    z = None
+    assert lib.moe_route(ctypes.byref(cfg), z, z, z, z, z, z, z, 0, z) == 0
+    assert lib.moe_overflow_reroute(ctypes.byref(cfg), z, z, z, z, z, z, z, z, 0, z) == 0
+    assert lib.moe_grouped_ffn(ctypes.byref(cfg), z, z, z, z, z, z, z, z, z, z, z, z, z, z, 0,
+                               z) == 0
+    assert lib.moe_combine(ctypes.byref(cfg), z, z, z, z, 0, z) == 0
+    assert lib.moe_layer_forward(ctypes.byref(cfg), z, z, z, z, z, z, 0, z) == 0
+    assert lib.moe_layer_forward_host(ctypes.byref(cfg), z, z, z, z, z, 0, z) == 0
+    q = M.MoeConfig.make(0, 128, 8, 2, 128, weight_bits=8)
+    assert lib.moe_grouped_ffn_quantized(ctypes.byref(q), z, z, z, z, z, z, z, 0, z) == 0
+    # the dispatch entry points still need their per-expert outputs
+    assert lib.moe_permute(ctypes.byref(cfg), z, z, z, z, z, z, 0, z) == 1
+    assert lib.moe_permute_noalloc(ctypes.byref(cfg), z, z, z, z, z, z, z) == 1
+    # config-level errors are still reported for an empty batch
+    bad = M.MoeConfig.make(0, 128, 8, 2, 128, weight_bits=8)
+    assert lib.moe_grouped_ffn(ctypes.byref(bad), z, z, z, z, z, z, z, z, z, z, z, z, z, z, 0,
+                               z) == 1
+    plain = M.MoeConfig.make(0, 128, 8, 2, 128)
+    assert lib.moe_overflow_reroute(ctypes.byref(plain), z, z, z, z, z, z, z, z, 0, z) == 1
