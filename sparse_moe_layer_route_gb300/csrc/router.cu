@@ -286,7 +286,11 @@ __device__ __forceinline__ float key_score(uint32_t k) {
 // partial logits over the K slices in slice order, forms their selection scores, and keeps their
 // keys. Each of the k+1 picks, in (score desc, index asc) order, is the warp's largest key, then
 // the smallest expert index among the lanes holding that key; the owner marks it taken.
+// M >= m is the compiled bound on experts per lane (1, 2, 4 or 8): the per-expert loops are
+// unrolled to M rather than to the largest supported E, so small E runs no predicated-off work.
+template <int M>
 __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a) {
+  static_assert(M >= 1 && M <= kSelMaxPerLane, "experts per lane");
   __shared__ uint32_t gkey[kSelWarps][64];  // group-limited routing: group maxima
   __shared__ float gsc[kSelWarps][64];
   griddep_wait();
@@ -296,11 +300,11 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a)
   const bool gumbel = a.mode == MOE_ROUTE_GUMBEL;
   const int m = (a.E + 31) >> 5;
   const int e0 = lane * m;
-  float sc[kSelMaxPerLane];
-  uint32_t key[kSelMaxPerLane];
+  float sc[M];
+  uint32_t key[M];
   float maxabs = 0.f;
 #pragma unroll
-  for (int i = 0; i < kSelMaxPerLane; ++i) {
+  for (int i = 0; i < M; ++i) {
     sc[i] = -INFINITY;
     key[i] = 0u;
     const int e = e0 + i;
@@ -326,7 +330,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a)
   if (a.sfull != nullptr) {
     // the overflow re-route ranks every expert of a token: keep the scores and the row scale
 #pragma unroll
-    for (int i = 0; i < kSelMaxPerLane; ++i)
+    for (int i = 0; i < M; ++i)
       if (i < m && e0 + i < a.E) a.sfull[(size_t)t * a.E + e0 + i] = sc[i];
     if (lane == 0) a.maxl_out[t] = maxabs;
   }
@@ -337,7 +341,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a)
     for (int g = lane; g < a.G; g += 32) gkey[warp][g] = 0u;
     __syncwarp();
 #pragma unroll
-    for (int i = 0; i < kSelMaxPerLane; ++i)
+    for (int i = 0; i < M; ++i)
       if (i < m && e0 + i < a.E) atomicMax(&gkey[warp][(e0 + i) / gsz], key[i]);
     __syncwarp();
     for (int g = lane; g < a.G; g += 32) gsc[warp][g] = key_score(gkey[warp][g]);
@@ -347,7 +351,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a)
     sel = __shfl_sync(0xffffffffu, sel, 0);
     gmarg = __shfl_sync(0xffffffffu, gmarg, 0);
 #pragma unroll
-    for (int i = 0; i < kSelMaxPerLane; ++i)
+    for (int i = 0; i < M; ++i)
       if (i < m && e0 + i < a.E && !((sel >> ((e0 + i) / gsz)) & 1ull)) {
         sc[i] = -INFINITY;
         key[i] = score_key(-INFINITY);
@@ -358,7 +362,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a)
     bk = 0u;
     be = INT_MAX;
 #pragma unroll
-    for (int i = 0; i < kSelMaxPerLane; ++i)
+    for (int i = 0; i < M; ++i)
       if (i < m && key[i] > bk) {
         bk = key[i];
         be = e0 + i;
@@ -387,7 +391,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a)
       prev = s_j;
       if (W >= e0 && W < e0 + m) {
 #pragma unroll
-        for (int i = 0; i < kSelMaxPerLane; ++i)
+        for (int i = 0; i < M; ++i)
           if (e0 + i == W) key[i] = 0u;
         lane_best(bk, be);
       }
@@ -403,7 +407,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a)
     int mine = 0;
     if (!group_tie) {
 #pragma unroll
-      for (int i = 0; i < kSelMaxPerLane; ++i)
+      for (int i = 0; i < M; ++i)
         if (i < m && e0 + i < a.E && sc[i] >= sk - band) ++mine;
     }
     int before = mine;
@@ -424,7 +428,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a)
     }
     if (nc > 0) {
 #pragma unroll
-      for (int i = 0; i < kSelMaxPerLane; ++i)
+      for (int i = 0; i < M; ++i)
         if (i < m && e0 + i < a.E && sc[i] >= sk - band) rec[2 + before++] = e0 + i;
     }
   }
@@ -729,8 +733,16 @@ cudaError_t launch_router(const Shape& s, const uint16_t* x, const uint16_t* W_g
   a.G = s.G;
   a.Gk = s.Gk;
   a.tau = s.tau;
-  err = launch_k(select_kernel, dim3((s.T + kSelWarps - 1) / kSelWarps), dim3(kSelThreads), 0,
-                 st, a);
+  const int m = (s.E + 31) / 32;  // experts per lane
+  const dim3 sgrid((s.T + kSelWarps - 1) / kSelWarps), sblock(kSelThreads);
+  if (m <= 1)
+    err = launch_k(select_kernel<1>, sgrid, sblock, 0, st, a);
+  else if (m <= 2)
+    err = launch_k(select_kernel<2>, sgrid, sblock, 0, st, a);
+  else if (m <= 4)
+    err = launch_k(select_kernel<4>, sgrid, sblock, 0, st, a);
+  else
+    err = launch_k(select_kernel<8>, sgrid, sblock, 0, st, a);
   if (err != cudaSuccess) return err;
   const int rgrid = num_sms();  // one CTA per SM (its registers allow no second)
   return launch_k(refine_kernel, dim3(rgrid), dim3(kThreads), 0, st, x, (const uint16_t*)rs.wg_t,
