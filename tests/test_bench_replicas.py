@@ -53,3 +53,27 @@ def test_reference_arm_other_ranks_exit_without_output():
                         "--config", "tiny", "--steps", "3", "--warmup", "3"],
                        capture_output=True, text=True, env=env, timeout=300)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_reference_arm_line_follows_the_bench_contract():
+    """Rank 0 of the reference arm (the float64 oracle on the host cores) prints one JSON line
+    with the keys the bench contract names, its e2e equal to its own value with no copies."""
+    import json
+    import subprocess
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--config", "tiny", "--steps", "3", "--warmup", "3"],
+                       capture_output=True, text=True, env=env, timeout=300)
+    assert r.returncode == 0, r.stderr
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    j = json.loads(lines[0])
+    assert j["impl"] == "reference" and j["n_gpus"] == 1 and j["steps"] == 3
+    assert j["warmup"] >= 3 and j["higher_is_better"] is True and j["scaling"] == "weak"
+    assert j["unit"] == "tokens/s" and j["value"] > 0 and j["ms_per_step"] > 0
+    assert j["config"]["workload"].startswith("tiny") and j["config"]["T"] == 128
+    cb = j["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"] and cb["value"] == j["value"]
+    e2e = j["e2e"]
+    assert e2e["value"] == j["value"] and e2e["unit"] == j["unit"]
+    assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
