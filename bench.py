@@ -8,10 +8,11 @@ A step is one moe_layer_forward call over one batch of the workload (inputs resi
 Between timed steps a 256 MB buffer is written to flush L2. Each step is timed with CUDA events on
 the launching stream; the K steps are bracketed by a barrier and a device synchronize.
 `e2e` is the same metric through moe_layer_forward_host (pinned host x in, host out, copies in
-the timed region), run as a serving loop buffers it (calls rotate over three streams and three workspaces, so the
-other calls' copies overlap one call's compute; events around the whole loop);
-the one-call-at-a-time latency is reported beside it as `e2e.serial`. `roofline` is for the step's dominant kernel, timed live with events recorded
-between the layer's phases (moe_layer_forward_profiled). `cpu_baseline` times the fp64 CPU
+the timed region), run as a serving loop runs it: calls rotate over three streams and three
+workspaces, so the other calls' copies overlap one call's compute, and events bracket the whole
+loop. The one-call-at-a-time latency is reported beside it as `e2e.serial`. `roofline` is for the
+step's dominant kernel, timed live with events recorded between the layer's phases
+(moe_layer_forward_profiled). `cpu_baseline` times the fp64 CPU
 oracle on a bounded sample of the same workload. With N > 1 (torchrun) every rank runs an
 independent replica of the layer (the layer has no cross-token exchange): value = N*T / max time.
 `--impl reference` times the oracle alone (rank 0; the other ranks exit) on the same workload.
@@ -36,10 +37,8 @@ METRIC = "MoE-layer tokens/s (bf16, 1 GB300) and achieved fraction of roofline"
 DEFAULT_CONFIG = "fine_grained"
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# DRAM bytes (read + write) per launch from one ncu capture of the current kernel, by
-# (workload, phase): profiles/grouped_gemm_fine_grained.md. Re-capture after changing the kernel.
 # (workload, phase) -> DRAM bytes read + written per launch, from one ncu capture of the current
-# kernel (profiles/grouped_gemm_fine_grained.md)
+# kernel (profiles/grouped_gemm_fine_grained.md). Re-capture after changing the kernel.
 NCU_TRAFFIC = {("fine_grained", "gate_up_gemm"): (879.400448e6 + 67.677184e6),
                ("fine_grained", "down_gemm"): (473.339648e6 + 95.139840e6)}
 # captured on the 32-expert decode shape (31 routed experts touched + the shared one); every
@@ -63,7 +62,7 @@ def launches_per_step(cfg):
     """Kernels of one layer call: router (weight prep, GEMM, selection, exact near-tie pass),
     dispatch (histogram with the scan and the tile list in its last CTA, scatter), gather, the two
     grouped GEMMs (or the two quantized FFN passes) and the combine; the overflow re-route adds its
-    three kernels and a second dispatch."""
+    four kernels and a second dispatch."""
     n = 10
     if getattr(cfg, "reroute", False) and cfg.capacity_factor > 0:
         n += 4 + 2
