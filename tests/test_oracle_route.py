@@ -160,6 +160,23 @@ def brute_group_topk(s_row, k, n_groups, g):
     return brute_topk(masked, k)
 
 
+def brute_group_margin(s_row, n_groups, g):
+    """The group decision's gap by enumeration: over every way of keeping g groups such that no
+    dropped group scores above a kept one, the weakest kept group score minus the strongest
+    dropped one (inf when every group is kept)."""
+    if g >= n_groups:
+        return math.inf
+    size = len(s_row) // n_groups
+    gs = [max(s_row[i * size:(i + 1) * size]) for i in range(n_groups)]
+    gaps = []
+    for sub in itertools.combinations(range(n_groups), g):
+        rest = [x for x in range(n_groups) if x not in sub]
+        lo, hi = min(gs[a] for a in sub), max(gs[b] for b in rest)
+        if lo >= hi:
+            gaps.append(lo - hi)
+    return max(gaps)
+
+
 def test_group_limited_fixture():
     from golden_io import read_kv
     g = read_kv("group_limited.txt")
@@ -168,6 +185,20 @@ def test_group_limited_fixture():
         assert O.topk(O.group_limit(s, 4, gk), 2)[0].tolist() == g[key]
     s2 = np.array([[0.5, 0.0, 0.5, 0.4, 0.1, 0.1, 0.2, 0.2]])
     assert O.topk(O.group_limit(s2, 4, 1), 2)[0].tolist() == g["tie1"]
+
+
+def test_group_margin_fixture():
+    """The group decision's gap, worked by hand: the gaps between adjacent sorted group scores
+    all differ, so indexing the wrong pair, or scoring a group by a member other than its
+    largest, fails."""
+    from golden_io import read_kv
+    g = read_kv("group_limited.txt")
+    s3 = np.array([[0.7, -0.2, 0.1, 0.65, 1.0, 0.3, -0.5, 0.4]])
+    for gk, key in ((1, "m1"), (2, "m2"), (3, "m3")):
+        np.testing.assert_allclose(O.group_margin(s3, 4, gk), [g[key]], rtol=0, atol=1e-12)
+    s2 = np.array([[0.5, 0.0, 0.5, 0.4, 0.1, 0.1, 0.2, 0.2]])
+    np.testing.assert_allclose(O.group_margin(s2, 4, 1), [g["mtie1"]], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(O.group_margin(s2, 4, 2), [g["mtie2"]], rtol=0, atol=1e-12)
 
 
 def test_group_limited_bruteforce():
@@ -180,8 +211,10 @@ def test_group_limited_bruteforce():
         k = int(rng.integers(1, g * size + 1))
         s = rng.integers(-2, 3, size=(5, E)).astype(np.float64)
         got = O.topk(O.group_limit(s, n_groups, g), k)
+        marg = O.group_margin(s, n_groups, g)
         for t in range(5):
             assert list(got[t]) == brute_group_topk(list(s[t]), k, n_groups, g)
+            assert marg[t] == brute_group_margin(list(s[t]), n_groups, g)
 
 
 def test_group_limited_all_groups_is_plain_topk():
