@@ -169,6 +169,9 @@ typedef struct {
   /* Quantized experts, used instead of the bf16 ones when moe_config.weight_bits is 4 or 8
    * (the bf16 expert pointers may then be NULL). */
   const moe_qweights* quant;
+  /* Optional W_g transposed, [E, d] bf16, written once by moe_prepare_router (16-byte aligned).
+   * NULL: every call transposes W_g into the workspace first (one extra kernel per call). */
+  const uint16_t* W_g_t;
 } moe_weights;
 
 /* Optional copies of the routing results written by moe_layer_forward (any member may be
@@ -194,15 +197,25 @@ moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes);
  * call. */
 moe_status moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* One-time weight preparation for the router: W_g_t[e, j] = W_g[j, e] (W_g [d, E] bf16 ->
+ * W_g_t [E, d] bf16), each expert's router weights contiguous. The router's tensor-core GEMM
+ * reads it as its operand and the exact dot products of near-tie tokens read it row by row.
+ * Requires 1 <= E <= 256 and d a multiple of 64 (else MOE_ERR_UNSUPPORTED); W_g_t 16-byte
+ * aligned. Asynchronous on stream. */
+moe_status moe_prepare_router(int32_t d, int32_t E, const uint16_t* W_g, uint16_t* W_g_t,
+                              moe_stream_t stream);
+
 /* Steps 1-4. Router: logits in fp32 (per-K-slice partial sums pass through the workspace; the
  * full logits exist only in the selection kernel's registers), selection score, top-k, gates.
- *   x [T, d] bf16, W_g [d, E] bf16, expert_bias [E] fp32 (BIAS_SELECT; else may be NULL),
- *   gumbel_u [T, E] fp32 (GUMBEL; else may be NULL).
+ *   x [T, d] bf16, W_g [d, E] bf16, W_g_t [E, d] bf16 from moe_prepare_router (NULL: W_g is
+ *   transposed into the workspace by this call), expert_bias [E] fp32 (BIAS_SELECT; else may be
+ *   NULL), gumbel_u [T, E] fp32 (GUMBEL; else may be NULL).
  *   Writes topk_idx [T, k] int32 (descending score, ties to the lower index) and
  *   topk_w [T, k] fp32 (gates, summing to 1 per token). */
 moe_status moe_route(const moe_config* cfg, const uint16_t* x, const uint16_t* W_g,
-                     const float* expert_bias, const float* gumbel_u, int32_t* topk_idx,
-                     float* topk_w, void* ws, size_t ws_bytes, moe_stream_t stream);
+                     const uint16_t* W_g_t, const float* expert_bias, const float* gumbel_u,
+                     int32_t* topk_idx, float* topk_w, void* ws, size_t ws_bytes,
+                     moe_stream_t stream);
 
 /* Step 5. Dispatch ("参数规模与稀疏激活的真相拆解", §3.2 for the capacity rule).
  *   topk_idx [T, k] int32 in [0, E) (an index outside it sets MOE_DEVFAULT_BAD_EXPERT_INDEX and
@@ -219,14 +232,15 @@ moe_status moe_permute(const moe_config* cfg, const int32_t* topk_idx, int32_t* 
 /* Level-2 overflow re-route (cfg->overflow_reroute = 1; see moe_config). Must follow moe_route and
  * moe_permute on the same workspace and config: it reads the selection scores that moe_route kept
  * in the workspace, and the Level-1 counts [E] and slot_pos [T * k] that moe_permute wrote.
- *   x [T, d] bf16 and expert_bias / gumbel_u as given to moe_route (the exact re-ordering of
- *   experts whose tensor-core scores are too close to call recomputes their logits).
+ *   x [T, d] bf16, W_g_t and expert_bias / gumbel_u as given to moe_route (the exact
+ *   re-ordering of experts whose tensor-core scores are too close to call recomputes their
+ *   logits; with W_g_t NULL it reads the transposed copy moe_route left in the workspace).
  *   topk_idx [T, k] is updated in place (dropped slots get their new expert), topk_w [T, k] is
  *   rewritten for the re-routed tokens. Run moe_permute again on the updated topk_idx for the
  *   final dispatch. Returns MOE_ERR_INVALID_ARG when cfg->overflow_reroute is 0, and does nothing
  *   when the config has no capacity limit. The proposal rounds run as one cooperative kernel whose
  *   grid barriers wait at most 2 s each (MOE_DEVFAULT_PIPELINE_TIMEOUT on expiry). */
-moe_status moe_overflow_reroute(const moe_config* cfg, const uint16_t* x,
+moe_status moe_overflow_reroute(const moe_config* cfg, const uint16_t* x, const uint16_t* W_g_t,
                                 const float* expert_bias, const float* gumbel_u,
                                 int32_t* topk_idx, float* topk_w, const int32_t* counts,
                                 const int32_t* slot_pos, void* ws, size_t ws_bytes,

@@ -18,7 +18,8 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 ROUTE_PLAIN, ROUTE_BIAS_SELECT, ROUTE_GUMBEL = 0, 1, 2
 DEVFAULT_BAD_EXPERT_INDEX, DEVFAULT_PIPELINE_TIMEOUT, DEVFAULT_BAD_TILE = 0x1, 0x2, 0x4
 
-EXPORTS = ("moe_workspace_size", "moe_workspace_init", "moe_route", "moe_permute",
+EXPORTS = ("moe_workspace_size", "moe_workspace_init", "moe_prepare_router", "moe_route",
+           "moe_permute",
            "moe_permute_noalloc", "moe_overflow_reroute",
            "moe_grouped_ffn", "moe_grouped_ffn_quantized", "moe_quantize_weights", "moe_combine", "moe_layer_forward", "moe_layer_forward_profiled",
            "moe_layer_forward_host", "moe_pack_f16", "moe_bias_update", "moe_device_status",
@@ -69,7 +70,7 @@ class MoeWeights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("W_g", "expert_bias", "W_gate", "W_up", "W_down", "Wsh_gate", "Wsh_up",
                  "Wsh_down", "W_down_f16", "Wsh_down_f16")] + \
-        [("quant", ctypes.POINTER(MoeQWeights))]
+        [("quant", ctypes.POINTER(MoeQWeights)), ("W_g_t", ctypes.c_void_p)]
 
 
 class MoeRouteOut(ctypes.Structure):
@@ -92,10 +93,11 @@ def lib():
         cfgp = ctypes.POINTER(MoeConfig)
         L.moe_workspace_size.argtypes = [cfgp, ctypes.POINTER(ctypes.c_size_t)]
         L.moe_workspace_init.argtypes = [P, S, P]
-        L.moe_route.argtypes = [cfgp, P, P, P, P, P, P, P, S, P]
+        L.moe_prepare_router.argtypes = [ctypes.c_int32, ctypes.c_int32, P, P, P]
+        L.moe_route.argtypes = [cfgp, P, P, P, P, P, P, P, P, S, P]
         L.moe_permute.argtypes = [cfgp, P, P, P, P, P, P, S, P]
         L.moe_permute_noalloc.argtypes = [cfgp, P, P, P, P, P, P, P]
-        L.moe_overflow_reroute.argtypes = [cfgp, P, P, P, P, P, P, P, P, S, P]
+        L.moe_overflow_reroute.argtypes = [cfgp, P, P, P, P, P, P, P, P, P, S, P]
         i32 = ctypes.c_int32
         L.moe_quantize_weights.argtypes = [i32, i32, i32, i32, P, P, P, P, P]
         L.moe_grouped_ffn_quantized.argtypes = [cfgp, P, P, P, P, ctypes.POINTER(MoeQWeights),
@@ -163,8 +165,19 @@ def workspace_init(ws, stream=None):
     _check(lib().moe_workspace_init(_ptr(ws), ws.numel(), _stream(stream)), "moe_workspace_init")
 
 
-def route(cfg, x, W_g, expert_bias, gumbel_u, topk_idx, topk_w, ws, stream=None):
-    _check(lib().moe_route(ctypes.byref(cfg), _ptr(x), _ptr(W_g), _ptr(expert_bias),
+def prepare_router(W_g, W_g_t=None, stream=None):
+    """W_g [d, E] bf16 transposed into W_g_t [E, d] (a new tensor unless given); one-time."""
+    import torch
+    d, E = W_g.shape
+    if W_g_t is None:
+        W_g_t = torch.empty((E, d), dtype=W_g.dtype, device=W_g.device)
+    _check(lib().moe_prepare_router(d, E, _ptr(W_g), _ptr(W_g_t), _stream(stream)),
+           "moe_prepare_router")
+    return W_g_t
+
+
+def route(cfg, x, W_g, expert_bias, gumbel_u, topk_idx, topk_w, ws, stream=None, W_g_t=None):
+    _check(lib().moe_route(ctypes.byref(cfg), _ptr(x), _ptr(W_g), _ptr(W_g_t), _ptr(expert_bias),
                            _ptr(gumbel_u), _ptr(topk_idx), _ptr(topk_w), _ptr(ws), ws.numel(),
                            _stream(stream)), "moe_route")
 
@@ -189,8 +202,8 @@ def permute_noalloc(cfg, topk_idx, counts, offsets, perm_slot, slot_pos, fault_b
 
 
 def overflow_reroute(cfg, x, expert_bias, gumbel_u, topk_idx, topk_w, counts, slot_pos, ws,
-                     stream=None):
-    _check(lib().moe_overflow_reroute(ctypes.byref(cfg), _ptr(x), _ptr(expert_bias),
+                     stream=None, W_g_t=None):
+    _check(lib().moe_overflow_reroute(ctypes.byref(cfg), _ptr(x), _ptr(W_g_t), _ptr(expert_bias),
                                       _ptr(gumbel_u), _ptr(topk_idx), _ptr(topk_w), _ptr(counts),
                                       _ptr(slot_pos), _ptr(ws), ws.numel(), _stream(stream)),
            "moe_overflow_reroute")
@@ -263,9 +276,10 @@ def combine(cfg, y_slot, slot_pos, out, ws, stream=None):
 
 def make_weights(W_g, expert_bias, W_gate, W_up, W_down, Wsh_gate=None, Wsh_up=None,
                  Wsh_down=None, W_down_f16=None, Wsh_down_f16=None,
-                 quant: MoeQWeights | None = None) -> MoeWeights:
+                 quant: MoeQWeights | None = None, W_g_t=None) -> MoeWeights:
     w = MoeWeights(*[_ptr(t) for t in (W_g, expert_bias, W_gate, W_up, W_down, Wsh_gate,
                                         Wsh_up, Wsh_down, W_down_f16, Wsh_down_f16)])
+    w.W_g_t = _ptr(W_g_t)
     if quant is not None:
         w.quant = ctypes.pointer(quant)
         w._quant_ref = quant          # keep the struct alive with the weights

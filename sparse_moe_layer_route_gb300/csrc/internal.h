@@ -55,7 +55,7 @@ struct Meta {
 // Offsets of every buffer carved from the caller's workspace (bytes, 256-aligned).
 struct WsLayout {
   size_t status, meta, topk_idx, topk_w, counts, offsets, perm_slot, slot_pos;
-  size_t blk_hist, blk_base, tiles, wg_pad, wg_t, rpart, rrec, xp, h, y, x_stage,
+  size_t blk_hist, blk_base, tiles, wg_t, rpart, rrec, xp, h, y, x_stage,
       u_stage, out_stage;
   size_t x16, sbx, tail_acc, tail_ticket;  // quantized experts only
   // overflow re-route (zero-sized unless enabled)
@@ -73,8 +73,7 @@ constexpr int kRouterMaxCand = 16;
 // [2, 2 + n) the candidate experts in index order (n <= kRouterMaxCand).
 constexpr int kRouterRecInts = 32;
 struct RouterScratch {
-  uint16_t* wg_pad;  // d x round_up(E, 64) bf16, used when E is not a multiple of 64
-  uint16_t* wg_t;    // E x d bf16: W_g transposed (exact near-tie pass)
+  uint16_t* wg_t;    // E x d bf16: W_g transposed for this call when the caller has none
   float* part;       // [splits, T, round_up(E, 64)] fp32 partial logits
   int32_t* rrec;     // [T][kRouterRecInts] near-tie records, appended by the selection
   int* rcount;       // their number (cleared by the router GEMM at the start of each call)
@@ -83,9 +82,15 @@ struct RouterScratch {
 };
 // K slices of the router GEMM for T tokens and hidden size d.
 int router_splits(int T, int d);
+// W_g_t: W_g transposed ([E, d], from moe_prepare_router), or nullptr to transpose into
+// rs.wg_t first.
 cudaError_t launch_router(const Shape& s, const uint16_t* x, const uint16_t* W_g,
-                          const float* bias, const float* u, int32_t* topk_idx, float* topk_w,
-                          const RouterScratch& rs, int* status, cudaStream_t st);
+                          const uint16_t* W_g_t, const float* bias, const float* u,
+                          int32_t* topk_idx, float* topk_w, const RouterScratch& rs, int* status,
+                          cudaStream_t st);
+// W_g_t[e, j] = W_g[j, e] for W_g [d, E].
+cudaError_t launch_router_transpose(int d, int E, const uint16_t* W_g, uint16_t* W_g_t,
+                                    cudaStream_t st);
 
 // Level-2 overflow re-route (reroute.cu). Per-token and per-expert state lives in the workspace;
 // the preceding router call left the selection scores (sfull), the row scales (maxl) and the

@@ -90,7 +90,6 @@ WsLayout ws_layout(const Shape& s) {
   L.blk_hist = take(sizeof(int32_t) * (size_t)s.n_pblk * s.E);
   L.blk_base = take(sizeof(int32_t) * (size_t)s.n_pblk * s.E);
   L.tiles = take(sizeof(TileEntry) * (size_t)s.max_tiles);
-  L.wg_pad = take(2ull * s.d * ((s.E + 63) / 64 * 64));
   L.wg_t = take(2ull * s.d * s.E);
   L.rpart = take(4ull * router_splits(s.T, s.d) * s.T * ((s.E + 63) / 64 * 64));
   L.rrec = take(sizeof(int32_t) * (size_t)s.T * kRouterRecInts);
@@ -187,10 +186,9 @@ moe_status clear_dispatch(int E, int32_t* counts, int32_t* offsets, cudaStream_t
 }
 
 moe_status route_impl(const Shape& s, const WsLayout& L, void* ws, const uint16_t* x,
-                      const uint16_t* W_g, const float* bias, const float* u, int32_t* idx,
-                      float* w, cudaStream_t st) {
+                      const uint16_t* W_g, const uint16_t* W_g_t, const float* bias,
+                      const float* u, int32_t* idx, float* w, cudaStream_t st) {
   RouterScratch rs;
-  rs.wg_pad = at<uint16_t>(ws, L.wg_pad);
   rs.wg_t = at<uint16_t>(ws, L.wg_t);
   rs.part = at<float>(ws, L.rpart);
   rs.rrec = at<int32_t>(ws, L.rrec);
@@ -198,7 +196,8 @@ moe_status route_impl(const Shape& s, const WsLayout& L, void* ws, const uint16_
   rs.rcount = &meta->refine_count;
   rs.sfull = s.reroute ? at<float>(ws, L.sfull) : nullptr;
   rs.maxl = s.reroute ? at<float>(ws, L.maxl) : nullptr;
-  return cuda_status(launch_router(s, x, W_g, bias, u, idx, w, rs, at<int>(ws, L.status), st));
+  return cuda_status(
+      launch_router(s, x, W_g, W_g_t, bias, u, idx, w, rs, at<int>(ws, L.status), st));
 }
 
 // with_tiles: the FFN follows, so the dispatch also builds its row-tile list
@@ -213,12 +212,15 @@ moe_status permute_impl(const Shape& s, const WsLayout& L, void* ws, const int32
                                     with_tiles ? meta : nullptr, st));
 }
 
+// W_g_t: the prepared transpose given to the router, or nullptr when the router made its own in
+// the workspace
 moe_status reroute_impl(const Shape& s, const WsLayout& L, void* ws, const uint16_t* x,
-                        const float* bias, const float* u, int32_t* idx, float* w,
-                        const int32_t* counts, const int32_t* slot_pos, cudaStream_t st) {
+                        const uint16_t* W_g_t, const float* bias, const float* u, int32_t* idx,
+                        float* w, const int32_t* counts, const int32_t* slot_pos,
+                        cudaStream_t st) {
   RerouteArgs a;
   a.x = x;
-  a.WgT = at<uint16_t>(ws, L.wg_t);
+  a.WgT = W_g_t != nullptr ? W_g_t : at<uint16_t>(ws, L.wg_t);
   a.bias = bias;
   a.u = u;
   a.sfull = at<float>(ws, L.sfull);
@@ -344,6 +346,7 @@ moe_status layer_impl(const moe_config* cfg, const moe_weights* w, const uint16_
   }
   if (!w || !x || !out || !w->W_g) return MOE_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(x) % 16 != 0) return MOE_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(w->W_g_t) % 16 != 0) return MOE_ERR_INVALID_ARG;
   const bool quant = cfg->weight_bits != 0;
   if (quant) {
     if (!qweights_ok(cfg, w->quant)) return MOE_ERR_INVALID_ARG;
@@ -366,7 +369,8 @@ moe_status layer_impl(const moe_config* cfg, const moe_weights* w, const uint16_
   int32_t* perm_slot = (ro && ro->perm_slot) ? ro->perm_slot : at<int32_t>(ws, L.perm_slot);
   int32_t* slot_pos = (ro && ro->slot_pos) ? ro->slot_pos : at<int32_t>(ws, L.slot_pos);
   if (!mark(0)) return MOE_ERR_CUDA;
-  if ((r = route_impl(s, L, ws, x, w->W_g, w->expert_bias, gumbel_u, idx, gw, st)) != MOE_OK)
+  if ((r = route_impl(s, L, ws, x, w->W_g, w->W_g_t, w->expert_bias, gumbel_u, idx, gw, st)) !=
+      MOE_OK)
     return r;
   if (!mark(1)) return MOE_ERR_CUDA;
   // the last dispatch also builds the FFN's row-tile list
@@ -375,8 +379,8 @@ moe_status layer_impl(const moe_config* cfg, const moe_weights* w, const uint16_
     return r;
   if (s.reroute) {
     // Level 2: dropped slots move to the best expert with room, then the final dispatch
-    if ((r = reroute_impl(s, L, ws, x, w->expert_bias, gumbel_u, idx, gw, counts, slot_pos,
-                          st)) != MOE_OK)
+    if ((r = reroute_impl(s, L, ws, x, w->W_g_t, w->expert_bias, gumbel_u, idx, gw, counts,
+                          slot_pos, st)) != MOE_OK)
       return r;
     if ((r = permute_impl(s, L, ws, idx, counts, offsets, perm_slot, slot_pos, st, true)) !=
         MOE_OK)
@@ -418,20 +422,30 @@ moe_status moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream) {
   return cuda_status(cudaMemsetAsync(ws, 0, 512, (cudaStream_t)stream));
 }
 
+moe_status moe_prepare_router(int32_t d, int32_t E, const uint16_t* W_g, uint16_t* W_g_t,
+                              moe_stream_t stream) {
+  if (d < 1 || E < 1 || !W_g || !W_g_t) return MOE_ERR_INVALID_ARG;
+  if (E > 256 || d % 64 != 0) return MOE_ERR_UNSUPPORTED;
+  if (reinterpret_cast<uintptr_t>(W_g_t) % 16 != 0) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_router_transpose(d, E, W_g, W_g_t, (cudaStream_t)stream));
+}
+
 moe_status moe_route(const moe_config* cfg, const uint16_t* x, const uint16_t* W_g,
-                     const float* expert_bias, const float* gumbel_u, int32_t* topk_idx,
-                     float* topk_w, void* ws, size_t ws_bytes, moe_stream_t stream) {
+                     const uint16_t* W_g_t, const float* expert_bias, const float* gumbel_u,
+                     int32_t* topk_idx, float* topk_w, void* ws, size_t ws_bytes,
+                     moe_stream_t stream) {
   moe_status r = check_cfg(cfg);
   if (r != MOE_OK) return r;
   if (cfg->T == 0) return MOE_OK;
   if (!x || !W_g || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(x) % 16 != 0) return MOE_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(W_g_t) % 16 != 0) return MOE_ERR_INVALID_ARG;
   if (cfg->mode == MOE_ROUTE_BIAS_SELECT && !expert_bias) return MOE_ERR_INVALID_ARG;
   if (cfg->mode == MOE_ROUTE_GUMBEL && !gumbel_u) return MOE_ERR_INVALID_ARG;
   if ((r = check_ws(cfg, ws, ws_bytes)) != MOE_OK) return r;
   const Shape s = make_shape(*cfg);
   const WsLayout L = ws_layout(s);
-  return route_impl(s, L, ws, x, W_g, expert_bias, gumbel_u, topk_idx, topk_w,
+  return route_impl(s, L, ws, x, W_g, W_g_t, expert_bias, gumbel_u, topk_idx, topk_w,
                     (cudaStream_t)stream);
 }
 
@@ -452,7 +466,7 @@ moe_status moe_permute(const moe_config* cfg, const int32_t* topk_idx, int32_t* 
                       (cudaStream_t)stream);
 }
 
-moe_status moe_overflow_reroute(const moe_config* cfg, const uint16_t* x,
+moe_status moe_overflow_reroute(const moe_config* cfg, const uint16_t* x, const uint16_t* W_g_t,
                                 const float* expert_bias, const float* gumbel_u,
                                 int32_t* topk_idx, float* topk_w, const int32_t* counts,
                                 const int32_t* slot_pos, void* ws, size_t ws_bytes,
@@ -463,14 +477,15 @@ moe_status moe_overflow_reroute(const moe_config* cfg, const uint16_t* x,
   if (cfg->T == 0) return MOE_OK;
   if (!x || !topk_idx || !topk_w || !counts || !slot_pos) return MOE_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(x) % 16 != 0) return MOE_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(W_g_t) % 16 != 0) return MOE_ERR_INVALID_ARG;
   if (cfg->mode == MOE_ROUTE_BIAS_SELECT && !expert_bias) return MOE_ERR_INVALID_ARG;
   if (cfg->mode == MOE_ROUTE_GUMBEL && !gumbel_u) return MOE_ERR_INVALID_ARG;
   if ((r = check_ws(cfg, ws, ws_bytes)) != MOE_OK) return r;
   const Shape s = make_shape(*cfg);
   if (!s.reroute) return MOE_OK;  // no capacity limit: nothing can overflow
   const WsLayout L = ws_layout(s);
-  return reroute_impl(s, L, ws, x, expert_bias, gumbel_u, topk_idx, topk_w, counts, slot_pos,
-                      (cudaStream_t)stream);
+  return reroute_impl(s, L, ws, x, W_g_t, expert_bias, gumbel_u, topk_idx, topk_w, counts,
+                      slot_pos, (cudaStream_t)stream);
 }
 
 moe_status moe_quantize_weights(int32_t bits, int32_t n_mat, int32_t K, int32_t N,

@@ -6,12 +6,15 @@
 
 namespace moe {
 
-// Half-width of the band around a score gap inside which the tensor-core logits could misorder
-// two experts: the tensor core's fp32 accumulation differs from an exactly rounded dot product by
-// up to ~4e-5 on unit-scale logits at d = 7168 (measured); the band is about 6x that, scaled
-// with sqrt(d) and with the row's largest |logit|.
+// Half-width of the band around a score gap inside which the router GEMM's logits could misorder
+// two experts. Those logits (a fresh tensor-core accumulator per 64-deep K block, the blocks
+// added in fp32) differ from the exactly rounded dot product by at most 7.9e-7 x max(1, |largest
+// logit of the row|) at d = 7168 (measured against float64 logits on 16384 x 7168 x 128,
+// 8192 x 4096 x 16, 4096 x 2048 x 64 and 64 x 7168 x 128), so a logit difference by at most
+// about 1.6e-6 on that scale; the band is about 9x that, scaled with sqrt(d) and with the row's
+// largest |logit|.
 __device__ __forceinline__ float router_band(int d, float max_abs_logit) {
-  return 2.5e-4f * sqrtf((float)d * (1.0f / 7168.0f)) * fmaxf(1.0f, max_abs_logit);
+  return 1.5e-5f * sqrtf((float)d * (1.0f / 7168.0f)) * fmaxf(1.0f, max_abs_logit);
 }
 
 // Selection score of one expert: the logit (PLAIN), logit + bias (BIAS_SELECT), or

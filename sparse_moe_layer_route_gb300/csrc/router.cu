@@ -9,28 +9,33 @@
 // (logits - log(-log u)) / tau from "GPT-4 Has 1.8 Trillion Parameters. It Uses 2% of Them Per
 // Token", §3.1 门控网络.
 //
-// Three kernels after the per-call weight preparation (prep_router_kernel):
+// Three kernels, after the one-time transpose of W_g (transpose_router_kernel, through
+// moe_prepare_router, or per call when the caller has no transposed copy):
 //  * router_gemm_kernel: CTA (row tile of 128 tokens, K slice). Warp 0 streams x tiles [128 x 64]
-//    (K-major) and W_g chunks [64 x 64] (expert-major, i.e. N-major) with TMA; warp 1 issues
-//    tcgen05.mma (M=128, N=E rounded up to 64, K=16) into TMEM; warps 4-7 write the fp32 partial
-//    logits of the slice. Splitting K fills the GPU when T is small (one row tile at decode).
+//    and W_g^T tiles [E rounded up to 64 x 64] (both K-major) with TMA; warp 1 issues tcgen05.mma
+//    (M=128, N=E rounded up to 64, K=16) into TMEM, one fresh accumulator per 64-deep K block;
+//    warps 4-11 add the blocks in fp32 registers and write the slice's partial logits. Splitting
+//    K fills the GPU when T is small (one row tile at decode).
 //  * select_kernel: one warp per token. The K-slice partials summed in slice order, selection
 //    scores, top-(k+1) by k+1 warp-wide key reductions (largest key, then the lowest expert index
 //    holding it), softmax gates and the near-tie test.
 //  * refine_kernel: the exact re-decision of the near-tie tokens (below).
 //
-// Exactness. The tensor core's fp32 accumulation differs from an exactly rounded dot product by
-// up to ~4e-5 on unit-scale logits at d = 7168 (measured), which is above the 1e-5 near-tie
-// margin of the parity contract. So a token whose top-(k+1) scores have an adjacent gap below a
-// conservative band (router_band: 2.5e-4 x sqrt(d / 7168) x max(1, |largest logit of the row|),
-// about 6x the largest measured error) is flagged together with its candidate experts: every
-// expert whose tensor-core score lies within the band of the k-th score (only those can be in
-// the exact top-k), or all experts when there are more than 16 of them or the group decision of
-// group-limited routing is itself that close. refine_kernel recomputes the candidates' logits as
-// plain fp32 dot products (error ~1e-7) and re-decides the token's top-k and gates. Tokens outside
-// the band cannot change their selection or order under the tensor-core error. Flagged tokens are
-// appended to a list (order irrelevant: each token is re-decided on its own) and spread over all
-// refine CTAs, a whole CTA per token, which keeps the pass short however the flags cluster.
+// Exactness. The logits differ from exactly rounded dot products by at most 7.9e-7 x max(1,
+// |largest logit of the row|) at d = 7168 (measured; see router_gemm_kernel for why each K block
+// gets its own accumulator), so the gates, a softmax over the selected logits, stay within 1e-5
+// of exact. An order decided on a score gap below that error could still differ from the exact
+// one, and the parity contract exempts only gaps below 1e-5. So a token whose top-(k+1) scores
+// have an adjacent gap below a band (router_band: 1.5e-5 x sqrt(d / 7168) x max(1, |largest
+// logit of the row|), about 9x the largest measured error of a logit difference) is flagged
+// together with its candidate experts: every expert whose score lies within the band of the
+// k-th score (only those can be in the exact top-k), or all experts when there are more than 16
+// of them or the group decision of group-limited routing is itself that close. refine_kernel
+// recomputes the candidates' logits as plain fp32 dot products (error ~1e-7) and re-decides the
+// token's top-k and gates. Tokens outside the band cannot change their selection or order under
+// the GEMM's error. Flagged tokens are appended to a list (order irrelevant: each token is
+// re-decided on its own) and spread over all refine CTAs, a whole CTA per token, which keeps the
+// pass short however the flags cluster.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <climits>
@@ -44,11 +49,11 @@
 namespace moe {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 256;      // selection-side kernels
+constexpr int kGemmThreads = 384;  // router GEMM: warps 0 TMA, 1 MMA, 2 TMEM, 4-11 epilogue
 constexpr int kBM = 128;
 constexpr int kBK = 64;
 constexpr int kABytes = kBM * kBK * 2;   // 16 KB
-constexpr int kChunkBytes = kBK * 64 * 2;  // 8 KB: 64 k-rows x 64 experts
 constexpr int kMaxK = 8;
 constexpr int kList = kMaxK + 1;  // top-(k+1) list: the (k+1)-th score bounds the selection gap
 constexpr int kMaxCand = 16;      // candidate experts recorded per near-tie token
@@ -56,23 +61,38 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 template <int NCH>
 struct RCfg {
-  static constexpr int EP = 64 * NCH;  // MMA N
-  static constexpr int kStageBytes = kABytes + NCH * kChunkBytes;
+  static constexpr int EP = 64 * NCH;                  // MMA N (experts rounded up to 64)
+  static constexpr int kBBytes = EP * kBK * 2;         // W_g^T rows [EP experts x 64 k]
+  static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kStages = (192 * 1024 / kStageBytes) > 8 ? 8 : (192 * 1024 / kStageBytes);
-  static constexpr int kTmemCols = EP <= 64 ? 64 : (EP <= 128 ? 128 : 256);
+  // one fresh accumulator per K block; the epilogue adds each into fp32 registers while the
+  // next blocks accumulate in the other buffers
+  static constexpr int kNAcc = EP <= 128 ? 4 : 2;
+  static constexpr int kTmemCols = kNAcc * EP <= 256 ? 256 : 512;
+  static constexpr int kHalf = EP / 2;                 // columns per epilogue thread
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 256;
 };
 
 // Partial logits of one K slice: part[split][t][0, EP) (fp32; columns >= E are zero).
+//
+// Accumulation. tcgen05.mma adds its products into the fp32 accumulator after aligning them
+// to the accumulator's exponent, and the bits shifted out are lost; summed over the d/16 MMAs of
+// a long dot product against a growing accumulator this drifts by up to ~4e-5 on unit-scale
+// logits at d = 7168 (measured). So every 64-deep K block starts from a zero accumulator (its
+// partial sum stays small, and so does that loss), and the epilogue adds the blocks in K order
+// in fp32 registers with round-to-nearest adds. Four (EP <= 128) or two accumulators rotate so
+// the MMAs of later blocks run while the epilogue reads earlier ones.
 template <int NCH>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kGemmThreads, 1)
     router_gemm_kernel(const __grid_constant__ CUtensorMap tmX,
                        const __grid_constant__ CUtensorMap tmW, float* __restrict__ part, int T,
-                       int kb_per_split, int k_blocks, int* status, int* rcount,
-                       int wait_at_end) {
+                       int kb_per_split, int k_blocks, int* status, int* rcount) {
   using C = RCfg<NCH>;
   constexpr int kStages = C::kStages;
-  constexpr uint32_t IDESC = ptx::idesc_f16kind_f32(kBM, C::EP, 0, 1, 1);
+  constexpr int NACC = C::kNAcc;
+  constexpr int HALF = C::kHalf;
+  // A = x rows (K-major), B = W_g^T rows (K-major): both 128-byte swizzled [rows][64 k]
+  constexpr uint32_t IDESC = ptx::idesc_f16kind_f32(kBM, C::EP, 0, 0, 1);
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
@@ -81,10 +101,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar0 = base + kStages * C::kStageBytes;
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
-  const uint32_t acc_bar = bar0 + 8u * (2 * kStages);
-  const uint32_t done_bar = bar0 + 8u * (2 * kStages + 1);
-  uint32_t* tmem_slot =
-      reinterpret_cast<uint32_t*>(gbase + kStages * C::kStageBytes + 8 * (2 * kStages + 2));
+  auto afull_bar = [&](int b) { return bar0 + 8u * (2 * kStages + b); };
+  auto aempty_bar = [&](int b) { return bar0 + 8u * (2 * kStages + NACC + b); };
+  const uint32_t done_bar = bar0 + 8u * (2 * kStages + 2 * NACC);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + kStages * C::kStageBytes +
+                                                    8 * (2 * kStages + 2 * NACC + 1));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* never = reinterpret_cast<volatile int*>(tmem_slot + 2);  // stays 0
 
@@ -99,7 +120,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(full_bar(s), 1);
       ptx::mbar_init(empty_bar(s), 1);
     }
-    ptx::mbar_init(acc_bar, 1);
+    for (int b = 0; b < NACC; ++b) {
+      ptx::mbar_init(afull_bar(b), 1);
+      ptx::mbar_init(aempty_bar(b), 8);  // the eight epilogue warps
+    }
     ptx::mbar_init(done_bar, 1);
     *abort_flag = 0;
     *never = 0;
@@ -115,10 +139,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  // The setup above touched only shared memory, TMEM and parameters. With wait_at_end, the
-  // preceding kernel (the weight transpose, whose output this kernel does not read) started this
-  // one after its own wait, so everything before it is complete: the wait moves to the end.
-  if (!wait_at_end) griddep_wait();
+  griddep_wait();  // the setup above touched only shared memory, TMEM and parameters
   // the near-tie list of this call starts empty: the selection (the next kernel) appends to it
   // and the previous call's refine pass, which read it, has completed
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *rcount = 0;
@@ -136,9 +157,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t fb = full_bar(stage);
         ptx::mbar_arrive_expect_tx(fb, C::kStageBytes);
         ptx::tma_load_2d(sA, &tmX, fb, kb * kBK, m0);
-#pragma unroll
-        for (int c = 0; c < NCH; ++c)
-          ptx::tma_load_2d(sA + kABytes + c * kChunkBytes, &tmW, fb, c * 64, kb * kBK);
+        // experts >= E lie past the map's rows: the copy fills them with zeros
+        ptx::tma_load_2d(sA + kABytes, &tmW, fb, kb * kBK, 0);
         issued |= 1u << stage;
         last_par = (last_par & ~(1u << stage)) | (phase << stage);
         if (++stage == kStages) {
@@ -155,58 +175,81 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // -------------------------------------------------------------- MMA issuer
-      int stage = 0;
-      uint32_t phase = 0;
-      bool ok = true;
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
       for (int kb = kb0; kb < kb1; ++kb) {
-        if (!ptx::mbar_wait_bounded(full_bar(stage), phase, abort_flag, status,
-                                    MOE_DEVFAULT_PIPELINE_TIMEOUT, kWaitLimitNs)) {
-          ok = false;
+        if (!ptx::mbar_wait_bounded(aempty_bar(acc), acc_phase ^ 1u, abort_flag, status,
+                                    MOE_DEVFAULT_PIPELINE_TIMEOUT, kWaitLimitNs))
           break;
-        }
+        if (!ptx::mbar_wait_bounded(full_bar(stage), phase, abort_flag, status,
+                                    MOE_DEVFAULT_PIPELINE_TIMEOUT, kWaitLimitNs))
+          break;
         ptx::tc_fence_after();
         const uint32_t sA = base + stage * C::kStageBytes;
         const uint32_t sB = sA + kABytes;
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * C::EP);
 #pragma unroll
         for (int kk = 0; kk < kBK / 16; ++kk) {
           const uint64_t adesc = ptx::smem_desc_sw128(sA + kk * 32, 16, 1024);
-          const uint64_t bdesc = ptx::smem_desc_sw128(sB + kk * 2048, kChunkBytes, 1024);
-          ptx::umma_f16(tmem_base, adesc, bdesc, IDESC, (kb > kb0 || kk) ? 1u : 0u);
+          const uint64_t bdesc = ptx::smem_desc_sw128(sB + kk * 32, 16, 1024);
+          ptx::umma_f16(d_tmem, adesc, bdesc, IDESC, kk ? 1u : 0u);
         }
         ptx::umma_commit(empty_bar(stage));
+        ptx::umma_commit(afull_bar(acc));
         if (++stage == kStages) {
           stage = 0;
           phase ^= 1u;
         }
+        if (++acc == NACC) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
       }
-      if (ok) ptx::umma_commit(acc_bar);
       ptx::umma_commit(done_bar);
       ptx::mbar_wait_bounded(done_bar, 0, never, status, MOE_DEVFAULT_PIPELINE_TIMEOUT,
                              kWaitLimitNs / 4);
     }
     __syncwarp();
   } else if (warp >= 4) {
-    // ---------------------------------------------------------------- epilogue: partials out
-    const int q = warp - 4;
+    // ------------------------------------------------ epilogue: K blocks summed, partials out
+    const int q = warp & 3;          // TMEM lanes [32q, 32q + 32): rows of the tile
+    const int h = (warp - 4) >> 2;   // columns [h * HALF, h * HALF + HALF)
     const int t = m0 + 32 * q + lane;
-    if (ptx::mbar_wait_bounded(acc_bar, 0, abort_flag, status, MOE_DEVFAULT_PIPELINE_TIMEOUT,
-                               kWaitLimitNs)) {
-      ptx::tc_fence_after();
-      const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16);
-      float* dst = part + ((size_t)split * T + t) * C::EP;
-#pragma unroll 1
-      for (int c = 0; c < C::EP / 32; ++c) {
-        uint32_t v[32];
-        ptx::tmem_ld_32x32b_x32(taddr + c * 32, v);
-        ptx::tmem_wait_ld();
-        if (t < T) {
-          float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+    float sum[HALF];
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            d4[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
-        }
+    for (int i = 0; i < HALF; ++i) sum[i] = 0.f;
+    const uint32_t trow = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(h * HALF);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int kb = kb0; kb < kb1; ++kb) {
+      if (!ptx::mbar_wait_bounded(afull_bar(acc), acc_phase, abort_flag, status,
+                                  MOE_DEVFAULT_PIPELINE_TIMEOUT, kWaitLimitNs)) {
+        ok = false;
+        break;
       }
+      ptx::tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < HALF / 32; ++c) {
+        uint32_t v[32];
+        ptx::tmem_ld_32x32b_x32(trow + (uint32_t)(acc * C::EP + c * 32), v);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) sum[c * 32 + i] += __uint_as_float(v[i]);
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(aempty_bar(acc));
+      if (++acc == NACC) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    if (ok && t < T) {
+      float4* d4 = reinterpret_cast<float4*>(part + ((size_t)split * T + t) * C::EP + h * HALF);
+#pragma unroll
+      for (int i = 0; i < HALF / 4; ++i)
+        d4[i] = make_float4(sum[4 * i], sum[4 * i + 1], sum[4 * i + 2], sum[4 * i + 3]);
     }
   }
 
@@ -216,7 +259,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, C::kTmemCols);
   }
-  if (wait_at_end) griddep_wait();  // the weight transpose has completed too
 }
 
 struct SelectArgs {
@@ -451,26 +493,22 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a)
   }
 }
 
-// Router weight preparation, per call: WgT[e, j] = W_g[j, e] (each expert's weights contiguous,
-// for the exact re-decision of near-tie tokens) and, when E is not a multiple of 64,
-// Wp[j, e] = e < E ? W_g[j, e] : 0 for e < EP (zero columns for the MMA's padding experts).
+// Router weight transpose: WgT[e, j] = W_g[j, e], each expert's weights contiguous. The router
+// GEMM reads it as its K-major B operand and the exact passes (near-tie re-decision, overflow
+// re-route) read one expert's row at a time. Weight preparation: once per weight set through
+// moe_prepare_router, or per call when the caller passes no transposed copy.
 // 32 x 32 tiles through shared memory so both sides are coalesced.
-__global__ void __launch_bounds__(kThreads) prep_router_kernel(const uint16_t* __restrict__ W,
-                                                               uint16_t* __restrict__ WgT,
-                                                               uint16_t* __restrict__ Wp, int d,
-                                                               int E, int EP) {
+__global__ void __launch_bounds__(kThreads) transpose_router_kernel(
+    const uint16_t* __restrict__ W, uint16_t* __restrict__ WgT, int d, int E) {
   __shared__ uint16_t tile[32][33];
   griddep_wait();
-  // without a padded copy the router GEMM does not read this kernel's output: let it start now
-  // (it takes its wait at its end, so the selection and the refine pass still follow both)
-  if (Wp == nullptr) griddep_launch_dependents();
+  // the router GEMM may start its setup; it waits for this kernel before reading WgT
+  griddep_launch_dependents();
   const int j0 = blockIdx.x * 32, e0 = blockIdx.y * 32;
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
   for (int r = ty; r < 32; r += 8) {
     const int j = j0 + r, e = e0 + tx;
-    const uint16_t v = (j < d && e < E) ? W[(size_t)j * E + e] : (uint16_t)0;
-    tile[r][tx] = v;
-    if (Wp != nullptr && j < d && e < EP) Wp[(size_t)j * EP + e] = v;
+    tile[r][tx] = (j < d && e < E) ? W[(size_t)j * E + e] : (uint16_t)0;
   }
   __syncthreads();
   for (int r = ty; r < 32; r += 8) {
@@ -663,14 +701,14 @@ __global__ void __launch_bounds__(kThreads) refine_kernel(
 template <int NCH>
 cudaError_t launch_gemm(const CUtensorMap& mx, const CUtensorMap& mw, float* part, int T,
                         int n_mt, int splits, int kb_per_split, int k_blocks, int* status,
-                        int* rcount, int wait_at_end, cudaStream_t st) {
+                        int* rcount, cudaStream_t st) {
   using C = RCfg<NCH>;
   cudaError_t err = cudaFuncSetAttribute(router_gemm_kernel<NCH>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmemBytes);
   if (err != cudaSuccess) return err;
-  return launch_k(router_gemm_kernel<NCH>, dim3(n_mt, splits), dim3(kThreads), C::kSmemBytes, st,
-                  mx, mw, part, T, kb_per_split, k_blocks, status, rcount, wait_at_end);
+  return launch_k(router_gemm_kernel<NCH>, dim3(n_mt, splits), dim3(kGemmThreads), C::kSmemBytes,
+                  st, mx, mw, part, T, kb_per_split, k_blocks, status, rcount);
 }
 
 }  // namespace
@@ -687,30 +725,35 @@ int router_splits(int T, int d) {
   return (k_blocks + kbs - 1) / kbs;
 }
 
+cudaError_t launch_router_transpose(int d, int E, const uint16_t* W_g, uint16_t* W_g_t,
+                                    cudaStream_t st) {
+  const dim3 grid((d + 31) / 32, (E + 31) / 32);
+  return launch_k(transpose_router_kernel, grid, dim3(kThreads), 0, st, W_g, W_g_t, d, E);
+}
+
 cudaError_t launch_router(const Shape& s, const uint16_t* x, const uint16_t* W_g,
-                          const float* bias, const float* u, int32_t* topk_idx, float* topk_w,
-                          const RouterScratch& rs, int* status, cudaStream_t st) {
+                          const uint16_t* W_g_t, const float* bias, const float* u,
+                          int32_t* topk_idx, float* topk_w, const RouterScratch& rs, int* status,
+                          cudaStream_t st) {
   const int EP = (s.E + 63) / 64 * 64;
-  const uint16_t* W = EP != s.E ? rs.wg_pad : W_g;
-  {
-    const dim3 grid((s.d + 31) / 32, (EP + 31) / 32);
-    const cudaError_t e = launch_k(prep_router_kernel, grid, dim3(kThreads), 0, st, W_g, rs.wg_t,
-                                   EP != s.E ? rs.wg_pad : nullptr, s.d, s.E, EP);
-    if (e != cudaSuccess) return e;
+  cudaError_t err;
+  if (W_g_t == nullptr) {
+    // no prepared transpose: make one in the workspace for this call
+    if ((err = launch_router_transpose(s.d, s.E, W_g, rs.wg_t, st)) != cudaSuccess) return err;
+    W_g_t = rs.wg_t;
   }
   CUtensorMap mx, mw;
-  if (!make_tmap_2d(&mx, x, s.T, s.d, kBK, kBM) || !make_tmap_2d(&mw, W, s.d, EP, 64, kBK))
+  if (!make_tmap_2d(&mx, x, s.T, s.d, kBK, kBM) || !make_tmap_2d(&mw, W_g_t, s.E, s.d, kBK, EP))
     return cudaErrorInvalidValue;
   const int n_mt = (s.T + kBM - 1) / kBM;
   const int k_blocks = s.d / kBK;
   const int splits = router_splits(s.T, s.d);
   const int kbs = (k_blocks + splits - 1) / splits;
-  cudaError_t err;
   switch (EP / 64) {
-    case 1: err = launch_gemm<1>(mx, mw, rs.part, s.T, n_mt, splits, kbs, k_blocks, status, rs.rcount, EP == s.E ? 1 : 0, st); break;
-    case 2: err = launch_gemm<2>(mx, mw, rs.part, s.T, n_mt, splits, kbs, k_blocks, status, rs.rcount, EP == s.E ? 1 : 0, st); break;
-    case 3: err = launch_gemm<3>(mx, mw, rs.part, s.T, n_mt, splits, kbs, k_blocks, status, rs.rcount, EP == s.E ? 1 : 0, st); break;
-    default: err = launch_gemm<4>(mx, mw, rs.part, s.T, n_mt, splits, kbs, k_blocks, status, rs.rcount, EP == s.E ? 1 : 0, st); break;
+    case 1: err = launch_gemm<1>(mx, mw, rs.part, s.T, n_mt, splits, kbs, k_blocks, status, rs.rcount, st); break;
+    case 2: err = launch_gemm<2>(mx, mw, rs.part, s.T, n_mt, splits, kbs, k_blocks, status, rs.rcount, st); break;
+    case 3: err = launch_gemm<3>(mx, mw, rs.part, s.T, n_mt, splits, kbs, k_blocks, status, rs.rcount, st); break;
+    default: err = launch_gemm<4>(mx, mw, rs.part, s.T, n_mt, splits, kbs, k_blocks, status, rs.rcount, st); break;
   }
   if (err != cudaSuccess) return err;
   SelectArgs a;
@@ -745,7 +788,7 @@ cudaError_t launch_router(const Shape& s, const uint16_t* x, const uint16_t* W_g
     err = launch_k(select_kernel<8>, sgrid, sblock, 0, st, a);
   if (err != cudaSuccess) return err;
   const int rgrid = num_sms();  // one CTA per SM (its registers allow no second)
-  return launch_k(refine_kernel, dim3(rgrid), dim3(kThreads), 0, st, x, (const uint16_t*)rs.wg_t,
+  return launch_k(refine_kernel, dim3(rgrid), dim3(kThreads), 0, st, x, W_g_t,
                   bias, u, (const int32_t*)rs.rrec, (const int*)rs.rcount, topk_idx, topk_w, s.T,
                   s.d, s.E,
                   s.k, s.mode, s.tau, s.G, s.Gk);

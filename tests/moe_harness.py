@@ -4,10 +4,10 @@ same bytes, and compare under the parity contract.
 Contract (per token):
   * expert indices bit-exact, except tokens whose oracle top-(k+1) adjacent score gap is below
     1e-5 (exempt; counted and reported);
-  * gates within 5e-5 of the oracle's gates at the GPU's indices (the gates come from
-    tensor-core logits whose fp32 accumulation differs from an exact dot product by up to
-    ~4e-5 in a logit difference at d = 7168; a softmax over two of them moves by at most
-    w_i w_j <= 1/4 of that, doubled by 1/tau = 2 for Gumbel scores);
+  * gates within 1e-5 of the oracle's gates at the GPU's indices (the contract's gate
+    tolerance; the router's logits are within about 2e-6 of the exact ones, and a softmax
+    over the selected logits moves by at most half the error of a logit difference, doubled by
+    1/tau = 2 for Gumbel scores);
   * counts / offsets / perm_slot / slot_pos bit-exact against the oracle dispatch run on the
     GPU's indices;
   * layer output (bf16) against the oracle's float64 output conditioned on the GPU's indices:
@@ -28,7 +28,7 @@ import oracle as O
 import sparse_moe_layer_route_gb300 as M
 import workloads as W
 
-GATE_ATOL = 5e-5
+GATE_ATOL = 1e-5
 OUT_MAXABS = 2e-2
 OUT_RELL2 = 1e-2
 
@@ -69,9 +69,17 @@ def quantize_inputs(inp, bits):
     return inp[key], inp[key + "_struct"]
 
 
-def run_layer(cfg, inp, capacity_override=0, stream=None, f16=True):
+def prepare_router(inp):
+    """The router weights transposed once (moe_prepare_router), as a deployment would."""
+    if "W_g_t" not in inp:
+        inp["W_g_t"] = M.prepare_router(inp["W_g"])
+    return inp["W_g_t"]
+
+
+def run_layer(cfg, inp, capacity_override=0, stream=None, f16=True, prepared=True):
     """moe_layer_forward with every routing output requested; returns numpy arrays.
     f16: use the fp16 down path (W_down re-encoded once), else the bf16 down path.
+    prepared: pass the router weights transposed once (else each call transposes them).
     With cfg.weight_bits the experts are quantized on the GPU first."""
     mc = M.MoeConfig.from_layer(cfg)
     mc.capacity_override = capacity_override
@@ -87,23 +95,26 @@ def run_layer(cfg, inp, capacity_override=0, stream=None, f16=True):
     out = torch.full((T, d), float("nan"), dtype=torch.bfloat16, device=dev)
     ws = M.alloc_workspace(mc, dev)
     bits = getattr(cfg, "weight_bits", 0)
+    wgt = prepare_router(inp) if prepared else None
     if bits:
         _, qstruct = quantize_inputs(inp, bits)
-        weights = M.make_weights(inp["W_g"], inp["bias"], None, None, None, quant=qstruct)
+        weights = M.make_weights(inp["W_g"], inp["bias"], None, None, None, quant=qstruct,
+                                 W_g_t=wgt)
     else:
         if f16:
             pack_down(inp)
         weights = M.make_weights(inp["W_g"], inp["bias"], inp["W_gate"], inp["W_up"],
                                  inp["W_down"], inp.get("Ws_gate"), inp.get("Ws_up"),
                                  inp.get("Ws_down"), inp.get("W_down_f16") if f16 else None,
-                                 inp.get("Ws_down_f16") if f16 else None)
+                                 inp.get("Ws_down_f16") if f16 else None, W_g_t=wgt)
     ro = M.make_route_out(idx, w, counts, offsets, perm_slot, slot_pos)
     primary = None
     if getattr(cfg, "reroute", False):
         # the router's own choice, before the re-route (deterministic: the layer computes the same)
         p_idx = torch.empty((T, k), **i32)
         p_w = torch.empty((T, k), dtype=torch.float32, device=dev)
-        M.route(mc, inp["x"], inp["W_g"], inp["bias"], inp.get("u"), p_idx, p_w, ws, stream)
+        M.route(mc, inp["x"], inp["W_g"], inp["bias"], inp.get("u"), p_idx, p_w, ws, stream,
+                W_g_t=wgt)
         primary = p_idx.cpu().numpy()
     M.layer_forward(mc, weights, inp["x"], inp.get("u"), out, ro, ws, stream)
     status = M.device_status(ws, stream)

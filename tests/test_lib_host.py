@@ -67,16 +67,16 @@ def test_entry_points_validate_before_any_launch(lib):
     need = M.workspace_size(cfg)
     fake = 0x10000000  # never dereferenced: every call below must fail validation first
     # missing tensors
-    assert lib.moe_route(ctypes.byref(cfg), None, fake, None, None, fake, fake, fake, need,
+    assert lib.moe_route(ctypes.byref(cfg), None, fake, None, None, None, fake, fake, fake, need,
                          None) == 1
     # bias mode without a bias
     bcfg = M.MoeConfig.make(64, 128, 8, 2, 128, mode=M.ROUTE_BIAS_SELECT)
-    assert lib.moe_route(ctypes.byref(bcfg), fake, fake, None, None, fake, fake, fake, need,
+    assert lib.moe_route(ctypes.byref(bcfg), fake, fake, None, None, None, fake, fake, fake, need,
                          None) == 1
     # workspace: NULL, misaligned, too small
-    assert lib.moe_route(ctypes.byref(cfg), fake, fake, None, None, fake, fake, None, need,
+    assert lib.moe_route(ctypes.byref(cfg), fake, fake, None, None, None, fake, fake, None, need,
                          None) == 3
-    assert lib.moe_route(ctypes.byref(cfg), fake, fake, None, None, fake, fake, fake + 8, need,
+    assert lib.moe_route(ctypes.byref(cfg), fake, fake, None, None, None, fake, fake, fake + 8, need,
                          None) == 3
     assert lib.moe_permute(ctypes.byref(cfg), fake, fake, fake, fake, fake, fake, need - 1,
                            None) == 3
@@ -98,10 +98,10 @@ def test_entry_points_validate_before_any_launch(lib):
                                  fake, need, None) == 1
     # the router's and the re-route's exact dot products and the quantized passes' activation
     # prep read x in 16-byte pieces too
-    assert lib.moe_route(ctypes.byref(cfg), fake + 2, fake, None, None, fake, fake, fake, need,
+    assert lib.moe_route(ctypes.byref(cfg), fake + 2, fake, None, None, None, fake, fake, fake, need,
                          None) == 1
     rcfg = M.MoeConfig.make(64, 128, 8, 2, 128, capacity_factor=1.0, overflow_reroute=1)
-    assert lib.moe_overflow_reroute(ctypes.byref(rcfg), fake + 4, None, None, fake, fake, fake,
+    assert lib.moe_overflow_reroute(ctypes.byref(rcfg), fake + 4, None, None, None, fake, fake, fake,
                                     fake, fake, M.workspace_size(rcfg), None) == 1
     qcfg = M.MoeConfig.make(64, 128, 8, 2, 128, weight_bits=8)
     qm = M.MoeQMatrix(q=fake, scale=fake, zero=fake)
@@ -109,6 +109,18 @@ def test_entry_points_validate_before_any_launch(lib):
     assert lib.moe_grouped_ffn_quantized(ctypes.byref(qcfg), fake + 6, fake, fake, None,
                                          ctypes.byref(qw), fake, fake, M.workspace_size(qcfg),
                                          None) == 1
+    # router preparation: NULL / misaligned transpose, unsupported sizes
+    assert lib.moe_prepare_router(128, 8, None, fake, None) == 1
+    assert lib.moe_prepare_router(128, 8, fake, fake + 2, None) == 1
+    assert lib.moe_prepare_router(96, 8, fake, fake, None) == 2
+    assert lib.moe_prepare_router(128, 257, fake, fake, None) == 2
+    assert lib.moe_route(ctypes.byref(cfg), fake, fake, fake + 8, None, None, fake, fake, fake, need,
+                         None) == 1
+    wt = M.MoeWeights()
+    wt.W_g = wt.W_gate = wt.W_up = wt.W_down = fake
+    wt.W_g_t = fake + 4
+    assert lib.moe_layer_forward(ctypes.byref(cfg), ctypes.byref(wt), fake, None, fake, None,
+                                 fake, need, None) == 1
     # pack: NULL / misaligned pointers
     assert lib.moe_pack_f16(None, fake, 16, None) == 1
     assert lib.moe_pack_f16(fake + 2, fake, 16, None) == 1
@@ -138,12 +150,12 @@ def test_reroute_workspace_and_validation(lib):
         M.workspace_size(M.MoeConfig.make(4096, 1024, 64, 2, 512, **nocap))
     off = M.MoeConfig.make(64, 128, 8, 2, 128, capacity_factor=1.0)
     P = ctypes.c_void_p(0x1000)
-    assert lib.moe_overflow_reroute(ctypes.byref(off), P, None, None, P, P, P, P, P, 1 << 30,
+    assert lib.moe_overflow_reroute(ctypes.byref(off), P, None, None, None, P, P, P, P, P, 1 << 30,
                                     None) == 1     # re-route not enabled in the config
     on = M.MoeConfig.make(64, 128, 8, 2, 128, capacity_factor=1.0, overflow_reroute=1)
-    assert lib.moe_overflow_reroute(ctypes.byref(on), None, None, None, P, P, P, P, P, 1 << 30,
+    assert lib.moe_overflow_reroute(ctypes.byref(on), None, None, None, None, P, P, P, P, P, 1 << 30,
                                     None) == 1     # x missing
-    assert lib.moe_overflow_reroute(ctypes.byref(on), P, None, None, P, P, P, P, None, 1 << 30,
+    assert lib.moe_overflow_reroute(ctypes.byref(on), P, None, None, None, P, P, P, P, None, 1 << 30,
                                     None) == 3     # no workspace
 
 
@@ -172,8 +184,8 @@ def test_empty_batch_is_a_no_op_on_the_host(lib):
     n = ctypes.c_size_t(0)
     assert lib.moe_workspace_size(ctypes.byref(cfg), ctypes.byref(n)) == 0 and n.value == 512
     z = None
-    assert lib.moe_route(ctypes.byref(cfg), z, z, z, z, z, z, z, 0, z) == 0
-    assert lib.moe_overflow_reroute(ctypes.byref(cfg), z, z, z, z, z, z, z, z, 0, z) == 0
+    assert lib.moe_route(ctypes.byref(cfg), z, z, z, z, z, z, z, z, 0, z) == 0
+    assert lib.moe_overflow_reroute(ctypes.byref(cfg), z, z, z, z, z, z, z, z, z, 0, z) == 0
     assert lib.moe_grouped_ffn(ctypes.byref(cfg), z, z, z, z, z, z, z, z, z, z, z, z, z, z, 0,
                                z) == 0
     assert lib.moe_combine(ctypes.byref(cfg), z, z, z, z, 0, z) == 0
@@ -189,4 +201,4 @@ def test_empty_batch_is_a_no_op_on_the_host(lib):
     assert lib.moe_grouped_ffn(ctypes.byref(bad), z, z, z, z, z, z, z, z, z, z, z, z, z, z, 0,
                                z) == 1
     plain = M.MoeConfig.make(0, 128, 8, 2, 128)
-    assert lib.moe_overflow_reroute(ctypes.byref(plain), z, z, z, z, z, z, z, z, 0, z) == 1
+    assert lib.moe_overflow_reroute(ctypes.byref(plain), z, z, z, z, z, z, z, z, z, 0, z) == 1

@@ -27,7 +27,8 @@ CASES = [  # T, d, E, k, mode, bias
 ]
 
 
-def run_route(cfg, inp):
+def run_route(cfg, inp, prepared=False):
+    """moe_route; prepared: with the router weights transposed once by moe_prepare_router."""
     mc = M.MoeConfig.from_layer(cfg)
     dev = "cuda"
     x, W_g = inp["x"].to(dev), inp["W_g"].to(dev)
@@ -36,8 +37,8 @@ def run_route(cfg, inp):
     idx = torch.full((cfg.T, cfg.k), -1, dtype=torch.int32, device=dev)
     w = torch.full((cfg.T, cfg.k), float("nan"), dtype=torch.float32, device=dev)
     ws = M.alloc_workspace(mc)
-    M.route(mc, x, W_g, bias, u, idx, w, ws)
-    torch.cuda.synchronize()
+    M.route(mc, x, W_g, bias, u, idx, w, ws, W_g_t=M.prepare_router(W_g) if prepared else None)
+    assert M.device_status(ws) == 0
     return idx.cpu().numpy(), w.cpu().numpy()
 
 
@@ -60,6 +61,9 @@ def test_route_matches_oracle(T, d, E, k, mode, bias):
     w_ref = O.gates(r["logits"], r["scores"], idx, mode)
     assert np.abs(w - w_ref).max() <= GATE_ATOL
     np.testing.assert_allclose(w.sum(1), 1.0, atol=2e-6)
+    # the once-prepared transpose gives the same bits as the per-call one
+    idx_p, w_p = run_route(cfg, inp, prepared=True)
+    assert np.array_equal(idx_p, idx) and np.array_equal(w_p.view(np.uint32), w.view(np.uint32))
 
 
 def test_route_exact_ties_lowest_index():
@@ -94,8 +98,10 @@ def test_route_k_equals_E_zero_router():
 
 def test_route_near_ties_are_decided_exactly():
     """Two router columns that differ in one weight by 16 bf16 ulps give logit differences
-    ~N(0, 3e-5): above the 1e-5 exemption, yet within the tensor core's accumulation error. The
-    near-tie pass must still pick and order them exactly as the oracle does."""
+    ~N(0, 3e-5): many lie above the 1e-5 exemption yet inside the router's near-tie band (8e-6
+    times the row's largest |logit| at d = 2048, and the pair's column is scaled to give logits
+    of a few units), where the token is re-decided from plain fp32 dot products. It must pick
+    and order them exactly as the oracle does."""
     cfg = W.small_config(T=2048, d=2048, E=64, k=4, f=64, seed=31)
     inp = W.make_routing_inputs(cfg)
     Wg = inp["W_g"].float()
@@ -143,8 +149,8 @@ def test_group_limited_route_matches_oracle(T, d, E, k, mode, bias, G, Gk):
 
 def test_group_near_ties_are_decided_exactly():
     """The best experts of groups 0 and 1 are two router columns 16 bf16 ulps apart in one
-    weight, so the group decision of many tokens hangs on a logit difference inside the tensor
-    core's error yet above the exemption margin. The full exact recompute must decide it."""
+    weight, so the group decision of many tokens hangs on a logit difference inside the router's
+    near-tie band yet above the exemption margin. The full exact recompute must decide it."""
     cfg = W.small_config(T=2048, d=2048, E=32, k=2, f=64, seed=41, n_groups=4, topk_groups=1)
     inp = W.make_routing_inputs(cfg)
     Wg = inp["W_g"].float()
