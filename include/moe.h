@@ -88,6 +88,18 @@ typedef enum {
 #define MOE_DEVFAULT_BAD_EXPERT_INDEX 0x1 /* a top-k index outside [0, E) reached dispatch   */
 #define MOE_DEVFAULT_PIPELINE_TIMEOUT 0x2 /* a GEMM pipeline wait exceeded its bound          */
 #define MOE_DEVFAULT_BAD_TILE 0x4         /* the grouped GEMM met an inconsistent tile list   */
+#define MOE_DEVFAULT_FP16_RANGE 0x8       /* a value stored in fp16 (H or a slot row on the fp16
+                                             down path or the quantized path, or a weight
+                                             re-encoded by moe_pack_f16) was past +-65504 (or
+                                             not finite) and was clamped: that output is not
+                                             exact; use the bf16 down path for such data   */
+
+/* Element type of the slot-ordered expert outputs y_slot (written by moe_grouped_ffn, read by
+ * moe_combine). */
+typedef enum {
+  MOE_Y_F16 = 0, /* fp16 rows: the fp16 down path (W_down_f16 given) and quantized experts */
+  MOE_Y_F32 = 1  /* fp32 rows: the bf16 down path (W_down_f16 NULL) */
+} moe_y_type;
 
 typedef struct {
   int32_t T;                 /* tokens */
@@ -160,9 +172,13 @@ typedef struct {
   const uint16_t* Wsh_up;     /* [S, d, d_ff] bf16 */
   const uint16_t* Wsh_down;   /* [S, d_ff, d] bf16 */
   /* Optional fp16 re-encodings of W_down / Wsh_down written once by moe_pack_f16. When given,
-   * the down GEMM runs fp16 x fp16 and carries the SwiGLU activations H in fp16 (11-bit
-   * significand) instead of bf16 (8-bit), which keeps the layer output within bf16 rounding of
-   * the exact result; NULL selects the bf16 down path (no packed copy needed). */
+   * the down GEMM runs fp16 x fp16 and carries the SwiGLU activations H and the gate-scaled
+   * expert outputs in fp16 (11-bit significand) instead of bf16 H (8-bit) and fp32 outputs,
+   * which keeps the layer output within bf16 rounding of the exact result and halves the
+   * combine's reads. fp16's range ends at 65504: a value past it is clamped and reported as
+   * MOE_DEVFAULT_FP16_RANGE. NULL selects the bf16 down path (no packed copy needed), whose H
+   * and outputs have fp32's range: choose it when activations may reach that magnitude (for
+   * instance outlier features of a trained model), or after that fault was reported. */
   const uint16_t* W_down_f16;   /* [E, d_ff, d] fp16 or NULL */
   const uint16_t* Wsh_down_f16; /* [S, d_ff, d] fp16 or NULL (required when W_down_f16 is set
                                  * and n_shared > 0) */
@@ -275,30 +291,38 @@ moe_status moe_permute_noalloc(const moe_config* cfg, const int32_t* topk_idx, i
  *   perm_slot, offsets as written by moe_permute; topk_w [T, k] (NULL: every gate is 1).
  *   Shared weights may be NULL when cfg->n_shared == 0. W_down_f16 / Wsh_down_f16: optional
  *   fp16 re-encodings from moe_pack_f16 (see moe_weights); NULL selects the bf16 down path.
- *   Writes y_slot [T * k + S * T, d] fp16 (round to nearest, saturating at +-65504):
- *   row t*k + j = gate[t,j] * y(t,j) for every kept slot (rows of dropped slots are not
- *   written); row T*k + s*T + t = z_s[t]. fp16 keeps 11 significant bits per term, so the
- *   fixed-order sum in moe_combine stays within bf16 rounding of the exact layer output. */
+ *   Writes y_slot [T * k + S * T, d]: row t*k + j = gate[t,j] * y(t,j) for every kept slot
+ *   (rows of dropped slots are not written); row T*k + s*T + t = z_s[t]. The rows are fp16
+ *   (MOE_Y_F16, round to nearest, saturating at +-65504 with MOE_DEVFAULT_FP16_RANGE recorded)
+ *   on the fp16 down path and fp32 (MOE_Y_F32) on the bf16 down path. fp16 keeps 11
+ *   significant bits per term, so the fixed-order sum in moe_combine stays within bf16
+ *   rounding of the exact layer output. */
 moe_status moe_grouped_ffn(const moe_config* cfg, const uint16_t* x, const int32_t* perm_slot,
                            const int32_t* offsets, const float* topk_w, const uint16_t* W_gate,
                            const uint16_t* W_up, const uint16_t* W_down,
                            const uint16_t* Wsh_gate, const uint16_t* Wsh_up,
                            const uint16_t* Wsh_down, const uint16_t* W_down_f16,
-                           const uint16_t* Wsh_down_f16, uint16_t* y_slot, void* ws,
+                           const uint16_t* Wsh_down_f16, void* y_slot, void* ws,
                            size_t ws_bytes, moe_stream_t stream);
 
 /* Step 10. out[t] = sum_{j=0..k-1, slot_pos[t*k+j] >= 0} y_slot[t*k+j]
  *                   + sum_{s=0..S-1} y_slot[T*k + s*T + t],
- * summed in fp32 in exactly that order and rounded once to bf16. y_slot fp16, out [T, d] bf16. */
-moe_status moe_combine(const moe_config* cfg, const uint16_t* y_slot, const int32_t* slot_pos,
-                       uint16_t* out, void* ws, size_t ws_bytes, moe_stream_t stream);
+ * summed in fp32 in exactly that order and rounded once to bf16. y_slot holds rows of y_type
+ * (moe_y_type, as moe_grouped_ffn wrote them: MOE_Y_F16 or MOE_Y_F32; anything else returns
+ * MOE_ERR_INVALID_ARG), out [T, d] bf16. */
+moe_status moe_combine(const moe_config* cfg, const void* y_slot, int32_t y_type,
+                       const int32_t* slot_pos, uint16_t* out, void* ws, size_t ws_bytes,
+                       moe_stream_t stream);
 
 /* One-time weight preparation (not part of the layer's per-call work): dst[i] = src[i]
  * re-encoded from bf16 to fp16, round to nearest even, saturating at +-65504. Exact for every
  * bf16 value whose magnitude lies in [2^-14, 65504]; smaller magnitudes become fp16 subnormals
- * (absolute error <= 2^-25). n elements; src and dst device pointers, 16-byte aligned. */
+ * (absolute error <= 2^-25). n elements; src and dst device pointers, 16-byte aligned.
+ * fault_bits: optional device int32 into which the call ORs MOE_DEVFAULT_FP16_RANGE when a
+ * weight had to be clamped (|w| >= 65536 or not finite); the caller clears it beforehand.
+ * Weights like that need the bf16 down path. */
 moe_status moe_pack_f16(const uint16_t* src_bf16, uint16_t* dst_f16, size_t n,
-                        moe_stream_t stream);
+                        int32_t* fault_bits, moe_stream_t stream);
 
 /* One-time weight preparation: group-wise quantization of n_mat bf16 matrices W [n_mat, K, N]
  * (row-major, K = input dimension, K % 128 == 0, N % 32 == 0) to bits = 4 or 8, in the layout

@@ -17,6 +17,8 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
                 3: "MOE_ERR_WORKSPACE", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE_FAULT"}
 ROUTE_PLAIN, ROUTE_BIAS_SELECT, ROUTE_GUMBEL = 0, 1, 2
 DEVFAULT_BAD_EXPERT_INDEX, DEVFAULT_PIPELINE_TIMEOUT, DEVFAULT_BAD_TILE = 0x1, 0x2, 0x4
+DEVFAULT_FP16_RANGE = 0x8
+Y_F16, Y_F32 = 0, 1
 
 EXPORTS = ("moe_workspace_size", "moe_workspace_init", "moe_prepare_router", "moe_route",
            "moe_permute",
@@ -103,14 +105,14 @@ def lib():
         L.moe_grouped_ffn_quantized.argtypes = [cfgp, P, P, P, P, ctypes.POINTER(MoeQWeights),
                                                 P, P, S, P]
         L.moe_grouped_ffn.argtypes = [cfgp, P, P, P, P, P, P, P, P, P, P, P, P, P, P, S, P]
-        L.moe_combine.argtypes = [cfgp, P, P, P, P, S, P]
+        L.moe_combine.argtypes = [cfgp, P, ctypes.c_int32, P, P, P, S, P]
         L.moe_layer_forward.argtypes = [cfgp, ctypes.POINTER(MoeWeights), P, P, P,
                                         ctypes.POINTER(MoeRouteOut), P, S, P]
         L.moe_layer_forward_profiled.argtypes = [cfgp, ctypes.POINTER(MoeWeights), P, P, P,
                                                  ctypes.POINTER(MoeRouteOut), P, S, P,
                                                  ctypes.POINTER(ctypes.c_void_p), I]
         L.moe_layer_forward_host.argtypes = [cfgp, ctypes.POINTER(MoeWeights), P, P, P, P, S, P]
-        L.moe_pack_f16.argtypes = [P, P, S, P]
+        L.moe_pack_f16.argtypes = [P, P, S, P, P]
         L.moe_bias_update.argtypes = [ctypes.c_int32, P, P, ctypes.c_float, ctypes.c_float, P]
         L.moe_device_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_int32)]
         L.moe_status_string.argtypes = [I]
@@ -211,7 +213,8 @@ def overflow_reroute(cfg, x, expert_bias, gumbel_u, topk_idx, topk_w, counts, sl
 
 def grouped_ffn(cfg, x, perm_slot, offsets, topk_w, W_gate, W_up, W_down, Wsh_gate, Wsh_up,
                 Wsh_down, y_slot, ws, stream=None, W_down_f16=None, Wsh_down_f16=None):
-    """y_slot: float16 [T*k + S*T, d]."""
+    """y_slot [T*k + S*T, d]: float16 on the fp16 down path (W_down_f16 given), float32 on the
+    bf16 down path."""
     _check(lib().moe_grouped_ffn(ctypes.byref(cfg), _ptr(x), _ptr(perm_slot), _ptr(offsets),
                                  _ptr(topk_w), _ptr(W_gate), _ptr(W_up), _ptr(W_down),
                                  _ptr(Wsh_gate), _ptr(Wsh_up), _ptr(Wsh_down),
@@ -254,23 +257,28 @@ def grouped_ffn_quantized(cfg, x, perm_slot, offsets, topk_w, qweights: MoeQWeig
            "moe_grouped_ffn_quantized")
 
 
-def pack_f16(src_bf16, dst_f16, stream=None):
-    """dst (int16/float16 tensor) = fp16 re-encoding of the bf16 tensor src (same shape)."""
+def pack_f16(src_bf16, dst_f16, stream=None, fault_bits=None):
+    """dst (int16/float16 tensor) = fp16 re-encoding of the bf16 tensor src (same shape).
+    fault_bits: optional int32 device tensor into which DEVFAULT_FP16_RANGE is OR-ed when a
+    weight had to be clamped."""
     assert src_bf16.numel() == dst_f16.numel()
-    _check(lib().moe_pack_f16(_ptr(src_bf16), _ptr(dst_f16), src_bf16.numel(), _stream(stream)),
-           "moe_pack_f16")
+    _check(lib().moe_pack_f16(_ptr(src_bf16), _ptr(dst_f16), src_bf16.numel(), _ptr(fault_bits),
+                              _stream(stream)), "moe_pack_f16")
 
 
-def packed_f16(src_bf16, stream=None):
+def packed_f16(src_bf16, stream=None, fault_bits=None):
     """A new float16 tensor holding the fp16 re-encoding of src (torch allocates)."""
     import torch
     dst = torch.empty(src_bf16.shape, dtype=torch.float16, device=src_bf16.device)
-    pack_f16(src_bf16, dst, stream)
+    pack_f16(src_bf16, dst, stream, fault_bits)
     return dst
 
 
 def combine(cfg, y_slot, slot_pos, out, ws, stream=None):
-    _check(lib().moe_combine(ctypes.byref(cfg), _ptr(y_slot), _ptr(slot_pos), _ptr(out),
+    """y_slot: float16 or float32 slot rows (its dtype selects MOE_Y_F16 / MOE_Y_F32)."""
+    import torch
+    y_type = Y_F32 if y_slot.dtype == torch.float32 else Y_F16
+    _check(lib().moe_combine(ctypes.byref(cfg), _ptr(y_slot), y_type, _ptr(slot_pos), _ptr(out),
                              _ptr(ws), ws.numel(), _stream(stream)), "moe_combine")
 
 

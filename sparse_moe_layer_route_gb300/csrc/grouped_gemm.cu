@@ -1,9 +1,11 @@
 // Grouped GEMM over variable-length expert segments on the 5th-generation tensor cores.
 //
 //   gate/up pass (MODE 0):  H[p, n] = silu(sum_k A[p,k] W_gate[e][k,n]) * (sum_k A[p,k] W_up[e][k,n])
-//   down pass    (MODE 1):  Y[row(p), n] = gate(p) * sum_k H[p,k] W_down[e][k,n]     (Y in fp16)
-// H is stored in fp16 (HF16, with an fp16 copy of W_down so both down operands share the type)
-// or in bf16.
+//   down pass    (MODE 1):  Y[row(p), n] = gate(p) * sum_k H[p,k] W_down[e][k,n]
+// On the fp16 down path (HF16, with an fp16 copy of W_down so both down operands share the
+// type) H and Y are stored in fp16: 11 significant bits, but a range of +-65504, so the
+// epilogues record MOE_DEVFAULT_FP16_RANGE when a value of a stored row would be clamped. On the
+// bf16 down path H is bf16 and Y fp32, with fp32's range.
 //
 // Expert SwiGLU: "GPT-4 Has 1.8 Trillion Parameters. It Uses 2% of Them Per Token", §3.3, and
 // "大模型MoE稀疏激活原理与工程实践", §3.2 (uniform d -> d_ff -> d experts). Running every
@@ -64,7 +66,7 @@ struct GemmArgs {
   int n_ntiles;       // column tiles
   int k_blocks;       // K / 64
   int E;              // routed experts; tile.expert >= E is shared expert (expert - E)
-  uint16_t* out;      // H (MODE 0) or Y (MODE 1, fp16)
+  void* out;          // H (MODE 0) or Y (MODE 1: fp16 on the fp16 down path, else fp32)
   long long out_ld;   // elements per output row
   const int32_t* perm_slot;  // MODE 1
   const float* topk_w;       // MODE 1 (NULL: gate 1)
@@ -94,6 +96,97 @@ __device__ __forceinline__ uint32_t pack_f16x2_sat(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
+}
+
+// Magnitude bits of a float with the sign cleared: they order as |v| does, and NaN orders above
+// infinity. A value whose bits reach kF16Clamp (65520.0f) would round past the largest finite
+// fp16 (65504), so the saturating conversion clamps it (or it is not finite at all).
+__device__ __forceinline__ uint32_t mag_bits(float v) { return __float_as_uint(v) & 0x7FFFFFFFu; }
+constexpr uint32_t kF16Clamp = 0x477FF000u;
+
+// The epilogue of one work unit for one accumulator row (one thread): the unit's BN accumulator
+// columns from TMEM at taddr, written to row `orow` of the output from column nt * (BN / 2)
+// (MODE 0) or nt * BN (MODE 1).
+//   MODE 0: H = silu(G) * U, G the first BN/2 columns and U the rest; fp16 (HF16) or bf16.
+//   MODE 1: Y = gate * acc; fp16 (HF16) or fp32 (the bf16 down path: no range limit).
+// Returns the largest magnitude bits (mag_bits) among values converted to fp16 by a valid row
+// (0 when nothing went to fp16), so the caller can report a clamp.
+template <int MODE, int BN, bool HF16>
+__device__ __forceinline__ uint32_t epilogue_row(uint32_t taddr, void* out, long long out_ld,
+                                                 long long orow, int nt, float gate,
+                                                 bool valid) {
+  uint32_t mx = 0u;
+  if (MODE == 0) {
+    uint16_t* dst = static_cast<uint16_t*>(out) + orow * out_ld + (long long)nt * (BN / 2);
+#pragma unroll 1
+    for (int c = 0; c < BN / 2 / 32; ++c) {
+      uint32_t g[32], u[32];
+      ptx::tmem_ld_32x32b_x32(taddr + c * 32, g);
+      ptx::tmem_ld_32x32b_x32(taddr + BN / 2 + c * 32, u);
+      ptx::tmem_wait_ld();
+      uint32_t hv[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
+        const float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
+        const float h0 = g0 / (1.0f + __expf(-g0)) * u0;
+        const float h1 = g1 / (1.0f + __expf(-g1)) * u1;
+        if (HF16) mx = max(mx, max(mag_bits(h0), mag_bits(h1)));
+        hv[i] = HF16 ? pack_f16x2_sat(h0, h1) : pack_bf16x2(h0, h1);
+      }
+      if (valid) {
+        uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          d4[i] = make_uint4(hv[4 * i], hv[4 * i + 1], hv[4 * i + 2], hv[4 * i + 3]);
+      }
+    }
+  } else if (HF16) {
+    uint16_t* dst = static_cast<uint16_t*>(out) + orow * out_ld + (long long)nt * BN;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      uint32_t v[32];
+      ptx::tmem_ld_32x32b_x32(taddr + c * 32, v);
+      ptx::tmem_wait_ld();
+      uint32_t yv[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float y0 = gate * __uint_as_float(v[2 * i]);
+        const float y1 = gate * __uint_as_float(v[2 * i + 1]);
+        mx = max(mx, max(mag_bits(y0), mag_bits(y1)));
+        yv[i] = pack_f16x2_sat(y0, y1);
+      }
+      if (valid) {
+        uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          d4[i] = make_uint4(yv[4 * i], yv[4 * i + 1], yv[4 * i + 2], yv[4 * i + 3]);
+      }
+    }
+  } else {
+    float* dst = static_cast<float*>(out) + orow * out_ld + (long long)nt * BN;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      uint32_t v[32];
+      ptx::tmem_ld_32x32b_x32(taddr + c * 32, v);
+      ptx::tmem_wait_ld();
+      if (valid) {
+        float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          d4[i] = make_float4(gate * __uint_as_float(v[4 * i]), gate * __uint_as_float(v[4 * i + 1]),
+                              gate * __uint_as_float(v[4 * i + 2]),
+                              gate * __uint_as_float(v[4 * i + 3]));
+      }
+    }
+  }
+  return valid ? mx : 0u;
+}
+
+// After an epilogue warp's last unit: one vote, and one atomic per warp that clamped a value.
+__device__ __forceinline__ void report_f16_clamp(uint32_t mx, int lane, int* status) {
+  if (__any_sync(0xffffffffu, mx >= kF16Clamp) && lane == 0)
+    atomicOr(status, MOE_DEVFAULT_FP16_RANGE);
 }
 
 template <int MODE, int NCH, bool HF16>
@@ -270,6 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row_in_tile = 32 * q + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
+    uint32_t clamp = 0u;  // largest magnitude this thread converted to fp16 (mag_bits)
     for (long long w = blockIdx.x; w < total; w += gridDim.x) {
       TileEntry te;
       int nt;
@@ -289,50 +383,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       ptx::tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN);
-      if (MODE == 0) {
-        uint16_t* dst = a.out + p * a.out_ld + (long long)nt * (BN / 2);
-#pragma unroll 1
-        for (int c = 0; c < BN / 2 / 32; ++c) {
-          uint32_t g[32], u[32];
-          ptx::tmem_ld_32x32b_x32(taddr + c * 32, g);
-          ptx::tmem_ld_32x32b_x32(taddr + BN / 2 + c * 32, u);
-          ptx::tmem_wait_ld();
-          uint32_t hv[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
-            const float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
-            const float h0 = g0 / (1.0f + __expf(-g0)) * u0;
-            const float h1 = g1 / (1.0f + __expf(-g1)) * u1;
-            hv[i] = HF16 ? pack_f16x2_sat(h0, h1) : pack_bf16x2(h0, h1);
-          }
-          if (valid) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              d4[i] = make_uint4(hv[4 * i], hv[4 * i + 1], hv[4 * i + 2], hv[4 * i + 3]);
-          }
-        }
-      } else {
-        uint16_t* dst = a.out + orow * a.out_ld + (long long)nt * BN;
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t v[32];
-          ptx::tmem_ld_32x32b_x32(taddr + c * 32, v);
-          ptx::tmem_wait_ld();
-          uint32_t yv[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            yv[i] = pack_f16x2_sat(gate * __uint_as_float(v[2 * i]),
-                                   gate * __uint_as_float(v[2 * i + 1]));
-          if (valid) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              d4[i] = make_uint4(yv[4 * i], yv[4 * i + 1], yv[4 * i + 2], yv[4 * i + 3]);
-          }
-        }
-      }
+      clamp = max(clamp, epilogue_row<MODE, BN, HF16>(taddr, a.out, a.out_ld,
+                                                       MODE == 0 ? p : orow, nt, gate, valid));
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(tempty_bar(acc));
@@ -341,6 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         acc_phase ^= 1u;
       }
     }
+    report_f16_clamp(clamp, lane, a.status);
   }
 
   ptx::tc_fence_before();
@@ -528,6 +581,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row_in_tile = kBM * (int)rank + 32 * q + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
+    uint32_t clamp = 0u;  // largest magnitude this thread converted to fp16 (mag_bits)
     for (long long w = pair; w < total; w += n_pairs) {
       TileEntry te;
       int nt;
@@ -546,50 +600,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       ptx::tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN);
-      if (MODE == 0) {
-        uint16_t* dst = a.out + p * a.out_ld + (long long)nt * (BN / 2);
-#pragma unroll 1
-        for (int c = 0; c < BN / 2 / 32; ++c) {
-          uint32_t g[32], u[32];
-          ptx::tmem_ld_32x32b_x32(taddr + c * 32, g);
-          ptx::tmem_ld_32x32b_x32(taddr + BN / 2 + c * 32, u);
-          ptx::tmem_wait_ld();
-          uint32_t hv[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
-            const float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
-            const float h0 = g0 / (1.0f + __expf(-g0)) * u0;
-            const float h1 = g1 / (1.0f + __expf(-g1)) * u1;
-            hv[i] = HF16 ? pack_f16x2_sat(h0, h1) : pack_bf16x2(h0, h1);
-          }
-          if (valid) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              d4[i] = make_uint4(hv[4 * i], hv[4 * i + 1], hv[4 * i + 2], hv[4 * i + 3]);
-          }
-        }
-      } else {
-        uint16_t* dst = a.out + orow * a.out_ld + (long long)nt * BN;
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t v[32];
-          ptx::tmem_ld_32x32b_x32(taddr + c * 32, v);
-          ptx::tmem_wait_ld();
-          uint32_t yv[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            yv[i] = pack_f16x2_sat(gate * __uint_as_float(v[2 * i]),
-                                   gate * __uint_as_float(v[2 * i + 1]));
-          if (valid) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              d4[i] = make_uint4(yv[4 * i], yv[4 * i + 1], yv[4 * i + 2], yv[4 * i + 3]);
-          }
-        }
-      }
+      clamp = max(clamp, epilogue_row<MODE, BN, HF16>(taddr, a.out, a.out_ld,
+                                                       MODE == 0 ? p : orow, nt, gate, valid));
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -603,6 +615,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         acc_phase ^= 1u;
       }
     }
+    report_f16_clamp(clamp, lane, a.status);
   }
 
   // every copy into either CTA has landed and every MMA has finished once rank 0's MMA thread

@@ -154,7 +154,7 @@ struct FfnPtrs {
   const uint16_t *Wsh_gate, *Wsh_up, *Wsh_down;
   const uint16_t *W_down_f16, *Wsh_down_f16;  // fp16 down path when W_down_f16 != nullptr
   uint16_t* h;                                // H: fp16 on the fp16 down path, else bf16
-  uint16_t* y;                                // slot-ordered expert outputs, fp16
+  void* y;  // slot-ordered expert outputs: fp16 on the fp16 down path, fp32 on the bf16 one
   const TileEntry* tiles;
   const Meta* meta;
   int* status;
@@ -180,6 +180,7 @@ struct QFfnPtrs {
   const TileEntry* tiles;     // kQTileM-row tiles (launch_tiles_and_gather)
   Meta* meta;
   const moe_qweights* qw;
+  int* status;                // device status word (MOE_DEVFAULT_FP16_RANGE)
 };
 // Pieces of split tail units the quantized passes can hold (at most one per resident warp).
 int quant_tail_cap();
@@ -190,10 +191,13 @@ cudaError_t launch_quant_act(const Shape& s, const QFfnPtrs& p, cudaStream_t st)
 cudaError_t launch_quant_ffn(const Shape& s, int bits, const QFfnPtrs& p, cudaStream_t st,
                              cudaEvent_t ev_mid = nullptr);
 
-cudaError_t launch_combine(const Shape& s, const uint16_t* y, const int32_t* slot_pos,
+// y_f32: the slot rows are fp32 (bf16 down path), else fp16.
+cudaError_t launch_combine(const Shape& s, const void* y, bool y_f32, const int32_t* slot_pos,
                            uint16_t* out, cudaStream_t st);
 
-cudaError_t launch_pack_f16(const uint16_t* src, uint16_t* dst, size_t n, cudaStream_t st);
+// fault (optional): MOE_DEVFAULT_FP16_RANGE is OR-ed in when a weight had to be clamped.
+cudaError_t launch_pack_f16(const uint16_t* src, uint16_t* dst, size_t n, int* fault,
+                            cudaStream_t st);
 
 cudaError_t launch_bias_update(int E, const int32_t* counts, float* bias, float decay, float rate,
                                cudaStream_t st);

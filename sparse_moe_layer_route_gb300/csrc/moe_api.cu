@@ -100,7 +100,7 @@ WsLayout ws_layout(const Shape& s) {
   L.tail_acc = take(quant ? 4ull * quant_tail_cap() * 16 * 32 : 0);
   L.tail_ticket = take(quant ? 4ull * 2 * quant_tail_cap() : 0);
   L.h = take(2ull * s.rows * s.f);
-  L.y = take(2ull * s.rows * s.d);
+  L.y = take(4ull * s.rows * s.d);  // fp32 rows on the bf16 down path, fp16 otherwise
   L.x_stage = take(2ull * s.T * s.d);
   L.u_stage = take(s.mode == MOE_ROUTE_GUMBEL ? 4ull * s.T * s.E : 0);
   L.out_stage = take(2ull * s.T * s.d);
@@ -265,7 +265,7 @@ moe_status ffn_impl(const Shape& s, const WsLayout& L, void* ws, const uint16_t*
                     const int32_t* perm_slot, const int32_t* offsets, const float* topk_w,
                     const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wd,
                     const uint16_t* Wsg, const uint16_t* Wsu, const uint16_t* Wsd,
-                    const uint16_t* Wd16, const uint16_t* Wsd16, uint16_t* y,
+                    const uint16_t* Wd16, const uint16_t* Wsd16, void* y,
                     cudaStream_t st, bool tiles_built = false, cudaEvent_t ev_gathered = nullptr,
                     cudaEvent_t ev_gate_up = nullptr) {
   cudaError_t e = launch_tiles_and_gather(s, x, perm_slot, offsets, at<uint16_t>(ws, L.xp),
@@ -306,7 +306,7 @@ bool qweights_ok(const moe_config* c, const moe_qweights* q) {
 
 moe_status qffn_impl(const Shape& s, int bits, const WsLayout& L, void* ws, const uint16_t* x,
                      const int32_t* perm_slot, const int32_t* offsets, const float* topk_w,
-                     const moe_qweights* qw, uint16_t* y, cudaStream_t st,
+                     const moe_qweights* qw, void* y, cudaStream_t st,
                      bool tiles_built = false, cudaEvent_t ev_gathered = nullptr,
                      cudaEvent_t ev_gate_up = nullptr) {
   if (!tiles_built &&
@@ -324,12 +324,13 @@ moe_status qffn_impl(const Shape& s, int bits, const WsLayout& L, void* ws, cons
   if (ev_gathered != nullptr && cudaEventRecord(ev_gathered, st) != cudaSuccess)
     return MOE_ERR_CUDA;
   p.h = at<uint16_t>(ws, L.h);
-  p.y = y;
+  p.y = static_cast<uint16_t*>(y);
   p.perm_slot = perm_slot;
   p.topk_w = topk_w;
   p.tiles = at<TileEntry>(ws, L.tiles);
   p.meta = at<Meta>(ws, L.meta);
   p.qw = qw;
+  p.status = at<int>(ws, L.status);
   return cuda_status(launch_quant_ffn(s, bits, p, st, ev_gate_up));
 }
 
@@ -387,7 +388,9 @@ moe_status layer_impl(const moe_config* cfg, const moe_weights* w, const uint16_
       return r;
   }
   if (!mark(2)) return MOE_ERR_CUDA;
-  uint16_t* y = at<uint16_t>(ws, L.y);
+  void* y = at<void>(ws, L.y);
+  // slot rows in fp32 on the bf16 down path (full range), else fp16
+  const bool y_f32 = !quant && w->W_down_f16 == nullptr;
   if (quant)
     r = qffn_impl(s, cfg->weight_bits, L, ws, x, perm_slot, offsets, gw, w->quant, y, st, true,
                   ev ? ev[3] : nullptr, ev ? ev[4] : nullptr);
@@ -397,7 +400,7 @@ moe_status layer_impl(const moe_config* cfg, const moe_weights* w, const uint16_
                  true, ev ? ev[3] : nullptr, ev ? ev[4] : nullptr);
   if (r != MOE_OK) return r;
   if (!mark(5)) return MOE_ERR_CUDA;
-  if ((r = cuda_status(launch_combine(s, y, slot_pos, out, st))) != MOE_OK) return r;
+  if ((r = cuda_status(launch_combine(s, y, y_f32, slot_pos, out, st))) != MOE_OK) return r;
   return mark(6) ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -540,7 +543,7 @@ moe_status moe_grouped_ffn(const moe_config* cfg, const uint16_t* x, const int32
                            const uint16_t* W_up, const uint16_t* W_down,
                            const uint16_t* Wsh_gate, const uint16_t* Wsh_up,
                            const uint16_t* Wsh_down, const uint16_t* W_down_f16,
-                           const uint16_t* Wsh_down_f16, uint16_t* y_slot, void* ws,
+                           const uint16_t* Wsh_down_f16, void* y_slot, void* ws,
                            size_t ws_bytes, moe_stream_t stream) {
   moe_status r = check_cfg(cfg);
   if (r != MOE_OK) return r;
@@ -558,15 +561,18 @@ moe_status moe_grouped_ffn(const moe_config* cfg, const uint16_t* x, const int32
                   Wsh_up, Wsh_down, W_down_f16, Wsh_down_f16, y_slot, (cudaStream_t)stream);
 }
 
-moe_status moe_combine(const moe_config* cfg, const uint16_t* y_slot, const int32_t* slot_pos,
-                       uint16_t* out, void* ws, size_t ws_bytes, moe_stream_t stream) {
+moe_status moe_combine(const moe_config* cfg, const void* y_slot, int32_t y_type,
+                       const int32_t* slot_pos, uint16_t* out, void* ws, size_t ws_bytes,
+                       moe_stream_t stream) {
   moe_status r = check_cfg(cfg);
   if (r != MOE_OK) return r;
+  if (y_type != MOE_Y_F16 && y_type != MOE_Y_F32) return MOE_ERR_INVALID_ARG;
   if (cfg->T == 0) return MOE_OK;
   if (!y_slot || !slot_pos || !out) return MOE_ERR_INVALID_ARG;
   if ((r = check_ws(cfg, ws, ws_bytes)) != MOE_OK) return r;
   const Shape s = make_shape(*cfg);
-  return cuda_status(launch_combine(s, y_slot, slot_pos, out, (cudaStream_t)stream));
+  return cuda_status(
+      launch_combine(s, y_slot, y_type == MOE_Y_F32, slot_pos, out, (cudaStream_t)stream));
 }
 
 moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const uint16_t* x,
@@ -614,11 +620,11 @@ moe_status moe_layer_forward_host(const moe_config* cfg, const moe_weights* w,
 }
 
 moe_status moe_pack_f16(const uint16_t* src_bf16, uint16_t* dst_f16, size_t n,
-                        moe_stream_t stream) {
+                        int32_t* fault_bits, moe_stream_t stream) {
   if (!src_bf16 || !dst_f16 || n == 0) return MOE_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(src_bf16) | reinterpret_cast<uintptr_t>(dst_f16)) % 16 != 0)
     return MOE_ERR_INVALID_ARG;
-  return cuda_status(launch_pack_f16(src_bf16, dst_f16, n, (cudaStream_t)stream));
+  return cuda_status(launch_pack_f16(src_bf16, dst_f16, n, fault_bits, (cudaStream_t)stream));
 }
 
 moe_status moe_bias_update(int32_t E, const int32_t* counts, float* expert_bias, float decay,

@@ -124,6 +124,7 @@ struct QArgs {
   float* tail_acc;            // partial accumulators of split tail units (see qffn_kernel)
   int* tail_ticket;           // pieces finished per split tail unit (zero between launches)
   int tail_cap;               // pieces tail_acc holds
+  int* status;                // MOE_DEVFAULT_FP16_RANGE when an fp16 output value is clamped
   int E, K, N, top_k;
 };
 
@@ -199,6 +200,11 @@ __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], 
 __device__ __forceinline__ uint16_t f16_sat(float v) {
   return __half_as_ushort(__float2half_rn(fminf(fmaxf(v, -65504.f), 65504.f)));
 }
+
+// Magnitude bits of a float with the sign cleared (they order as |v|; NaN above infinity). From
+// kF16Clamp (65520.0f) on, a value is past the largest finite fp16 and f16_sat clamps it.
+__device__ __forceinline__ uint32_t mag_bits(float v) { return __float_as_uint(v) & 0x7FFFFFFFu; }
+constexpr uint32_t kF16Clamp = 0x477FF000u;
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
@@ -372,6 +378,7 @@ __global__ void __launch_bounds__(kQThreads, MODE == 0 ? (BITS == 8 ? 4 : 1) : 0
   }
   const int work = full + tail * S;
   constexpr int F = NM * TL * 4;  // accumulators per lane
+  uint32_t clamp = 0u;             // largest magnitude this lane stored in fp16 (mag_bits)
   while (true) {
     int v = 0;
     if (lane == 0) v = atomicAdd(counter, 1);
@@ -530,10 +537,13 @@ __global__ void __launch_bounds__(kQThreads, MODE == 0 ? (BITS == 8 ? 4 : 1) : 0
         } else {
           v = gate * acc[0][t][i];
         }
+        clamp = max(clamp, mag_bits(v));
         a.out[orow * a.N + col] = f16_sat(v);
       }
     }
   }
+  if (__any_sync(0xffffffffu, clamp >= kF16Clamp) && lane == 0)
+    atomicOr(a.status, MOE_DEVFAULT_FP16_RANGE);
 }
 
 }  // namespace
@@ -574,6 +584,7 @@ cudaError_t launch_quant_ffn(const Shape& s, int bits, const QFfnPtrs& p, cudaSt
   a.top_k = s.k;
   a.tail_acc = p.tail_acc;
   a.tail_cap = p.tail_cap;
+  a.status = p.status;
   a.tail_ticket = p.tail_ticket;  // gate/up; the down pass uses the next tail_cap
   const int sms = num_sms();
   // persistent: as many CTAs as fit (work units come from the counters in Meta)

@@ -25,7 +25,9 @@ def run_case(T, d, E, k, f, S, C, skew, seed, f16=True):
     dev = "cuda"
     mc = M.MoeConfig.make(T, d, E, k, f, n_shared=S, capacity_override=C)
     x = inp["x"].to(dev)
-    y = torch.full((T * k + S * T, d), float("nan"), dtype=torch.float16, device=dev)
+    # slot rows: fp16 on the fp16 down path, fp32 on the bf16 one
+    y = torch.full((T * k + S * T, d), float("nan"), dtype=torch.float16 if f16 else torch.float32,
+                   device=dev)
     ws = M.alloc_workspace(mc)
     Wd16 = M.packed_f16(inp["W_down"]) if f16 else None
     Wsd16 = M.packed_f16(inp["Ws_down"]) if (f16 and S > 0) else None
@@ -67,7 +69,8 @@ def test_grouped_ffn_matches_oracle(T, d, E, k, f, S, C, skew):
 @pytest.mark.parametrize("T,d,E,k,f,S", [(300, 256, 8, 2, 512, 0), (257, 192, 5, 2, 320, 1),
                                          (129, 128, 4, 1, 128, 0)])
 def test_grouped_ffn_bf16_down_path(T, d, E, k, f, S):
-    """The path without the fp16 copy of W_down: H carried in bf16, down GEMM in bf16."""
+    """The path without the fp16 copy of W_down: H carried in bf16, down GEMM in bf16, slot rows
+    in fp32."""
     run_case(T, d, E, k, f, S, 0, None, seed=T + 1, f16=False)
 
 
@@ -76,11 +79,24 @@ def test_pack_f16_matches_torch_conversion():
     src = (torch.randn(1000003, generator=g, device="cuda") * 3).to(torch.bfloat16)
     src[:6] = torch.tensor([0.0, -0.0, 1e-6, -2.0 ** -20, 65504.0, 1.5e5], dtype=torch.bfloat16)
     dst = torch.empty(src.shape, dtype=torch.float16, device="cuda")
-    M.pack_f16(src, dst)
+    fault = torch.zeros(1, dtype=torch.int32, device="cuda")
+    M.pack_f16(src, dst, fault_bits=fault)
     torch.cuda.synchronize()
     want = src.float().clamp(-65504, 65504).to(torch.float16)
     assert torch.equal(dst.view(torch.int16), want.view(torch.int16))
     assert dst[5].item() == 65504.0
+    assert int(fault.item()) == M.DEVFAULT_FP16_RANGE      # 1.5e5 was clamped, and reported
+    # the largest bf16 below fp16's limit converts without a report; the next one is clamped
+    fault.zero_()
+    ok = torch.tensor([65280.0, -65280.0, 1.0, 0.0, 2.0, 3.0, 4.0, 5.0], dtype=torch.bfloat16,
+                      device="cuda")
+    M.pack_f16(ok, torch.empty(8, dtype=torch.float16, device="cuda"), fault_bits=fault)
+    torch.cuda.synchronize()
+    assert int(fault.item()) == 0
+    M.pack_f16(ok * 0 - 65536.0, torch.empty(8, dtype=torch.float16, device="cuda"),
+               fault_bits=fault)
+    torch.cuda.synchronize()
+    assert int(fault.item()) == M.DEVFAULT_FP16_RANGE
 
 
 def test_grouped_ffn_empty_experts():

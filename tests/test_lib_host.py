@@ -122,8 +122,11 @@ def test_entry_points_validate_before_any_launch(lib):
     assert lib.moe_layer_forward(ctypes.byref(cfg), ctypes.byref(wt), fake, None, fake, None,
                                  fake, need, None) == 1
     # pack: NULL / misaligned pointers
-    assert lib.moe_pack_f16(None, fake, 16, None) == 1
-    assert lib.moe_pack_f16(fake + 2, fake, 16, None) == 1
+    assert lib.moe_pack_f16(None, fake, 16, None, None) == 1
+    assert lib.moe_pack_f16(fake + 2, fake, 16, None, None) == 1
+    # combine: the slot rows' type must be one of the two
+    assert lib.moe_combine(ctypes.byref(cfg), fake, 2, fake, fake, fake, need, None) == 1
+    assert lib.moe_combine(ctypes.byref(cfg), fake, -1, fake, fake, fake, need, None) == 1
     w = M.MoeWeights()
     assert lib.moe_layer_forward(ctypes.byref(cfg), ctypes.byref(w), fake, None, fake, None,
                                  fake, need, None) == 1
@@ -188,7 +191,7 @@ def test_empty_batch_is_a_no_op_on_the_host(lib):
     assert lib.moe_overflow_reroute(ctypes.byref(cfg), z, z, z, z, z, z, z, z, z, 0, z) == 0
     assert lib.moe_grouped_ffn(ctypes.byref(cfg), z, z, z, z, z, z, z, z, z, z, z, z, z, z, 0,
                                z) == 0
-    assert lib.moe_combine(ctypes.byref(cfg), z, z, z, z, 0, z) == 0
+    assert lib.moe_combine(ctypes.byref(cfg), z, 0, z, z, z, 0, z) == 0
     assert lib.moe_layer_forward(ctypes.byref(cfg), z, z, z, z, z, z, 0, z) == 0
     assert lib.moe_layer_forward_host(ctypes.byref(cfg), z, z, z, z, z, 0, z) == 0
     q = M.MoeConfig.make(0, 128, 8, 2, 128, weight_bits=8)
