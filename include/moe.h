@@ -381,6 +381,20 @@ moe_status moe_layer_forward_profiled(const moe_config* cfg, const moe_weights* 
 moe_status moe_bias_update(int32_t E, const int32_t* counts, float* expert_bias, float decay,
                            float rate, moe_stream_t stream);
 
+/* Failure-detection check of this device: runs the library's two kinds of bounded device wait,
+ * each against a condition that never comes true, with a wait limit of limit_ns (100 us .. 2 s;
+ * the layer's own waits use 2 s). One is the mbarrier wait of the tensor-core pipelines (a
+ * barrier no one arrives on), the other the grid barrier of the overflow re-route's proposal
+ * rounds (one of its two CTAs skips its arrival). Each must give up after about limit_ns, record
+ * MOE_DEVFAULT_PIPELINE_TIMEOUT in the status word of ws and return, leaving nothing in flight
+ * and the context usable. expired: device int32[2], set to 1 for each wait that gave up (0 would
+ * mean a wait saw its condition come true). ws: a workspace initialised by moe_workspace_init
+ * (its first 512 bytes are used). No counterpart in the source pages, whose overflow circuit
+ * breaker ("参数规模与稀疏激活的真相拆解", §3.2) is the analogue on the serving side. Read the
+ * result with moe_device_status, which then returns MOE_ERR_DEVICE_FAULT with that bit. */
+moe_status moe_check_bounded_waits(int64_t limit_ns, int32_t* expired, void* ws, size_t ws_bytes,
+                                   moe_stream_t stream);
+
 /* Synchronises stream, reads the device status word of ws into *fault_bits (MOE_DEVFAULT_*),
  * clears it, and returns MOE_ERR_DEVICE_FAULT if any bit was set, MOE_ERR_CUDA if the stream
  * reported an error, else MOE_OK. */

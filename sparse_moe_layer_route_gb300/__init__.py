@@ -21,10 +21,10 @@ DEVFAULT_FP16_RANGE = 0x8
 Y_F16, Y_F32 = 0, 1
 
 EXPORTS = ("moe_workspace_size", "moe_workspace_init", "moe_prepare_router", "moe_route",
-           "moe_permute",
-           "moe_permute_noalloc", "moe_overflow_reroute",
-           "moe_grouped_ffn", "moe_grouped_ffn_quantized", "moe_quantize_weights", "moe_combine", "moe_layer_forward", "moe_layer_forward_profiled",
-           "moe_layer_forward_host", "moe_pack_f16", "moe_bias_update", "moe_device_status",
+           "moe_permute", "moe_permute_noalloc", "moe_overflow_reroute", "moe_grouped_ffn",
+           "moe_grouped_ffn_quantized", "moe_quantize_weights", "moe_combine",
+           "moe_layer_forward", "moe_layer_forward_profiled", "moe_layer_forward_host",
+           "moe_pack_f16", "moe_bias_update", "moe_check_bounded_waits", "moe_device_status",
            "moe_status_string")
 
 
@@ -115,6 +115,7 @@ def lib():
         L.moe_pack_f16.argtypes = [P, P, S, P, P]
         L.moe_bias_update.argtypes = [ctypes.c_int32, P, P, ctypes.c_float, ctypes.c_float, P]
         L.moe_device_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_int32)]
+        L.moe_check_bounded_waits.argtypes = [ctypes.c_int64, P, P, S, P]
         L.moe_status_string.argtypes = [I]
         L.moe_status_string.restype = ctypes.c_char_p
         for name in EXPORTS:
@@ -336,6 +337,13 @@ def bias_update(counts, expert_bias, decay=0.99, rate=0.01, stream=None):
     """In place: expert_bias <- decay*expert_bias - rate*counts/(mean(counts)+1e-8)."""
     _check(lib().moe_bias_update(expert_bias.numel(), _ptr(counts), _ptr(expert_bias), decay, rate,
                                  _stream(stream)), "moe_bias_update")
+
+
+def check_bounded_waits(limit_ns, expired, ws, stream=None):
+    """Both bounded device waits against conditions that never come true (limit_ns each);
+    expired: int32 device tensor of 2. Read the result with device_status()."""
+    _check(lib().moe_check_bounded_waits(int(limit_ns), _ptr(expired), _ptr(ws), ws.numel(),
+                                         _stream(stream)), "moe_check_bounded_waits")
 
 
 def device_status(ws, stream=None) -> int:

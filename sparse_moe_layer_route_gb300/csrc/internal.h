@@ -49,8 +49,10 @@ struct Meta {
   int reroute_rounds; // proposal rounds of the last overflow re-route (diagnostic)
   int work[2];        // next work unit of the quantized gate/up and down passes
   int reroute_exact;  // first windows listed for the re-route's exact pass (zero between calls)
-  int pad[56];
+  unsigned check_arrive, check_gen;  // grid barrier of moe_check_bounded_waits (arrivals zero)
+  int pad[54];
 };
+static_assert(sizeof(Meta) == 256, "moe_workspace_init clears the status word and this block");
 
 // Offsets of every buffer carved from the caller's workspace (bytes, 256-aligned).
 struct WsLayout {
@@ -122,6 +124,9 @@ struct RerouteArgs {
   float tau;
 };
 cudaError_t launch_reroute(const RerouteArgs& a, cudaStream_t st);
+// moe_check_bounded_waits: both bounded waits against conditions that never come true.
+cudaError_t launch_wait_check(uint64_t limit_ns, int* status, int32_t* expired,
+                              unsigned* arrive, unsigned* gen, cudaStream_t st);
 
 // Dispatch: histogram (its last CTA also scans, and builds the row-tile list into tiles/meta
 // unless tiles is nullptr), then the stable scatter. *ticket is zero before and after.

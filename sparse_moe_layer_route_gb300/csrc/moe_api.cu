@@ -634,6 +634,17 @@ moe_status moe_bias_update(int32_t E, const int32_t* counts, float* expert_bias,
   return cuda_status(launch_bias_update(E, counts, expert_bias, decay, rate, (cudaStream_t)stream));
 }
 
+moe_status moe_check_bounded_waits(int64_t limit_ns, int32_t* expired, void* ws,
+                                   size_t ws_bytes, moe_stream_t stream) {
+  if (ws == nullptr || ws_bytes < 512 || (reinterpret_cast<uintptr_t>(ws) % 256) != 0)
+    return MOE_ERR_WORKSPACE;
+  if (expired == nullptr || limit_ns < 100000 || limit_ns > 2000000000) return MOE_ERR_INVALID_ARG;
+  Meta* meta = reinterpret_cast<Meta*>(static_cast<char*>(ws) + 256);  // ws_layout's meta block
+  return cuda_status(launch_wait_check((uint64_t)limit_ns, static_cast<int*>(ws), expired,
+                                       &meta->check_arrive, &meta->check_gen,
+                                       (cudaStream_t)stream));
+}
+
 moe_status moe_device_status(void* ws, moe_stream_t stream, int32_t* fault_bits) {
   if (ws == nullptr) return MOE_ERR_WORKSPACE;
   cudaStream_t st = (cudaStream_t)stream;

@@ -41,6 +41,7 @@
 #include <cstdint>
 
 #include "internal.h"
+#include "ptx.cuh"
 #include "route_common.cuh"
 
 namespace moe {
@@ -444,10 +445,11 @@ __global__ void __launch_bounds__(kThreads) reroute_exact_kernel(const RerouteAr
   }
 }
 
-// Grid-wide barrier for the cooperative launch. Returns false when the wait ran past its bound
+// Grid-wide barrier for the cooperative launch. Returns false when the wait ran past limit_ns
 // (status bit set); the caller then leaves the rounds.
 __device__ bool grid_barrier(unsigned* arrive, volatile unsigned* gen, unsigned& my_gen,
-                             int* status, volatile int* fail) {
+                             int* status, volatile int* fail,
+                             uint64_t limit_ns = kBarrierLimitNs) {
   __syncthreads();
   if (threadIdx.x == 0) {
     const unsigned g = my_gen;
@@ -459,7 +461,7 @@ __device__ bool grid_barrier(unsigned* arrive, volatile unsigned* gen, unsigned&
     } else {
       const uint64_t t0 = globaltimer();
       while (*gen == g) {
-        if (globaltimer() - t0 > kBarrierLimitNs) {
+        if (globaltimer() - t0 > limit_ns) {
           atomicOr(status, MOE_DEVFAULT_PIPELINE_TIMEOUT);
           *fail = 1;
           break;
@@ -472,6 +474,39 @@ __device__ bool grid_barrier(unsigned* arrive, volatile unsigned* gen, unsigned&
   }
   __syncthreads();
   return *fail == 0;
+}
+
+// Failure-detection check (moe_check_bounded_waits): the two kinds of bounded device wait, each
+// against a condition that never comes true, with a short limit. CTA 0 waits on an mbarrier
+// nobody arrives on (the wait of every tcgen05 pipeline, ptx::mbar_wait_bounded); CTA 1 enters
+// the grid barrier of the proposal rounds, on which CTA 0 never arrives. Both must give up after
+// limit_ns, record MOE_DEVFAULT_PIPELINE_TIMEOUT and return; expired[i] = 1 says wait i did.
+// Nothing else is in flight, so nothing is left behind.
+__global__ void __launch_bounds__(32) wait_check_kernel(uint64_t limit_ns, int* status,
+                                                        int32_t* expired, unsigned* arrive,
+                                                        unsigned* gen) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int flag;
+  griddep_wait();
+  if (blockIdx.x == 0) {
+    if (threadIdx.x == 0) {
+      const uint32_t b = ptx::smem_u32(&bar);
+      ptx::mbar_init(b, 1);
+      ptx::fence_mbarrier_init();
+      flag = 0;  // the abort flag of the CTA's other roles: never raised here
+      const bool ok = ptx::mbar_wait_bounded(b, 0u, &flag, status, MOE_DEVFAULT_PIPELINE_TIMEOUT,
+                                             limit_ns);
+      expired[0] = ok ? 0 : 1;
+    }
+  } else {
+    if (threadIdx.x == 0) flag = 0;
+    unsigned my_gen = *reinterpret_cast<volatile unsigned*>(gen);
+    const bool ok = grid_barrier(arrive, gen, my_gen, status, &flag, limit_ns);
+    if (threadIdx.x == 0) {
+      expired[1] = ok ? 0 : 1;
+      atomicExch(arrive, 0u);  // this CTA's arrival is withdrawn: the counter is clean again
+    }
+  }
 }
 
 __global__ void __launch_bounds__(kThreads) reroute_da_kernel(const RerouteArgs a) {
@@ -706,6 +741,12 @@ cudaError_t launch_reroute(const RerouteArgs& args, cudaStream_t st) {
   if (err != cudaSuccess) return err;
   return launch_k(reroute_finalize_kernel, dim3(tok_blocks < 4 * sms ? tok_blocks : 4 * sms),
                   dim3(kThreads), 0, st, a);
+}
+
+cudaError_t launch_wait_check(uint64_t limit_ns, int* status, int32_t* expired,
+                              unsigned* arrive, unsigned* gen, cudaStream_t st) {
+  return launch_k(wait_check_kernel, dim3(2), dim3(32), 0, st, limit_ns, status, expired, arrive,
+                  gen);
 }
 
 }  // namespace moe

@@ -131,6 +131,12 @@ def test_entry_points_validate_before_any_launch(lib):
     assert lib.moe_layer_forward(ctypes.byref(cfg), ctypes.byref(w), fake, None, fake, None,
                                  fake, need, None) == 1
     assert lib.moe_workspace_init(None, 0, None) == 3
+    # the bounded-wait check: workspace, expired flags, limit range (100 us .. 2 s)
+    assert lib.moe_check_bounded_waits(1000000, fake, None, 512, None) == 3
+    assert lib.moe_check_bounded_waits(1000000, fake, fake, 256, None) == 3
+    assert lib.moe_check_bounded_waits(1000000, None, fake, 512, None) == 1
+    assert lib.moe_check_bounded_waits(99999, fake, fake, 512, None) == 1
+    assert lib.moe_check_bounded_waits(2000000001, fake, fake, 512, None) == 1
 
 
 def test_status_strings(lib):
