@@ -13,8 +13,12 @@ workspaces, so the other calls' copies overlap one call's compute, and events br
 loop. The one-call-at-a-time latency is reported beside it as `e2e.serial`. `roofline` is for the
 step's dominant kernel, timed live with events recorded between the layer's phases
 (moe_layer_forward_profiled). `cpu_baseline` times the fp64 CPU
-oracle on a bounded sample of the same workload. With N > 1 (torchrun) every rank runs an
-independent replica of the layer (the layer has no cross-token exchange): value = N*T / max time.
+oracle on a bounded sample of the same workload. The headline workload is the largest one that
+fits one GPU (the skewed prefill with a capacity limit); `per_config` times the fine-grained
+prefill, the Gumbel prefill and the decode shape in the same run (device-resident inputs, L2
+flushed between steps), each with its own layer and dominant-kernel rooflines.
+With N > 1 (torchrun) every rank runs an independent replica of the layer (the layer has no
+cross-token exchange): value = N*T / max time; `per_config` is then left out.
 `--impl reference` times the oracle alone (rank 0; the other ranks exit) on the same workload.
 """
 from __future__ import annotations
@@ -34,27 +38,44 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "MoE-layer tokens/s (bf16, 1 GB300) and achieved fraction of roofline"
-DEFAULT_CONFIG = "fine_grained"
+DEFAULT_CONFIG = "skewed_cap"  # the largest single-GPU workload: 11.75 GB of algorithmic bytes
+# timed in the same run after the headline workload, each reported under "per_config"
+PER_CONFIG = ("fine_grained", "gumbel", "decode")
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# (workload, phase) -> DRAM bytes read + written per launch, from one ncu capture of the current
-# kernel (profiles/grouped_gemm_fine_grained.md). Re-capture after changing the kernel.
-NCU_TRAFFIC = {("fine_grained", "gate_up_gemm"): (879.400448e6 + 67.677184e6),
-               ("fine_grained", "down_gemm"): (473.339648e6 + 95.139840e6)}
-# captured on the 32-expert decode shape (31 routed experts touched + the shared one); every
-# touched expert's weights are read once, so a launch's DRAM bytes scale with the experts touched:
-# (DRAM read per touched expert, DRAM write per launch)
-NCU_TRAFFIC_PER_EXPERT = {("decode", "gate_up_gemm"): (1.884023e9 / 32, 3.743488e6),
-                          ("decode", "down_gemm"): (0.942734e9 / 32, 1.710592e6)}
+# DRAM bytes per launch of the dominant kernels, from ncu captures of the current kernels (one
+# line per workload and phase; see the file's header). Re-captured whenever a kernel changes.
+NCU_DRAM_FILE = os.path.join(ROOT, "profiles", "ncu_dram_bytes.txt")
 
 
-def ncu_traffic(cfg, kernel, n_touched):
-    """DRAM bytes per launch of the dominant kernel from an ncu capture, or None."""
-    if (cfg.name, kernel) in NCU_TRAFFIC:
-        return NCU_TRAFFIC[(cfg.name, kernel)]
-    if (cfg.name, kernel) in NCU_TRAFFIC_PER_EXPERT:
-        per_expert, writes = NCU_TRAFFIC_PER_EXPERT[(cfg.name, kernel)]
-        return per_expert * (n_touched + cfg.S) + writes
+def read_ncu_dram(path=NCU_DRAM_FILE):
+    """{(workload, phase): (scaling, read_bytes, write_bytes, captured_alg_bytes)} from the
+    capture table."""
+    out = {}
+    if not os.path.exists(path):
+        return out
+    with open(path) as fh:
+        for line in fh:
+            f = line.split("#", 1)[0].split()
+            if len(f) >= 5:
+                out[(f[0], f[1])] = (f[2], float(f[3]), float(f[4]),
+                                     float(f[5]) if len(f) > 5 else None)
+    return out
+
+
+def ncu_traffic(cfg, kernel, alg_bytes, table=None):
+    """DRAM bytes (read + write) per launch of the dominant kernel from an ncu capture, or None.
+    'launch' lines hold one full launch of the workload. 'alg' lines were captured on a smaller
+    shape with the same rows per expert (the full launch exceeds a capture's size): their bytes
+    are scaled by the ratio of the full launch's algorithmic bytes to the captured launch's."""
+    t = read_ncu_dram() if table is None else table
+    if (cfg.name, kernel) not in t:
+        return None
+    scaling, rd, wr, alg_cap = t[(cfg.name, kernel)]
+    if scaling == "launch":
+        return rd + wr
+    if scaling == "alg" and alg_cap:
+        return (rd + wr) * alg_bytes / alg_cap
     return None
 
 
@@ -325,6 +346,130 @@ def config_dict(cfg):
 
 
 # ------------------------------------------------------------------------------ our arm
+def load_workload(M, W, cfg, dev):
+    """The workload's seeded inputs on the device and the one-time weight preparation (outside
+    any timed region): the router weights' transpose, and the fp16 re-encoding of W_down or the
+    group-wise quantization of every expert matrix. Returns (inp_host, inp, weights, keep,
+    pack_ms); `keep` holds the prepared tensors the weights struct points at."""
+    import torch
+    inp_host = W.make_inputs(cfg, weights_device=dev)
+    inp = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp_host.items()}
+    pk0, pk1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    pk0.record()
+    keep = {"W_g_t": M.prepare_router(inp["W_g"])}
+    if cfg.weight_bits:
+        names = ("W_gate", "W_up", "W_down", "Ws_gate", "Ws_up", "Ws_down")
+        keep["q"] = {n: (M.quantize_weights(inp[n], cfg.weight_bits) if inp.get(n) is not None
+                         else None) for n in names}
+        keep["qstruct"] = M.make_qweights(*[keep["q"][n] for n in names])
+    else:
+        keep["Wd16"] = M.packed_f16(inp["W_down"])
+        keep["Wsd16"] = (M.packed_f16(inp["Ws_down"]) if inp.get("Ws_down") is not None
+                         else None)
+    pk1.record()
+    torch.cuda.synchronize()
+    if cfg.weight_bits:
+        weights = M.make_weights(inp["W_g"], inp["bias"], None, None, None,
+                                 quant=keep["qstruct"], W_g_t=keep["W_g_t"])
+    else:
+        weights = M.make_weights(inp["W_g"], inp["bias"], inp["W_gate"], inp["W_up"],
+                                 inp["W_down"], inp.get("Ws_gate"), inp.get("Ws_up"),
+                                 inp.get("Ws_down"), keep["Wd16"], keep["Wsd16"],
+                                 W_g_t=keep["W_g_t"])
+    return inp_host, inp, weights, keep, pk0.elapsed_time(pk1)
+
+
+def timed_steps(step, flush, stream, n):
+    """Per-step ms of n calls of step(), each bracketed by CUDA events on the launching stream,
+    with L2 flushed before each."""
+    import torch
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    for i in range(n):
+        flush.fill_(i & 0xFF)
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+
+def phase_times(M, mc, weights, inp, out, ro, ws, flush, n):
+    """Median ms of each phase of n layer calls through moe_layer_forward_profiled (the same
+    kernels with events recorded between the phases); medians, so a host stall that lets the
+    queue drain inflates one call's phase and not the figure."""
+    import torch
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(n)]
+    for i in range(n):
+        flush.fill_(i & 0xFF)
+        M.layer_forward_profiled(mc, weights, inp["x"], inp.get("u"), out, ro, ws, evs[i])
+    torch.cuda.synchronize()
+    return {ph: statistics.median(e[j].elapsed_time(e[j + 1]) for e in evs)
+            for j, ph in enumerate(M.PROFILE_PHASES)}
+
+
+def workload_report(cfg, ms, phase_ms, counts_h, peaks, peak_src):
+    """Layer roofline, the dominant kernel's roofline, per-phase fractions and routing figures."""
+    C = M_capacity(cfg)
+    n_touched, n_kept = touched_experts(counts_h, C)
+    lr = layer_roofline(cfg, n_touched, n_kept, ms / 1e3, peaks)
+    dom = max(phase_ms, key=phase_ms.get)
+    fl, by = kernel_work(cfg, dom, n_touched, n_kept)
+    roof = roofline_for(dom, fl, by, phase_ms[dom] / 1e3, peaks)
+    roof["kernel"] = dom
+    roof["traffic"] = ncu_traffic(cfg, dom, by)
+    roof["peak_source"] = f"{peak_src} ({'bf16 burst' if roof['unit'] == 'TFLOP/s' else 'copy'})"
+    kernels = {}
+    for ph, t in phase_ms.items():
+        f_, b_ = kernel_work(cfg, ph, n_touched, n_kept)
+        r = roofline_for(ph, f_, b_, t / 1e3, peaks) if t > 0 else {}
+        kernels[ph] = {"us": t * 1e3, **{kk: r[kk] for kk in ("bound", "frac") if kk in r}}
+    routing = {"experts_hit": n_touched, "kept_slots": n_kept, "capacity": C,
+               "dropped_slots": cfg.T * cfg.k - n_kept, "max_load": max(counts_h),
+               "mean_load": cfg.T * cfg.k / cfg.E}
+    return lr, roof, kernels, routing
+
+
+def measure_other(M, W, name, dev, steps, warmup, peaks, peak_src, local):
+    """One more workload timed in the same process (device-resident inputs, L2 flushed between
+    steps, CUDA events): tokens/s, latency, layer and dominant-kernel rooflines, clocks."""
+    import torch
+    cfg = W.CONFIGS[name]
+    _, inp, weights, keep, _ = load_workload(M, W, cfg, dev)
+    mc = M.MoeConfig.from_layer(cfg)
+    ws = M.alloc_workspace(mc, dev)
+    out = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16, device=dev)
+    counts = torch.empty(cfg.E, dtype=torch.int32, device=dev)
+    slot_pos = torch.empty(cfg.T * cfg.k, dtype=torch.int32, device=dev)
+    ro = M.make_route_out(counts=counts, slot_pos=slot_pos)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        M.layer_forward(mc, weights, inp["x"], inp.get("u"), out, ro, ws)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    step_ms = timed_steps(step, flush, stream, steps)
+    clk = clocks.stop()
+    phase_ms = phase_times(M, mc, weights, inp, out, ro, ws, flush, steps)
+    faults = M.device_status(ws)
+    if faults:
+        raise SystemExit(f"device fault bits {faults:#x} in workload {name}")
+    ms = sum(step_ms) / len(step_ms)
+    lr, roof, kernels, routing = workload_report(cfg, ms, phase_ms, counts.cpu().tolist(), peaks,
+                                                 peak_src)
+    del inp, weights, keep, ws, flush
+    return {"workload": cfg.name + ": " + cfg.description, "value": cfg.T / (ms / 1e3),
+            "unit": "tokens/s", "ms_per_step": ms, "ms_per_step_median": statistics.median(step_ms),
+            "steps": steps, "warmup": warmup, "layer_roofline": lr, "roofline": roof,
+            "kernels": kernels, "routing": routing, "clocks": clk,
+            "gpu_launches": launches_per_step(cfg) * steps}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -333,6 +478,8 @@ def main():
     ap.add_argument("--config", default=DEFAULT_CONFIG)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="time only the --config workload (no per_config object)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -357,33 +504,9 @@ def main():
     peaks, peak_src = load_peaks()
 
     dev = f"cuda:{local}"
-    inp_host = W.make_inputs(cfg, weights_device=dev)
-    inp = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp_host.items()}
+    inp_host, inp, weights, keep, pack_ms = load_workload(M, W, cfg, dev)
     mc = M.MoeConfig.from_layer(cfg)
     ws = M.alloc_workspace(mc, dev)
-    # one-time weight preparation (outside the timed layer): the fp16 re-encoding of W_down, or
-    # the group-wise quantization of every expert matrix, and the router weights' transpose
-    pk0, pk1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    pk0.record()
-    if cfg.weight_bits:
-        names = ("W_gate", "W_up", "W_down", "Ws_gate", "Ws_up", "Ws_down")
-        qmats = {n: (M.quantize_weights(inp[n], cfg.weight_bits) if inp.get(n) is not None
-                     else None) for n in names}
-        qstruct = M.make_qweights(*[qmats[n] for n in names])
-    else:
-        Wd16 = M.packed_f16(inp["W_down"])
-        Wsd16 = M.packed_f16(inp["Ws_down"]) if inp.get("Ws_down") is not None else None
-    W_g_t = M.prepare_router(inp["W_g"])
-    pk1.record()
-    torch.cuda.synchronize()
-    pack_ms = pk0.elapsed_time(pk1)
-    if cfg.weight_bits:
-        weights = M.make_weights(inp["W_g"], inp["bias"], None, None, None, quant=qstruct,
-                                 W_g_t=W_g_t)
-    else:
-        weights = M.make_weights(inp["W_g"], inp["bias"], inp["W_gate"], inp["W_up"],
-                                 inp["W_down"], inp.get("Ws_gate"), inp.get("Ws_up"),
-                                 inp.get("Ws_down"), Wd16, Wsd16, W_g_t=W_g_t)
     T, k, E, d = cfg.T, cfg.k, cfg.E, cfg.d
     out = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
     counts = torch.empty(E, dtype=torch.int32, device=dev)
@@ -428,15 +551,7 @@ def main():
     ms_median = statistics.median(step_ms)
 
     # ---- phase breakdown through the profiled entry point (same kernels, events in between)
-    n_prof = min(args.steps, 200)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(n_prof)]
-    for i in range(n_prof):
-        flush.fill_(i & 0xFF)
-        M.layer_forward_profiled(mc, weights, inp["x"], u, out, ro, ws, evs[i])
-    torch.cuda.synchronize()
-    # medians: a host stall that lets the queue drain inflates one step's phase, not the median
-    phase_ms = {ph: statistics.median(e[j].elapsed_time(e[j + 1]) for e in evs)
-                for j, ph in enumerate(M.PROFILE_PHASES)}
+    phase_ms = phase_times(M, mc, weights, inp, out, ro, ws, flush, min(args.steps, 200))
 
     # ---- the same step replayed from a CUDA graph (launch overhead removed; L2 still flushed)
     graph = graph_replay(step, flush, stream, min(args.steps, 200))
@@ -517,22 +632,23 @@ def main():
     if loop_dev_ms is not None:
         loop_dev_ms = max_over_ranks([loop_dev_ms], dist, dev)[0]
 
-    counts_h = counts.cpu().tolist()
-    C = M_capacity(cfg)
-    n_touched, n_kept = touched_experts(counts_h, C)
-    lr = layer_roofline(cfg, n_touched, n_kept, ms / 1e3, peaks)
-    dom = max(phase_ms, key=phase_ms.get)
-    fl, by = kernel_work(cfg, dom, n_touched, n_kept)
-    roof = roofline_for(dom, fl, by, phase_ms[dom] / 1e3, peaks)
-    roof["kernel"] = dom
-    roof["traffic"] = ncu_traffic(cfg, dom, n_touched)
-    roof["peak_source"] = f"{peak_src} ({'bf16 burst' if roof['unit'] == 'TFLOP/s' else 'copy'})"
-    kernels = {}
-    for ph in M.PROFILE_PHASES:
-        f_, b_ = kernel_work(cfg, ph, n_touched, n_kept)
-        r = roofline_for(ph, f_, b_, phase_ms[ph] / 1e3, peaks) if phase_ms[ph] > 0 else {}
-        kernels[ph] = {"us": phase_ms[ph] * 1e3, **{kk: r[kk] for kk in ("bound", "frac")
-                                                    if kk in r}}
+    lr, roof, kernels, routing = workload_report(cfg, ms, phase_ms, counts.cpu().tolist(), peaks,
+                                                 peak_src)
+    # ---- the oracle on the host cores, on a bounded sample of the same workload
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(cfg, inp_host_weights(inp_host, inp))
+    # ---- the other workloads, timed in the same run (one GPU only; the scaling runs skip them)
+    per_config = None
+    if world == 1 and not args.no_per_config:
+        del inp, weights, keep, ws, ws2, flush, x_h, u_h, out_h, out_d2
+        torch.cuda.empty_cache()
+        per_config = {}
+        for name in PER_CONFIG:
+            if name != cfg.name:
+                per_config[name] = measure_other(M, W, name, dev, min(args.steps, 100),
+                                                 args.warmup, peaks, peak_src, local)
+                torch.cuda.empty_cache()
 
     if rank != 0:
         return
@@ -566,15 +682,14 @@ def main():
                                                      "on device buffers (no copies)"})},
             "gpu_launches": launches_per_step(cfg) * args.steps,
             "clocks": clk,
-            "routing": {"experts_hit": n_touched, "kept_slots": n_kept, "capacity": C,
-                        "dropped_slots": T * k - n_kept,
-                        "max_load": max(counts_h), "mean_load": T * k / E},
+            "routing": routing,
             "ms_per_step_median": ms_median,
             "graph_replay": graph,
             "weight_pack_ms": pack_ms,
-            "wall_s_timed": wall}
-    if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(cfg, inp_host_weights(inp_host, inp))
+            "wall_s_timed": wall,
+            "per_config": per_config}
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()

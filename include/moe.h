@@ -273,10 +273,13 @@ moe_status moe_overflow_reroute(const moe_config* cfg, const uint16_t* x, const 
  *   Takes no workspace and allocates nothing (no cudaMalloc, cudaFree or allocating library
  *   call). Its scratch (per-block expert histograms and their running sums, 512 KB) is a
  *   file-scope static __device__ array that every GPU loading this library holds until the
- *   process exits. The first call on each device looks up that array's device address
- *   (cudaGetSymbolAddress) with that device current; make that first call before any stream
- *   capture. All calls share the one array, so calls whose executions overlap on the GPU
- *   (different streams, or several host threads) race and must be serialised by the caller.
+ *   process exits. Each call made outside stream capture looks up that array's device address
+ *   (cudaGetSymbolAddress) with the current device, so a device reset in between is harmless; a
+ *   call made while the stream is capturing uses the address found by the last call outside
+ *   capture on that device. So make one call outside capture before capturing (and again after
+ *   any device reset). All calls share the one array, so calls whose executions overlap on the
+ *   GPU (different streams, or several host threads) race and must be serialised by the
+ *   caller.
  *   fault_bits: optional device int32 the call clears and then ORs MOE_DEVFAULT_* bits into
  *   (NULL: faults are not reported; a bad index still only drops its slot).
  *   Returns MOE_ERR_UNSUPPORTED when T * top_k > MOE_NOALLOC_MAX_SLOTS (or the config is

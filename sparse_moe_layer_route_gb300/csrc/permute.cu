@@ -311,19 +311,24 @@ static __device__ __align__(256) int32_t g_noalloc_scratch[kNoallocInts];
 std::mutex g_noalloc_mu;
 void* g_noalloc_addr[64] = {nullptr};
 
-// Device address of g_noalloc_scratch on the current device. In host code the array's name
-// is only a host-side stand-in, so the address is looked up once per device (with that device
-// current) and cached.
-cudaError_t noalloc_scratch(int32_t** out) {
+// Device address of g_noalloc_scratch on the current device. In host code the array's name is
+// only a host-side stand-in, so the address comes from cudaGetSymbolAddress with the device
+// current. It is looked up afresh on every call made outside stream capture (a device reset, or
+// another context on the device, may have loaded the module at another address) and remembered
+// per device; a call made while `st` is capturing uses the address remembered from the last call
+// outside capture, and looks it up only if there is none yet.
+cudaError_t noalloc_scratch(cudaStream_t st, int32_t** out) {
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if ((err = cudaStreamIsCapturing(st, &cs)) != cudaSuccess) return err;
+  const bool slot = dev >= 0 && dev < 64;
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  void* p = (dev >= 0 && dev < 64) ? g_noalloc_addr[dev] : nullptr;
-  if (p == nullptr) {
-    err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (err != cudaSuccess) return err;
-    if (dev >= 0 && dev < 64) g_noalloc_addr[dev] = p;
+  void* p = slot ? g_noalloc_addr[dev] : nullptr;
+  if (cs == cudaStreamCaptureStatusNone || p == nullptr) {
+    if ((err = cudaGetSymbolAddress(&p, g_noalloc_scratch)) != cudaSuccess) return err;
+    if (slot) g_noalloc_addr[dev] = p;
   }
   *out = static_cast<int32_t*>(p);
   return cudaSuccess;
@@ -335,7 +340,7 @@ cudaError_t launch_permute_noalloc(const Shape& s, const int32_t* topk_idx, int3
                                    int* fault_bits, cudaStream_t st) {
   if (s.TK > MOE_NOALLOC_MAX_SLOTS || s.E > kMaxE) return cudaErrorInvalidValue;
   int32_t* scratch = nullptr;
-  cudaError_t err = noalloc_scratch(&scratch);
+  cudaError_t err = noalloc_scratch(st, &scratch);
   if (err != cudaSuccess) return err;
   int* status = fault_bits;
   if (status != nullptr) {

@@ -3,15 +3,18 @@ plugin that a host application hands only input and output buffers, or a latency
 that may not call cudaMalloc/cudaFree). Its scratch is the library's own static device array, so
 it takes no workspace.
 
-Checked through the C ABI against moe_permute (the workspace-based entry point) on two calls in a
-row with different routing, so a call that leaned on the previous call's leftovers in the shared
-static array would show up. Dispatch outputs are integers: the comparison is exact."""
+Checked through the C ABI against the oracle's dispatch (the counting-sort definition of
+"参数规模与稀疏激活的真相拆解", §3.2's capacity rule) and against moe_permute (the workspace-based
+entry point) on two calls in a row with different routing, so a call that leaned on the previous
+call's leftovers in the shared static array would show up. Dispatch outputs are integers: the
+comparisons are exact."""
 import ctypes
 
 import numpy as np
 import pytest
 import torch
 
+import oracle as O
 import sparse_moe_layer_route_gb300 as M
 
 pytestmark = pytest.mark.gpu
@@ -35,7 +38,8 @@ def test_noalloc_permute_matches_workspace_permute_twice():
     # two consecutive calls, different sizes and routing; the second has fewer dispatch blocks
     # and a capacity limit, so stale histogram rows from the first call would corrupt it
     for seed, (T, E, k, cap) in enumerate([(20000, 128, 8, 0), (3001, 64, 6, 150)]):
-        idx = torch.as_tensor(_routing(seed, T, E, k, 1.2), device=dev)
+        idx_np = _routing(seed, T, E, k, 1.2)
+        idx = torch.as_tensor(idx_np, device=dev)
         cfg = M.MoeConfig.make(T, 64, E, k, 64, capacity_override=cap)
         ref = _outputs(T, E, k, dev)
         ws = M.alloc_workspace(cfg)
@@ -50,7 +54,9 @@ def test_noalloc_permute_matches_workspace_permute_twice():
         torch.cuda.synchronize()
         assert M.device_status(ws) == 0
         assert int(fault.item()) == 0          # cleared by the call, no fault recorded
+        want = O.permute(idx_np, E, cap if cap else None)
         for name, a, b in zip(("counts", "offsets", "perm_slot", "slot_pos"), ref, got):
+            assert np.array_equal(b.cpu().numpy(), want[name]), name + " differs from the oracle"
             assert torch.equal(a, b), name
 
 
