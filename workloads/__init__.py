@@ -114,6 +114,17 @@ CONFIGS = {
     "gumbel": LayerConfig(
         "gumbel", T=8192, d=4096, E=16, k=2, f=14336, S=0, mode=GUMBEL, tau=0.5, seed=4,
         description="Gumbel top-2: T=8192 d=4096 E=16 k=2 d_ff=14336, tau=0.5"),
+    # profiling sizes of the two prefill shapes: the same rows per expert (gumbel: T k / E =
+    # 1024; skewed: mean 256 with capacity 320) at about 1.4 GB of expert weights each
+    "gumbel_e4": LayerConfig(
+        "gumbel_e4", T=2048, d=4096, E=4, k=2, f=14336, S=0, mode=GUMBEL, tau=0.5, seed=4,
+        description="Gumbel top-2 with 4 experts: T=2048 d=4096 k=2 d_ff=14336 (profiling "
+                    "size)"),
+    "skewed_e16": LayerConfig(
+        "skewed_e16", T=2048, d=7168, E=16, k=2, f=2048, S=0, mode=BIAS_SELECT,
+        capacity_factor=1.25, seed=3, bias="zipf", zipf_s=1.1,
+        description="skewed prefill with 16 experts: T=2048 d=7168 k=2 d_ff=2048, Zipf(1.1) "
+                    "bias, capacity ceil(1.25*T*k/E) = 320 (profiling size)"),
 }
 
 
