@@ -96,6 +96,12 @@ CONFIGS = {
         "skewed_reroute_f128", T=16384, d=7168, E=128, k=2, f=128, S=0, mode=BIAS_SELECT,
         capacity_factor=1.25, seed=3, bias="zipf", zipf_s=1.1, reroute=True,
         description="the skewed prefill with re-route at d_ff=128 (profiling size)"),
+    # profiling size of the skewed prefill's router and dispatch: the same routing without the
+    # re-route, d_ff = 128 (about 2.5 GB on the device with the workspace)
+    "skewed_f128": LayerConfig(
+        "skewed_f128", T=16384, d=7168, E=128, k=2, f=128, S=0, mode=BIAS_SELECT,
+        capacity_factor=1.25, seed=3, bias="zipf", zipf_s=1.1,
+        description="the skewed prefill at d_ff=128 (profiling size of its router)"),
     # profiling size of the decode shape (32 routed experts: about 3 GB of weights on the device)
     "decode_e32": LayerConfig(
         "decode_e32", T=64, d=7168, E=32, k=2, f=2048, S=1, mode=PLAIN, seed=2,
