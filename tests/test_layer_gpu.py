@@ -25,6 +25,11 @@ SMALL = [
     dict(T=1024, d=256, E=4, k=2, f=256, S=1),
     dict(T=700, d=512, E=4, k=2, f=384, mode=W.BIAS_SELECT, bias="normal", bias_var=0.1),
     dict(T=1500, d=256, E=8, k=3, f=128, S=2, mode=W.GUMBEL, tau=0.5),
+    # rows of 2-4 column groups per combine thread (a CTA per token): with a capacity limit and
+    # a shared expert (d = 2560), and without either (d = 8192)
+    dict(T=400, d=2560, E=8, k=2, f=128, S=1, mode=W.BIAS_SELECT, bias="zipf",
+         capacity_factor=1.0),
+    dict(T=320, d=8192, E=4, k=1, f=128),
 ]
 
 
@@ -40,6 +45,14 @@ def test_layer_matches_oracle(kw):
 def test_layer_bf16_down_path():
     cfg = W.small_config(T=600, d=256, E=16, k=2, f=256, mode=W.GUMBEL, tau=0.5, seed=77)
     inp = to_device(W.make_inputs(cfg, weights_device="cuda"))
+    check_layer(cfg, inp, run_layer(cfg, inp, f16=False))
+
+
+def test_layer_bf16_down_path_token_combine():
+    """fp32 slot rows read by the per-token combine (d = 4096, capacity drops)."""
+    cfg = W.small_config(T=512, d=4096, E=8, k=2, f=128, mode=W.BIAS_SELECT, bias="zipf",
+                         capacity_factor=1.0, seed=78)
+    inp = to_device(W.make_inputs(cfg, weights_device="cuda", zipf_scale=1.5))
     check_layer(cfg, inp, run_layer(cfg, inp, f16=False))
 
 
