@@ -24,9 +24,12 @@
 // x16 (gate/up) or from one more MMA against an all-ones fragment (down): the result is the dequantized weights' (q - z) * s dot product up
 // to the fp32 rounding of the offset (about 1e-4 of it, far below the fp16 rows' rounding). The
 // zero-point subtraction thus leaves the per-code path, which at 4 bits was the limit (the
-// kernel issue-bound below the memory rate). A tcgen05 MMA would need the dequantized
-// tile in shared memory first: 2 more bytes written and read per weight on top of the code, more
-// shared-memory traffic than the SM has at the HBM rate of 1-byte codes.
+// kernel issue-bound below the memory rate). tcgen05 measured slower for this shape: with A in
+// shared memory the dequantized tile costs 2 more bytes written and read per weight, more
+// shared-memory traffic than the SM has at the HBM rate of 1-byte codes; with A in TMEM (codes
+// dequantized in registers, tcgen05.st, an M = 128 N = 16 MMA per 16-deep step) the stores ran at
+// about 48 B per clock per SM and each N = 16 MMA took 60-90 cycles to issue, so the 4-bit decode
+// layer took 0.97 ms against this kernel's 0.52 ms. Register operands skip both.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <algorithm>
