@@ -378,8 +378,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         orow = slot;
         if (a.topk_w != nullptr) gate = a.topk_w[slot];
       }
-      if (!ptx::mbar_wait_bounded(tfull_bar(acc), acc_phase, abort_flag, a.status,
-                                  MOE_DEVFAULT_PIPELINE_TIMEOUT, kWaitLimitNs))
+      if (!ptx::mbar_wait_bounded_warp(tfull_bar(acc), acc_phase, abort_flag, a.status,
+                                       MOE_DEVFAULT_PIPELINE_TIMEOUT, kWaitLimitNs))
         break;
       ptx::tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN);
@@ -595,8 +595,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         orow = slot;
         if (a.topk_w != nullptr) gate = a.topk_w[slot];
       }
-      if (!ptx::mbar_wait_bounded(tfull_bar(acc), acc_phase, abort_flag, a.status,
-                                  MOE_DEVFAULT_PIPELINE_TIMEOUT, kWaitLimitNs))
+      if (!ptx::mbar_wait_bounded_warp(tfull_bar(acc), acc_phase, abort_flag, a.status,
+                                       MOE_DEVFAULT_PIPELINE_TIMEOUT, kWaitLimitNs))
         break;
       ptx::tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN);

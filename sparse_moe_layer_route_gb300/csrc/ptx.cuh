@@ -83,6 +83,15 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
   }
 }
 
+// The same wait by every lane of a warp that goes on to warp-collective (.sync.aligned) work:
+// the warp proceeds only when all of its lanes saw the phase, so it never splits on a timeout.
+__device__ __forceinline__ bool mbar_wait_bounded_warp(uint32_t bar, uint32_t parity,
+                                                       volatile int* abort_flag, int* status,
+                                                       int fault_bit, uint64_t limit_ns) {
+  const bool got = mbar_wait_bounded(bar, parity, abort_flag, status, fault_bit, limit_ns);
+  return __all_sync(0xffffffffu, got);
+}
+
 // ---------------------------------------------------------------------------- TMA
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");

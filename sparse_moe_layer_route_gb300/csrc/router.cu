@@ -223,8 +223,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint32_t acc_phase = 0;
     bool ok = true;
     for (int kb = kb0; kb < kb1; ++kb) {
-      if (!ptx::mbar_wait_bounded(afull_bar(acc), acc_phase, abort_flag, status,
-                                  MOE_DEVFAULT_PIPELINE_TIMEOUT, kWaitLimitNs)) {
+      if (!ptx::mbar_wait_bounded_warp(afull_bar(acc), acc_phase, abort_flag, status,
+                                       MOE_DEVFAULT_PIPELINE_TIMEOUT, kWaitLimitNs)) {
         ok = false;
         break;
       }
