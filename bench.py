@@ -175,8 +175,9 @@ def layer_roofline(cfg, n_touched, n_kept, t_layer_s, peaks):
             "frac_alg": t_alg / t_layer_s}
 
 
-def kernel_work(cfg, phase, n_touched, n_kept):
-    """Algorithmic (flops, bytes) of one launch of a phase, from the config and the routing."""
+def kernel_work(cfg, phase, n_touched, n_kept, n_tok_kept=None):
+    """Algorithmic (flops, bytes) of one launch of a phase, from the config and the routing.
+    n_tok_kept: tokens with at least one kept slot (all T when None)."""
     d, f, E, T, k, S = cfg.d, cfg.f, cfg.E, cfg.T, cfg.k, cfg.S
     rows = n_kept + S * T
     ne = n_touched + S
@@ -190,9 +191,11 @@ def kernel_work(cfg, phase, n_touched, n_kept):
     if phase == "combine":
         return 0.0, (n_kept + S * T) * d * 2.0 + T * d * 2.0 + T * k * 4.0
     if phase == "tiles_gather":
-        # gathered rows written once; x read once from DRAM (repeat reads of a token's row hit
-        # L2)
-        return 0.0, n_kept * d * 2.0 + T * d * 2.0
+        # gathered rows written once; the x row of every token with a kept slot read once from
+        # DRAM (repeat reads of a token's row hit L2; tokens whose slots were all dropped are
+        # not read)
+        n_tok = T if n_tok_kept is None else n_tok_kept
+        return 0.0, n_kept * d * 2.0 + n_tok * d * 2.0
     if phase == "dispatch":
         return 0.0, T * k * 4.0 * 4
     return 0.0, 0.0
@@ -408,23 +411,29 @@ def phase_times(M, mc, weights, inp, out, ro, ws, flush, n):
             for j, ph in enumerate(M.PROFILE_PHASES)}
 
 
-def workload_report(cfg, ms, phase_ms, counts_h, peaks, peak_src):
+def tokens_with_kept_slot(slot_pos, T, k):
+    """Tokens at least one of whose k slots was kept (slot_pos >= 0)."""
+    return int((slot_pos.view(T, k) >= 0).any(dim=1).sum().item())
+
+
+def workload_report(cfg, ms, phase_ms, counts_h, peaks, peak_src, n_tok_kept=None):
     """Layer roofline, the dominant kernel's roofline, per-phase fractions and routing figures."""
     C = M_capacity(cfg)
     n_touched, n_kept = touched_experts(counts_h, C)
     lr = layer_roofline(cfg, n_touched, n_kept, ms / 1e3, peaks)
     dom = max(phase_ms, key=phase_ms.get)
-    fl, by = kernel_work(cfg, dom, n_touched, n_kept)
+    fl, by = kernel_work(cfg, dom, n_touched, n_kept, n_tok_kept)
     roof = roofline_for(dom, fl, by, phase_ms[dom] / 1e3, peaks)
     roof["kernel"] = dom
     roof["traffic"] = ncu_traffic(cfg, dom, by)
     roof["peak_source"] = f"{peak_src} ({'bf16 burst' if roof['unit'] == 'TFLOP/s' else 'copy'})"
     kernels = {}
     for ph, t in phase_ms.items():
-        f_, b_ = kernel_work(cfg, ph, n_touched, n_kept)
+        f_, b_ = kernel_work(cfg, ph, n_touched, n_kept, n_tok_kept)
         r = roofline_for(ph, f_, b_, t / 1e3, peaks) if t > 0 else {}
         kernels[ph] = {"us": t * 1e3, **{kk: r[kk] for kk in ("bound", "frac") if kk in r}}
-    routing = {"experts_hit": n_touched, "kept_slots": n_kept, "capacity": C,
+    routing = {"experts_hit": n_touched, "kept_slots": n_kept, "tokens_kept": n_tok_kept,
+               "capacity": C,
                "dropped_slots": cfg.T * cfg.k - n_kept, "max_load": max(counts_h),
                "mean_load": cfg.T * cfg.k / cfg.E}
     return lr, roof, kernels, routing
@@ -461,7 +470,8 @@ def measure_other(M, W, name, dev, steps, warmup, peaks, peak_src, local):
         raise SystemExit(f"device fault bits {faults:#x} in workload {name}")
     ms = sum(step_ms) / len(step_ms)
     lr, roof, kernels, routing = workload_report(cfg, ms, phase_ms, counts.cpu().tolist(), peaks,
-                                                 peak_src)
+                                                 peak_src,
+                                                 tokens_with_kept_slot(slot_pos, cfg.T, cfg.k))
     del inp, weights, keep, ws, flush
     return {"workload": cfg.name + ": " + cfg.description, "value": cfg.T / (ms / 1e3),
             "unit": "tokens/s", "ms_per_step": ms, "ms_per_step_median": statistics.median(step_ms),
@@ -633,7 +643,7 @@ def main():
         loop_dev_ms = max_over_ranks([loop_dev_ms], dist, dev)[0]
 
     lr, roof, kernels, routing = workload_report(cfg, ms, phase_ms, counts.cpu().tolist(), peaks,
-                                                 peak_src)
+                                                 peak_src, tokens_with_kept_slot(slot_pos, T, k))
     # ---- the oracle on the host cores, on a bounded sample of the same workload
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
