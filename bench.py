@@ -207,8 +207,12 @@ def roofline_for(phase, flops, nbytes, secs, peaks):
         ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
         if flops / max(nbytes, 1.0) >= ridge:
             ach = flops / secs / 1e12
-            return {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"],
-                    "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"]}
+            r = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"],
+                 "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"]}
+            # beside the burst figure: the power-capped rate a seconds-long GEMM loop settles at
+            if peaks.get("bf16_tflops_sustained"):
+                r["frac_of_sustained"] = ach / peaks["bf16_tflops_sustained"]
+            return r
     ach = nbytes / secs / 1e9
     return {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": ach / peaks["hbm_gbs"]}
@@ -431,7 +435,8 @@ def workload_report(cfg, ms, phase_ms, counts_h, peaks, peak_src, n_tok_kept=Non
     for ph, t in phase_ms.items():
         f_, b_ = kernel_work(cfg, ph, n_touched, n_kept, n_tok_kept)
         r = roofline_for(ph, f_, b_, t / 1e3, peaks) if t > 0 else {}
-        kernels[ph] = {"us": t * 1e3, **{kk: r[kk] for kk in ("bound", "frac") if kk in r}}
+        kernels[ph] = {"us": t * 1e3, **{kk: r[kk] for kk in ("bound", "frac", "frac_of_sustained")
+                                         if kk in r}}
     routing = {"experts_hit": n_touched, "kept_slots": n_kept, "tokens_kept": n_tok_kept,
                "capacity": C,
                "dropped_slots": cfg.T * cfg.k - n_kept, "max_load": max(counts_h),
