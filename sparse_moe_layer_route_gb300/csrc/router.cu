@@ -330,6 +330,52 @@ __device__ __forceinline__ float key_score(uint32_t k) {
 // the smallest expert index among the lanes holding that key; the owner marks it taken.
 // M >= m is the compiled bound on experts per lane (1, 2, 4 or 8): the per-expert loops are
 // unrolled to M rather than to the largest supported E, so small E runs no predicated-off work.
+// v[i] = p[i] for i < n (else 0): one or M / 4 vector loads when the whole run is there and
+// aligned, scalar loads otherwise.
+template <int M>
+__device__ __forceinline__ void load_run(const float* p, int n, float (&v)[M]) {
+  constexpr int VB = M % 4 == 0 ? 16 : (M == 2 ? 8 : 0);  // vector bytes
+  if (VB != 0 && n == M && (reinterpret_cast<uintptr_t>(p) % VB) == 0) {
+    if (M == 2) {
+      const float2 f = __ldg(reinterpret_cast<const float2*>(p));
+      v[0] = f.x;
+      v[M - 1] = f.y;
+    } else {
+#pragma unroll
+      for (int c = 0; c < M / 4; ++c) {
+        const float4 f = __ldg(reinterpret_cast<const float4*>(p) + c);
+        v[4 * c] = f.x;
+        v[4 * c + 1] = f.y;
+        v[4 * c + 2] = f.z;
+        v[4 * c + 3] = f.w;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < M; ++i) v[i] = i < n ? __ldg(p + i) : 0.f;
+  }
+}
+
+// p[i] = v[i] for i < n, the same way.
+template <int M>
+__device__ __forceinline__ void store_run(float* p, int n, const float (&v)[M]) {
+  constexpr int VB = M % 4 == 0 ? 16 : (M == 2 ? 8 : 0);
+  if (VB != 0 && n == M && (reinterpret_cast<uintptr_t>(p) % VB) == 0) {
+    if (M == 2) {
+      *reinterpret_cast<float2*>(p) = make_float2(v[0], v[M - 1]);
+    } else {
+#pragma unroll
+      for (int c = 0; c < M / 4; ++c)
+        reinterpret_cast<float4*>(p)[c] =
+            make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < M; ++i)
+      if (i < n) p[i] = v[i];
+  }
+}
+
 template <int M>
 __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a) {
   static_assert(M >= 1 && M <= kSelMaxPerLane, "experts per lane");
@@ -345,25 +391,75 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a)
   float sc[M];
   uint32_t key[M];
   float maxabs = 0.f;
+  // this lane's logits: the slices added in slice order; when the lane holds exactly M experts
+  // (e0 = lane * M, 4 M-byte aligned) each slice comes in M / 4 float4 (or one float2) loads
+  float lg[M];
+  {
+    const float* p = a.part + (size_t)t * a.EP + e0;
+    const size_t stride = (size_t)a.T * a.EP;
+    if (m == M && (M == 2 || M % 4 == 0)) {
+      // every slice's load issued before the first add
+      float v[8][M];
+#pragma unroll
+      for (int sp = 0; sp < 8; ++sp) {
+        const float* q = p + sp * stride;
+        if (M == 2) {
+          const float2 f = sp < a.splits ? __ldg(reinterpret_cast<const float2*>(q))
+                                         : make_float2(0.f, 0.f);
+          v[sp][0] = f.x;
+          v[sp][M - 1] = f.y;
+        } else {
+#pragma unroll
+          for (int c = 0; c < M / 4; ++c) {
+            const float4 f = sp < a.splits ? __ldg(reinterpret_cast<const float4*>(q) + c)
+                                           : make_float4(0.f, 0.f, 0.f, 0.f);
+            v[sp][4 * c] = f.x;
+            v[sp][4 * c + 1] = f.y;
+            v[sp][4 * c + 2] = f.z;
+            v[sp][4 * c + 3] = f.w;
+          }
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < M; ++i) {
+        lg[i] = v[0][i];
+#pragma unroll
+        for (int sp = 1; sp < 8; ++sp)
+          if (sp < a.splits) lg[i] += v[sp][i];
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < M; ++i) {
+        lg[i] = 0.f;
+        if (i < m && e0 + i < a.E) {
+          float v[8];
+#pragma unroll
+          for (int sp = 0; sp < 8; ++sp)
+            v[sp] = sp < a.splits ? __ldg(p + i + sp * stride) : 0.f;
+          float l = v[0];
+#pragma unroll
+          for (int sp = 1; sp < 8; ++sp)
+            if (sp < a.splits) l += v[sp];
+          lg[i] = l;
+        }
+      }
+    }
+  }
+  // this lane's experts [e0, e0 + nv) and their bias or Gumbel draws
+  const int nv = max(0, min(m, a.E - e0));
+  float bv[M], uv[M];
+#pragma unroll
+  for (int i = 0; i < M; ++i) bv[i] = uv[i] = 0.f;
+  if (a.mode == MOE_ROUTE_BIAS_SELECT) load_run<M>(a.bias + e0, nv, bv);
+  if (gumbel) load_run<M>(a.u + (size_t)t * a.E + e0, nv, uv);
 #pragma unroll
   for (int i = 0; i < M; ++i) {
     sc[i] = -INFINITY;
     key[i] = 0u;
-    const int e = e0 + i;
-    if (i < m && e < a.E) {
-      // at most 8 slices: every load issued before the sum, which runs in slice order
-      const float* p = a.part + (size_t)t * a.EP + e;
-      const size_t stride = (size_t)a.T * a.EP;
-      float v[8];
-#pragma unroll
-      for (int sp = 0; sp < 8; ++sp) v[sp] = sp < a.splits ? __ldg(p + sp * stride) : 0.f;
-      float l = v[0];
-#pragma unroll
-      for (int sp = 1; sp < 8; ++sp)
-        if (sp < a.splits) l += v[sp];
+    if (i < nv) {
+      const float l = lg[i];
       maxabs = fmaxf(maxabs, fabsf(l));
-      sc[i] = selection_score(a.mode, l, a.mode == MOE_ROUTE_BIAS_SELECT ? __ldg(a.bias + e) : 0.f,
-                              gumbel ? __ldg(a.u + (size_t)t * a.E + e) : 0.f, a.tau);
+      sc[i] = selection_score(a.mode, l, bv[i], uv[i], a.tau);
       key[i] = score_key(sc[i]);
     }
   }
@@ -371,9 +467,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a)
   maxabs = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(maxabs)));
   if (a.sfull != nullptr) {
     // the overflow re-route ranks every expert of a token: keep the scores and the row scale
-#pragma unroll
-    for (int i = 0; i < M; ++i)
-      if (i < m && e0 + i < a.E) a.sfull[(size_t)t * a.E + e0 + i] = sc[i];
+    store_run<M>(a.sfull + (size_t)t * a.E + e0, nv, sc);
     if (lane == 0) a.maxl_out[t] = maxabs;
   }
   float gmarg = INFINITY;
@@ -404,11 +498,11 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a)
     bk = 0u;
     be = INT_MAX;
 #pragma unroll
-    for (int i = 0; i < M; ++i)
-      if (i < m && key[i] > bk) {
-        bk = key[i];
-        be = e0 + i;
-      }
+    for (int i = 0; i < M; ++i) {
+      const bool better = i < m && key[i] > bk;
+      bk = better ? key[i] : bk;
+      be = better ? e0 + i : be;
+    }
   };
   uint32_t bk;
   int be;
@@ -420,24 +514,19 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a)
   int my_e = 0;
 #pragma unroll
   for (int j = 0; j < kList; ++j) {
-    if (j < nl) {
-      const uint32_t K = __reduce_max_sync(0xffffffffu, bk);
-      const int W = (int)__reduce_min_sync(0xffffffffu, bk == K ? (uint32_t)be : 0xffffffffu);
-      const float s_j = key_score(K);
-      if (lane == j) {
-        my_s = s_j;
-        my_e = W;
-      }
-      if (j > 0) min_gap = fminf(min_gap, prev - s_j);
-      if (j == k - 1) sk = s_j;
-      prev = s_j;
-      if (W >= e0 && W < e0 + m) {
+    if (j >= nl) break;  // uniform over the warp
+    const uint32_t K = __reduce_max_sync(0xffffffffu, bk);
+    const int W = (int)__reduce_min_sync(0xffffffffu, bk == K ? (uint32_t)be : 0xffffffffu);
+    const float s_j = key_score(K);
+    my_s = lane == j ? s_j : my_s;
+    my_e = lane == j ? W : my_e;
+    if (j > 0) min_gap = fminf(min_gap, prev - s_j);
+    if (j == k - 1) sk = s_j;
+    prev = s_j;
+    // every lane drops the pick (only its owner holds it) and rescans: no divergent branch
 #pragma unroll
-        for (int i = 0; i < M; ++i)
-          if (e0 + i == W) key[i] = 0u;
-        lane_best(bk, be);
-      }
-    }
+    for (int i = 0; i < M; ++i) key[i] = e0 + i == W ? 0u : key[i];
+    lane_best(bk, be);
   }
   // near-tie test (scores in their own units: GUMBEL scores carry 1/tau)
   float band = router_band(a.d, maxabs);
