@@ -24,6 +24,9 @@ CASES = [  # T, d, E, k, mode, bias
     (333, 256, 33, 3, W.BIAS_SELECT, "normal"),
     (250, 256, 96, 4, W.GUMBEL, "zero"),
     (130, 192, 200, 7, W.BIAS_SELECT, "zipf"),
+    # Gumbel draws of E = 33 per row: every other token's row starts off an 8-byte boundary, so
+    # the selection's two-float runs of u alternate between vector and scalar loads
+    (201, 128, 33, 2, W.GUMBEL, "zero"),
 ]
 
 
@@ -189,3 +192,41 @@ def test_route_zero_columns_tie_lowest_index():
     assert (same | inexact).all(), np.nonzero(~(same | inexact))[0][:10]
     zero_picked = np.isin(r["topk_idx"], (2, 5, 6, 11)).sum(1)
     assert (zero_picked >= 2).sum() > 20       # zero-score ties were really decided
+
+
+def test_route_unaligned_bias_and_noise_same_bits():
+    """The selection loads a lane's run of biases (or Gumbel draws) as vectors when the run is
+    whole and aligned, else element by element. Views one float off their allocation's alignment
+    must give the same bits as aligned copies, and the oracle's selection."""
+    for mode, E, bias_kind in ((W.BIAS_SELECT, 128, "normal"), (W.GUMBEL, 64, "zero")):
+        cfg = W.small_config(T=300, d=256, E=E, k=2, f=64, mode=mode,
+                             tau=0.5 if mode == W.GUMBEL else 1.0, seed=61 + E, bias=bias_kind,
+                             bias_var=0.1)
+        inp = W.make_routing_inputs(cfg)
+        idx, w = run_route(cfg, inp)
+        # device copies one float past a 256-byte-aligned allocation
+        dev = {"bias": torch.cat([torch.zeros(1), inp["bias"]]).cuda()[1:]}
+        if inp["u"] is not None:
+            dev["u"] = torch.cat([torch.zeros(1), inp["u"].reshape(-1)]).cuda()[1:].view(cfg.T, E)
+        assert dev["bias"].data_ptr() % 16 == 4
+        idx_s, w_s = run_route_device(cfg, inp, dev)
+        assert np.array_equal(idx_s, idx)
+        assert np.array_equal(w_s.view(np.uint32), w.view(np.uint32))
+        r = oracle_for(cfg, inp)
+        exempt = r["margin"] < O.TIE_MARGIN
+        assert not ((idx_s != r["topk_idx"]).any(1) & ~exempt).any()
+
+
+def run_route_device(cfg, inp, dev_bias_u):
+    """run_route with the bias and Gumbel draws given as (possibly offset) device views."""
+    mc = M.MoeConfig.from_layer(cfg)
+    dev = "cuda"
+    x = inp["x"].to(dev)
+    W_g = inp["W_g"].to(dev)
+    idx = torch.full((cfg.T, cfg.k), -1, dtype=torch.int32, device=dev)
+    w = torch.full((cfg.T, cfg.k), float("nan"), dtype=torch.float32, device=dev)
+    ws = M.alloc_workspace(mc)
+    M.route(mc, x, W_g, dev_bias_u["bias"], dev_bias_u.get("u"), idx, w, ws)
+    assert M.device_status(ws) == 0
+    return idx.cpu().numpy(), w.cpu().numpy()
+
