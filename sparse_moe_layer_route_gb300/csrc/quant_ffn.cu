@@ -21,7 +21,8 @@
 // m16n8k16 as the A operand straight from registers (weights as the M side, up to 8 tokens as
 // N); every product is exact and the sums are fp32. Per 128-row group the constant is removed
 // once, (1024 + z) * sum(b), and the group's fp32 scale applied; sum(b) comes precomputed with
-// x16 (gate/up) or from one more MMA against an all-ones fragment (down): the result is the dequantized weights' (q - z) * s dot product up
+// x16 (gate/up), or in the down pass from one more MMA against an all-ones fragment (8-bit) or
+// fp32 adds of the lane's own H values (4-bit): the result is the dequantized weights' (q - z) * s dot product up
 // to the fp32 rounding of the offset (about 1e-4 of it, far below the fp16 rows' rounding). The
 // zero-point subtraction thus leaves the per-code path, which at 4 bits was the limit (the
 // kernel issue-bound below the memory rate). tcgen05 measured slower for this shape: with A in
@@ -266,8 +267,10 @@ __device__ __forceinline__ void load_group_q(GroupQ<NM, TL>& q, const QMat* mats
 }
 
 // The group's activation sum per token 2c + j (this lane's accumulator columns): M = 0 takes it
-// from sb_in (precomputed by act_prep_kernel), M = 1 forms it with one more MMA per step against
-// an all-ones A fragment.
+// from sb_in (precomputed by act_prep_kernel); M = 1 forms it from the B fragments themselves, at
+// 8 bits with one more MMA per step against an all-ones A fragment, at 4 bits (where the MMAs per
+// code byte double) by fp32 adds of the lane's H values and three shuffles (measured: 4-bit down
+// 192.5 -> 188.4 us on the decode shape, while the adds cost the 8-bit pass 12 us).
 template <int BITS, int MODE, int NM, int TL, int NL>
 __device__ __forceinline__ void compute_group(const uint4 (&code)[NM][TL][NL],
                                               const uint32_t (&bq)[8][2],
@@ -280,13 +283,23 @@ __device__ __forceinline__ void compute_group(const uint4 (&code)[NM][TL][NL],
     for (int t = 0; t < TL; ++t)
 #pragma unroll
       for (int i = 0; i < 4; ++i) cg[m][t][i] = 0.f;
+  constexpr bool kAddSums = MODE == 1 && BITS == 4;
   float sb[4] = {sb_in[0], sb_in[1], 0.f, 0.f};
   if (MODE == 1) sb[0] = sb[1] = 0.f;
   const uint32_t ones[4] = {0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u};  // fp16 1.0
+  // 4-bit M = 1: this lane's share of token g's group sum (k = 2c, 2c + 1, 2c + 8, 2c + 9 of
+  // every step)
+  float part = 0.f;
 #pragma unroll
   for (int st = 0; st < 8; ++st) {
     const uint32_t b0 = bq[st][0], b1 = bq[st][1];
-    if (MODE == 1) mma16816(sb, ones, b0, b1);
+    if (kAddSums) {
+      const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&b0));
+      const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&b1));
+      part += (f0.x + f0.y) + (f1.x + f1.y);
+    } else if (MODE == 1) {
+      mma16816(sb, ones, b0, b1);
+    }
 #pragma unroll
     for (int m = 0; m < NM; ++m)
 #pragma unroll
@@ -303,6 +316,14 @@ __device__ __forceinline__ void compute_group(const uint4 (&code)[NM][TL][NL],
         }
         mma16816(cg[m][t], af, b0, b1);
       }
+  }
+  if (kAddSums) {
+    // the four lanes of token g add their shares; each lane then takes tokens 2c and 2c + 1
+    part += __shfl_xor_sync(0xffffffffu, part, 1);
+    part += __shfl_xor_sync(0xffffffffu, part, 2);
+    const int c = threadIdx.x & 3;
+    sb[0] = __shfl_sync(0xffffffffu, part, 8 * c);
+    sb[1] = __shfl_sync(0xffffffffu, part, 8 * c + 4);
   }
   // element i: row n + 8 (i / 2) of the tile, token 2c + i % 2
 #pragma unroll
