@@ -132,6 +132,16 @@ struct QArgs {
   int E, K, N, top_k;
 };
 
+// The activations the passes read as MMA B operands (x16, H) are kept in fragment order inside
+// every 128-column group: column 16 s + j of the group (step s, j < 16) sits at
+//   32 p + 4 s + 2 w + e,   p = (j % 8) / 2, w = j / 8, e = j % 2,
+// so the 32 values lane c of a token's quad needs for the group's eight steps (k = 16 s + 2c,
+// 2c + 1, 2c + 8, 2c + 9) are 64 contiguous bytes, four 16-byte loads.
+__host__ __device__ constexpr int frag_pos(int col) {
+  return (col & ~127) + ((col & 7) >> 1) * 32 + ((col & 127) >> 4) * 4 + ((col >> 3) & 1) * 2 +
+         (col & 1);
+}
+
 // x16[t, :] = fp16(x[t, :]) (round to nearest, as the MMA operand takes it) and
 // sbx[t, g] = the fp32 sum of x16[t, 128 g : 128 g + 128]: each lane adds its 8 values in column
 // order, then 16 lanes combine by a fixed tree. One warp per (token, 256 columns): two groups.
@@ -157,8 +167,11 @@ __global__ void __launch_bounds__(256) act_prep_kernel(const uint16_t* __restric
       const uint4 v = src[c];
       const uint4 h = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y),
                                  bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
-      dst[c] = h;
       const uint32_t hw[4] = {h.x, h.y, h.z, h.w};
+      // pair p of the chunk (columns 8 c + 2p, + 1) to its fragment-order place
+      uint32_t* drow = reinterpret_cast<uint32_t*>(dst);
+#pragma unroll
+      for (int p = 0; p < 4; ++p) drow[frag_pos(8 * c + 2 * p) / 2] = hw[p];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hw[i]));
@@ -458,13 +471,20 @@ __global__ void __launch_bounds__(kQThreads, MODE == 0 ? (BITS == 8 ? 4 : 1) : 0
       for (int t = 0; t < TL; ++t)
 #pragma unroll
         for (int i = 0; i < 4; ++i) acc[m][t][i] = 0.f;
-    uint32_t bq[8][2];
+    // the group's B fragments: 64 contiguous bytes per lane in the fragment-order layout
+    auto load_b = [&](int grp, bool ok, uint32_t (&b)[8][2]) {
+      const uint4* p4 = reinterpret_cast<const uint4*>(brow + grp * 64 + c * 16);
 #pragma unroll
-    for (int st = 0; st < 8; ++st) {
-      const int k0 = (gA * 8 + st) * 16;
-      bq[st][0] = tok_ok ? brow[(k0 + 2 * c) / 2] : 0u;
-      bq[st][1] = tok_ok ? brow[(k0 + 2 * c + 8) / 2] : 0u;
-    }
+      for (int q = 0; q < 4; ++q) {
+        const uint4 v = ok ? p4[q] : make_uint4(0u, 0u, 0u, 0u);
+        b[2 * q][0] = v.x;
+        b[2 * q][1] = v.y;
+        b[2 * q + 1][0] = v.z;
+        b[2 * q + 1][1] = v.w;
+      }
+    };
+    uint32_t bq[8][2];
+    load_b(gA, tok_ok, bq);
     GroupQ<NM, TL> gq;
     load_group_q<BITS, NM, TL>(gq, mats, ex_ix, gA, groups, a.N, n, true);
     float sb[2];
@@ -486,13 +506,7 @@ __global__ void __launch_bounds__(kQThreads, MODE == 0 ? (BITS == 8 ? 4 : 1) : 0
             code[m][t][l] = ring4[(((stage * NM + m) * TL + t) * NL + l) * 32 + lane];
       // the next group's activations, scales and zero-points, loaded during this group's MMAs
       uint32_t bn[8][2];
-#pragma unroll
-      for (int st = 0; st < 8; ++st) {
-        const int k0 = ((grp + 1) * 8 + st) * 16;
-        const bool ok = tok_ok && grp + 1 < gB;
-        bn[st][0] = ok ? brow[(k0 + 2 * c) / 2] : 0u;
-        bn[st][1] = ok ? brow[(k0 + 2 * c + 8) / 2] : 0u;
-      }
+      load_b(grp + 1, tok_ok && grp + 1 < gB, bn);
       GroupQ<NM, TL> gn;
       load_group_q<BITS, NM, TL>(gn, mats, ex_ix, grp + 1, groups, a.N, n, grp + 1 < gB);
       float sbn[2];
@@ -562,7 +576,8 @@ __global__ void __launch_bounds__(kQThreads, MODE == 0 ? (BITS == 8 ? 4 : 1) : 0
           v = gate * acc[0][t][i];
         }
         clamp = max(clamp, mag_bits(v));
-        a.out[orow * a.N + col] = f16_sat(v);
+        // H (M = 0) in fragment order for the down pass; Y (M = 1) in plain column order
+        a.out[orow * a.N + (MODE == 0 ? frag_pos(col) : col)] = f16_sat(v);
       }
     }
   }
