@@ -352,10 +352,12 @@ __device__ __forceinline__ void compute_group(const uint4 (&code)[NM][TL][NL],
 }
 
 // 16-column tiles per work unit: 4-bit groups carry half the bytes of 8-bit ones, so a 4-bit
-// unit takes two tiles to give each group the same code bytes and twice the MMAs per activation.
-template <int BITS>
+// unit takes two tiles (gate/up, two matrices) or four (down) to give each group at least the same
+// code bytes, and its B fragments serve more MMAs (4-bit down with four tiles: 157.7 -> 147.5 us
+// on the decode shape; the 8-bit down pass with two measured slower).
+template <int BITS, int MODE>
 __host__ __device__ constexpr int tiles_per_unit() {
-  return BITS == 8 ? 1 : 2;
+  return BITS == 8 ? 1 : (MODE == 0 ? 2 : 4);
 }
 
 template <int NM, int TL, int NL>
@@ -377,7 +379,7 @@ __global__ void __launch_bounds__(kQThreads, MODE == 0 ? (BITS == 8 ? 4 : 1) : 0
     qffn_kernel(const QArgs a) {
   constexpr int NM = MODE == 0 ? 2 : 1;  // matrices per unit (gate and up, or down)
   constexpr int NL = BITS == 8 ? 4 : 2;  // 512-byte code blocks per group, matrix and tile
-  constexpr int TL = tiles_per_unit<BITS>();
+  constexpr int TL = tiles_per_unit<BITS, MODE>();
   constexpr int RB = ring_bytes_per_warp<NM, TL, NL>();
   extern __shared__ __align__(16) uint8_t qsmem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -628,10 +630,11 @@ cudaError_t launch_quant_ffn(const Shape& s, int bits, const QFfnPtrs& p, cudaSt
   const int sms = num_sms();
   // persistent: as many CTAs as fit (work units come from the counters in Meta)
   auto smem_of = [&](int mode) {
-    const int rb = bits == 8 ? (mode == 0 ? ring_bytes_per_warp<2, tiles_per_unit<8>(), 4>()
-                                          : ring_bytes_per_warp<1, tiles_per_unit<8>(), 4>())
-                             : (mode == 0 ? ring_bytes_per_warp<2, tiles_per_unit<4>(), 2>()
-                                          : ring_bytes_per_warp<1, tiles_per_unit<4>(), 2>());
+    const int rb =
+        bits == 8 ? (mode == 0 ? ring_bytes_per_warp<2, tiles_per_unit<8, 0>(), 4>()
+                               : ring_bytes_per_warp<1, tiles_per_unit<8, 1>(), 4>())
+                  : (mode == 0 ? ring_bytes_per_warp<2, tiles_per_unit<4, 0>(), 2>()
+                               : ring_bytes_per_warp<1, tiles_per_unit<4, 1>(), 2>());
     return (size_t)(kQThreads / 32) * rb;
   };
   auto grid_of = [&](void (*k)(const QArgs), size_t smem) {
