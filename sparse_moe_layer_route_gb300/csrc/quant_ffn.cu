@@ -22,8 +22,10 @@
 // N); every product is exact and the sums are fp32. Per 128-row group the constant is removed
 // once, (1024 + z) * sum(b), and the group's fp32 scale applied; sum(b) comes precomputed with
 // x16 (gate/up), or in the down pass from one more MMA against an all-ones fragment (8-bit) or
-// fp32 adds of the lane's own H values (4-bit): the result is the dequantized weights' (q - z) * s dot product up
-// to the fp32 rounding of the offset (about 1e-4 of it, far below the fp16 rows' rounding). The
+// fp32 adds of the lane's own H values (4-bit). The result is the dequantized weights'
+// (q - z) * s dot product up to the fp32 rounding of the offset (about 1e-4 of it, far below the
+// fp16 rows' rounding). x16 and H are stored in fragment order (frag_pos), so a lane reads its B
+// operands of a group in four 16-byte loads. The
 // zero-point subtraction thus leaves the per-code path, which at 4 bits was the limit (the
 // kernel issue-bound below the memory rate). tcgen05 measured slower for this shape: with A in
 // shared memory the dequantized tile costs 2 more bytes written and read per weight, more
